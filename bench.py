@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark of the USP-Attention forward hot path on GB300 (one JSON line on stdout, rank 0).
+
+A step is one pass of the whole hot path over one batch of the workload: for every head group, the
+zigzag split of Q, K, V (a1), AllToAll4D (a2), ring attention with the LSE merge (a3 + a4) and the
+inverse AllToAll4D of out and lse (a5). ``value`` is the causal-adjusted attention FLOPs of the step
+(2 * bs * hq * L^2 * hd) divided by the step time, in TFLOP/s, aggregated over all ranks (each rank
+runs an independent replica: the virtual-rank grid lives inside one device, nothing is exchanged).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from seeded_inputs import WORKLOADS, default_seed, make_rows, make_workload_qkv  # noqa: E402
+
+DEFAULT_WORKLOAD = 1
+L2_BYTES = 129 * 10 ** 6
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.json")
+ATTN_SRC = os.path.join(ROOT, "sequence_long_context_zigzag_gb300", "csrc", "attn_tc.cu")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle baseline")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (barrier and max over ranks only; no data-path collective)
+# ------------------------------------------------------------------------------------------------
+class Dist:
+    def __init__(self, backend=None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend or ("nccl" if torch.cuda.is_available() else "gloo"))
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            if torch.cuda.is_available() and self.pg.get_backend() == "nccl":
+                self.pg.barrier(device_ids=[torch.cuda.current_device()])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return FALLBACK, "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = None
+        self.idx = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.idx)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ------------------------------------------------------------------------------------------------
+# the step
+# ------------------------------------------------------------------------------------------------
+class Step:
+    """Preallocated buffers and the ABI calls of one step (no allocation inside the timed loop)."""
+
+    def __init__(self, usp, w, q, k, v):
+        self.usp, self.w = usp, w
+        self.q, self.k, self.v = q, k, v
+        rd, ud, bs, L, hd = w.rd, w.ud, w.bs, w.L, w.hd
+        hc = w.head_chunk or w.hq
+        G = w.hq // w.hkv
+        hkc = hc // G
+        Lu, Lr = L // (rd * ud), L // rd
+        dev, dt = q.device, q.dtype
+        self.groups = [(g0, g0 // G) for g0 in range(0, w.hq, hc)]
+        self.hc, self.hkc = hc, hkc
+        self.ql = torch.empty(rd, ud, bs, Lu, hc, hd, device=dev, dtype=dt)
+        self.kl = torch.empty(rd, ud, bs, Lu, hkc, hd, device=dev, dtype=dt)
+        self.vl = torch.empty_like(self.kl)
+        self.qh = torch.empty(rd, ud, hc // ud, bs, Lr, hd, device=dev, dtype=dt)
+        self.kh = torch.empty(rd, ud, hkc // ud, bs, Lr, hd, device=dev, dtype=dt)
+        self.vh = torch.empty_like(self.kh)
+        self.oh = torch.empty_like(self.qh)
+        self.lh = torch.empty(rd, ud, hc // ud, bs, Lr, device=dev, dtype=torch.float32)
+        self.o_loc = torch.empty(rd, ud, bs, Lu, w.hq, hd, device=dev, dtype=dt)
+        self.l_loc = torch.empty(rd, ud, bs, Lu, w.hq, device=dev, dtype=torch.float32)
+        es = q.element_size()
+        # algorithmic permute bytes per step: one read + one write of every moved tensor
+        tok = bs * L
+        self.permute_bytes = 2 * (2 * tok * (hc + 2 * hkc) * hd * es + tok * hc * (hd * es + 4)) * len(self.groups)
+        self.launches_per_step = 9 * len(self.groups)
+        self.attn_events = []
+        self.perm_events = []
+
+    def run(self, record=False):
+        usp, w = self.usp, self.w
+        rd, ud = w.rd, w.ud
+        st = torch.cuda.current_stream()
+        for g0, gk in self.groups:
+            if record:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+            usp.usp_extract_local(self.q, self.ql, rd, ud, h0=g0, H=self.hc)
+            usp.usp_extract_local(self.k, self.kl, rd, ud, h0=gk, H=self.hkc)
+            usp.usp_extract_local(self.v, self.vl, rd, ud, h0=gk, H=self.hkc)
+            usp.usp_a2a4d(self.ql, self.qh, rd, ud, 1)
+            usp.usp_a2a4d(self.kl, self.kh, rd, ud, 1)
+            usp.usp_a2a4d(self.vl, self.vh, rd, ud, 1)
+            if record:
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record(st)
+            usp.usp_attn_fwd(self.qh, self.kh, self.vh, self.oh, self.lh, causal=w.causal)
+            if record:
+                e2 = torch.cuda.Event(enable_timing=True)
+                e2.record(st)
+            usp.usp_a2a4d(self.oh, self.o_loc, rd, ud, -1, h0=g0, H=self.hc)
+            usp.usp_a2a4d(self.lh, self.l_loc, rd, ud, -1, h0=g0, H=self.hc)
+            if record:
+                e3 = torch.cuda.Event(enable_timing=True)
+                e3.record(st)
+                self.attn_events.append((e1, e2))
+                self.perm_events.append((e0, e1, e2, e3))
+
+
+def traffic_for_current_kernel():
+    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on the
+    attention kernel source as it is now (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        with open(ATTN_SRC, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+    except (OSError, ValueError):
+        return None
+    if rec.get("attn_src_sha256_16") != h:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------------------------
+# the oracle on the host cores (the CPU baseline, and the reference arm)
+# ------------------------------------------------------------------------------------------------
+def oracle_rows_flops(w, rows):
+    """Causal FLOPs of the selected query rows for every head: 4 hd (i + 1) per (row, head)."""
+    n = sum((int(i) + 1) if w.causal else w.L for i in rows)
+    return 4.0 * w.hd * n * w.hq * w.bs
+
+
+def time_oracle(w, q, k, v, target_s, seed):
+    import oracle
+    oracle.build()
+    n = 8
+    rows = make_rows(w.L, w.c, n, seed)[:n]
+    while True:
+        t0 = time.perf_counter()
+        oracle.attn_direct(q, k, v, causal=w.causal, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or len(rows) >= w.L:
+            break
+        grow = max(2.0, min(16.0, target_s / max(dt, 1e-3)))
+        n = min(w.L, int(n * grow) + 1)
+        rows = list(range(0, w.L, max(1, w.L // n)))[:n]
+    flops = oracle_rows_flops(w, rows)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} query rows x {w.hq} heads of {w.name} (fp64 direct attention, "
+                      f"{flops / 1e9:.1f} GFLOP causal-adjusted, {dt:.1f} s)"}
+
+
+def run_reference(args, dist):
+    """The reference arm: the oracle as it stands, timed on this host's cores."""
+    if dist.rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wi = args.workload
+    w = WORKLOADS[wi]
+    q, k, v = make_workload_qkv(w, default_seed(wi))
+    # a fixed bounded sample per step, sized for roughly 2 s of work on this host
+    probe = list(range(w.L // 8, w.L, w.L // 4))[:4]
+    t0 = time.perf_counter()
+    oracle.attn_direct(q, k, v, causal=w.causal, rows=probe)
+    per_row = max((time.perf_counter() - t0) / len(probe), 1e-6)
+    n = max(1, min(w.L, int(2.0 / per_row)))
+    rows = list(range(0, w.L, max(1, w.L // n)))[:n]
+    for _ in range(args.warmup):
+        oracle.attn_direct(q, k, v, causal=w.causal, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attn_direct(q, k, v, causal=w.causal, rows=rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = oracle_rows_flops(w, rows)
+    value = flops / dt / 1e12
+    cb = {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": f"{len(rows)} query rows x {w.hq} heads of {w.name} per step (fp64 direct attention)"}
+    line = {"impl": "reference", "metric": "fwd causal-adjusted attention TFLOP/s (bf16)", "value": value,
+            "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": cb, "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def workload_config(w):
+    return {"workload": w.name, "bs": w.bs, "seq_len": w.L, "hq": w.hq, "hkv": w.hkv, "head_dim": w.hd,
+            "ulysses_degree": w.ud, "ring_degree": w.rd, "head_chunk": w.head_chunk, "causal": w.causal,
+            "parallelism": f"virtual u{w.ud}xr{w.rd} grid on one GPU; replicas across GPUs"}
+
+
+# ------------------------------------------------------------------------------------------------
+def main():
+    args = parse()
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+        dist.close()
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(dist.local_rank)
+    import sequence_long_context_zigzag_gb300 as usp
+
+    wi = args.workload
+    w = WORKLOADS[wi]
+    seed = default_seed(wi)
+    q_h, k_h, v_h = make_workload_qkv(w, seed)
+    q, k, v = q_h.cuda(), k_h.cuda(), v_h.cuda()
+    step = Step(usp, w, q, k, v)
+    flops = w.causal_flops
+    peaks, peak_src = load_peaks()
+
+    for _ in range(args.warmup):
+        step.run()
+    usp.usp_check()
+
+    # ---- device-timed region ----------------------------------------------------------------
+    sampler = ClockSampler(gpu_index(dist.local_rank))
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    st = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(st)
+    for _ in range(args.steps):
+        step.run(record=True)
+    ev1.record(st)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    usp.usp_check()
+    t_step = ev0.elapsed_time(ev1) / 1e3 / args.steps
+    t_step_max = dist.max(t_step)
+    attn_t = [a.elapsed_time(b) / 1e3 for a, b in step.attn_events]
+    perm_t = [(a.elapsed_time(b) + c.elapsed_time(d)) / 1e3 for a, b, c, d in step.perm_events]
+    per_group_flops = flops / len(step.groups)
+    attn_avg = sum(attn_t) / len(attn_t)
+    attn_tflops = per_group_flops / attn_avg / 1e12
+    perm_gbs = step.permute_bytes / (sum(perm_t) / args.steps) / 1e9
+
+    # ---- end to end through the public API, host buffers ------------------------------------
+    qp, kp, vp = (x.pin_memory() for x in (q_h, k_h, v_h))
+    out_h = torch.empty(w.bs, w.L, w.hq, w.hd, dtype=q_h.dtype).pin_memory()
+    lse_h = torch.empty(w.bs, w.L, w.hq, dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp))
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+
+    def e2e_step():
+        qd, kd, vd = (x.to("cuda", non_blocking=True) for x in (qp, kp, vp))
+        o, l = usp.usp_attention(qd, kd, vd, ud=w.ud, rd=w.rd, causal=w.causal, head_chunk=w.head_chunk)
+        out_h.copy_(o, non_blocking=True)
+        lse_h.copy_(l, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    n_e2e = max(1, args.steps // 2)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t_e2e = max(e0.elapsed_time(e1) / 1e3, 0.0) / n_e2e
+    t_e2e = dist.max(max(t_e2e, (time.perf_counter() - t0) / n_e2e))
+    usp.usp_check()
+
+    # ---- CPU baseline (the oracle on the host cores), rank 0 at N = 1 -----------------------
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(w, q_h, k_h, v_h, args.cpu_seconds, seed)
+
+    if dist.rank == 0:
+        peak = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+        hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+        ws_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, step.ql, step.kl, step.vl, step.qh,
+                                                                step.kh, step.vh, step.oh, step.o_loc))
+        line = {
+            "metric": "fwd causal-adjusted attention TFLOP/s (bf16) and % of GB300 dense peak; permute GB/s",
+            "value": dist.world * flops / t_step_max / 1e12,
+            "unit": "TFLOP/s",
+            "n_gpus": dist.world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": t_step_max * 1e3,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32",
+            "data": "synthetic: seeded N(0,1) Q/K/V rounded to bf16",
+            "config": dict(workload_config(w), l2="step working set %.0f MiB > L2 (129 MB); no flush" %
+                           (ws_bytes / 2 ** 20)),
+            "attn_kernel_tflops": attn_tflops,
+            "attn_frac_of_peak": attn_tflops / peak,
+            "permute_gbs": perm_gbs,
+            "permute_frac_of_hbm": perm_gbs / hbm,
+            "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": attn_tflops / peak, "traffic": traffic_for_current_kernel(),
+                         "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)",
+                         "kernel": "usp_attn_fwd (bf16 ring attention)",
+                         "algorithmic_flops_per_launch": per_group_flops},
+            "e2e": {"value": dist.world * flops / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "api": "usp_attention (natural-order output)"},
+            "gpu_launches": step.launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * usp.h -- C ABI of the USP-Attention forward hot path on one GPU (sm_103a).
+ *
+ * USP-Attention ("USP: 统一序列并行方法用于长上下文生成式AI", section 三, Algorithm 1) runs
+ * AllToAll4D over a Ulysses group, ring attention with log-sum-exp merging over a Ring group, and the
+ * inverse AllToAll4D. Here the ud x rd process grid is a set of VIRTUAL ranks inside one device:
+ * every "rank" is an index range of one device buffer, the all-to-all is an on-device permute, and
+ * the ring's point-to-point sends become the order in which KV blocks are fed to the attention
+ * kernel. No call communicates between devices.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are DEVICE pointers unless stated otherwise. The caller owns every buffer; the
+ *    library never allocates caller-visible memory and never frees anything.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream). Argument
+ *    errors are returned before anything is launched. USP_ERR_CUDA reports a launch failure.
+ *  - Device-side waits inside kernels are bounded; a wait that runs out sets a per-device status word
+ *    and the kernel returns early. usp_check() synchronises the stream and reports it as
+ *    USP_ERR_TIMEOUT.
+ *  - Virtual rank (u, r) (Ulysses rank u, ring rank r) has flat id vr = r * ud + u (ring-major; the
+ *    USP review's Tip 7 orders process groups TP -> Ulysses -> Ring from low to high).
+ *  - Notation: c = L / (2 rd) zigzag chunk length, Lr = L / rd ring-local length,
+ *    Lu = L / (rd ud) tokens per virtual rank, Hl = H / ud heads per Ulysses rank.
+ *  - Shapes: L % (2 rd) == 0 and Lr % ud == 0 (equal chunks, as torch.chunk gives in the pages'
+ *    setting); H % ud == 0 for an all-to-all (the Ulysses degree divides the head count, the
+ *    Context-Parallel page's "head 数整除检查"); hq % hkv == 0. Violations return USP_ERR_SHAPE.
+ *  - Sizes: every row count handled by one call must stay below 2^31.
+ */
+#ifndef USP_H
+#define USP_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define USP_API __attribute__((visibility("default")))
+#else
+#define USP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *usp_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    USP_OK = 0,
+    USP_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad enum value */
+    USP_ERR_SHAPE = -2,       /* divisibility rules above */
+    USP_ERR_DTYPE = -3,       /* unknown dtype code */
+    USP_ERR_ALIGN = -4,       /* a pointer is not aligned as the call requires */
+    USP_ERR_UNSUPPORTED = -5, /* valid but not implemented (e.g. head_dim not 64/128) */
+    USP_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
+    USP_ERR_TIMEOUT = -7      /* a bounded device-side wait ran out (reported by usp_check) */
+} usp_status;
+
+typedef enum { USP_F32 = 0, USP_BF16 = 1 } usp_dtype;
+
+/* Shape of one tensor moved by a permute. */
+typedef struct {
+    int64_t bs;      /* batch size */
+    int64_t L;       /* global sequence length */
+    int32_t H;       /* heads moved by this call */
+    int32_t hd;      /* elements per row: the head dim (1 for an lse tensor) */
+    int32_t dtype;   /* usp_dtype: element size 4 (USP_F32) or 2 (USP_BF16) */
+    int32_t rd;      /* ring degree  >= 1 */
+    int32_t ud;      /* Ulysses degree >= 1 */
+    int32_t H_total; /* heads per token in the natural / sequence-sharded tensor (0 means H) */
+    int32_t h0;      /* first head of the window [h0, h0 + H) in that tensor */
+} usp_dims;
+
+/*
+ * usp_extract_local -- the zigzag load-balanced split (step a1).
+ * Source: USP review, section 三, Algorithm 2 (seq.chunk(2 rd); rank r keeps chunks r and
+ * 2 rd - r - 1; then the u-th of ud equal parts); Context-Parallel page, Fig. 2.
+ *
+ *   natural  : (bs, L, H_total, hd) row-major, natural token order; the call reads/writes the heads
+ *              [h0, h0 + H) of it.
+ *   local    : [rd][ud][bs][Lu][H][hd] (all virtual ranks, vr-major), or (bs, Lu, H, hd) for one rank.
+ *   Local slot (r, u, b, j, h) holds token zig(r, u Lu + j) of head h0 + h, where
+ *   zig(r, p) = r c + p for p < c and (2 rd - 1 - r) c + (p - c) otherwise.
+ *
+ * inverse == 0: src = natural, dst = local.  inverse != 0: src = local, dst = natural (restores
+ * natural order; heads outside the window are left untouched).
+ * vr == -1: all ud * rd virtual ranks in one launch; 0 <= vr < ud * rd: only that rank's part.
+ * Bit-exact copy. Both pointers must be 16-byte aligned when hd * elem_size is a multiple of 16,
+ * else 4-byte aligned. src and dst must not overlap.
+ */
+USP_API int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, int inverse, usp_stream_t stream);
+
+/*
+ * usp_a2a4d -- AllToAll4D inside every Ulysses group (steps a2 and a5).
+ * Source: USP review, section 三 (AllToAll4D: Q, K, V of shape (bs, L/N, hc, hd) become
+ * (hc/N, bs, L, hd); Algorithm 1 steps 1-3, and step 5 with scatter/gather indices swapped).
+ *
+ *   sequence-sharded : [rd][ud][bs][Lu][H_total][hd], heads [h0, h0 + H) taking part.
+ *   head-sharded     : [rd][ud][Hl][bs][Lr][hd] (compact, Hl = H / ud).
+ *   head-sharded[r][u'][h'][b][u Lu + j] = sequence-sharded[r][u][b][j][h0 + u' Hl + h'],
+ *   i.e. pieces are gathered by source Ulysses rank ascending.
+ * dir == +1: sequence-sharded -> head-sharded.  dir == -1: head-sharded -> sequence-sharded.
+ * Alignment and overlap rules as for usp_extract_local. An lse tensor is moved with hd = 1, USP_F32.
+ */
+USP_API int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stream);
+
+/* Attention modes (step a3 with the merge of step a4). */
+typedef enum {
+    USP_MODE_FUSED = 0, /* the whole ring: every ring step folded into one online softmax */
+    USP_MODE_STEP = 1,  /* one ring step `step`: write its partial (o_t, lse_t); empty rows get
+                           o = 0, lse = -inf */
+    USP_MODE_ACCUM = 2  /* one ring step `step`, merged into the (out, lse) already in the buffers */
+} usp_mode;
+
+typedef struct {
+    int64_t bs;     /* batch size */
+    int64_t L;      /* global sequence length */
+    int32_t hq;     /* query heads (global, of this head group) */
+    int32_t hkv;    /* KV heads (global, of this head group); GQA: q head h reads KV head h / (hq/hkv) */
+    int32_t hd;     /* head dim: 64 or 128 */
+    int32_t rd;     /* ring degree */
+    int32_t ud;     /* Ulysses degree */
+    int32_t dtype;  /* usp_dtype of q, k, v and out */
+    int32_t causal; /* nonzero: key at global position j visible to query at i iff j <= i */
+    float scale;    /* softmax scale; <= 0 means 1/sqrt(hd) */
+    int32_t mode;   /* usp_mode */
+    int32_t step;   /* ring step t for USP_MODE_STEP / USP_MODE_ACCUM, 0 <= t < rd */
+} usp_attn_desc;
+
+/*
+ * usp_attn_fwd -- LoadBalance-RingAttention forward over all virtual ring ranks (steps a3 + a4).
+ * Source: USP review, Algorithm 1 step 4; Context-Parallel page, section 先弄清楚 (each KV block
+ * gives o_j and lse_j; lse = log(e^lse1 + e^lse2), o = e^(lse1-lse) o1 + e^(lse2-lse) o2) and Fig. 1
+ * (at step t ring rank r works on the KV block of rank (r - t) mod rd).
+ *
+ *   q, out : [rd][ud][hq/ud][bs][Lr][hd]   (head-sharded, as usp_a2a4d dir=+1 writes it)
+ *   k, v   : [rd][ud][hkv/ud][bs][Lr][hd]
+ *   lse    : [rd][ud][hq/ud][bs][Lr] fp32, natural log of the row's softmax normaliser.
+ * Row p of ring rank r is the token at global position zig(r, p); the causal mask compares global
+ * positions. Scores are scale * <q, k>; inputs bf16 (tensor cores, fp32 accumulation, bf16 out) or
+ * fp32 (fp32 arithmetic, fp32 out). All pointers 16-byte aligned. out/lse must not overlap inputs.
+ * In USP_MODE_ACCUM, out and lse are read and rewritten in place.
+ */
+USP_API int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d,
+                 usp_stream_t stream);
+
+/*
+ * usp_lse_merge -- fold one partial into a running one, in place (step a4 as a standalone pass).
+ * Source: Context-Parallel page, section 先弄清楚 (the online-softmax merge equation).
+ *   (o_acc, lse_acc) <- (e^(l1 - l) o_acc + e^(l2 - l) o_new, l),  l = log(e^l1 + e^l2),
+ *   l1 = lse_acc, l2 = lse_new. lse = -inf marks an empty partial (weight 0); two empty partials
+ *   give (0, -inf).
+ *   o_acc, o_new : rows x hd of `dtype` (row-major);  lse_acc, lse_new : rows fp32.
+ * Pointers 16-byte aligned; hd * elem_size a multiple of 16. fp32 arithmetic.
+ */
+USP_API int usp_lse_merge(void *o_acc, float *lse_acc, const void *o_new, const float *lse_new, int64_t rows,
+                  int32_t hd, int32_t dtype, usp_stream_t stream);
+
+/* Synchronise `stream`, then report (and clear) the device status word of the current device:
+ * USP_OK, USP_ERR_TIMEOUT, or USP_ERR_CUDA if the synchronisation itself failed. */
+USP_API int usp_check(usp_stream_t stream);
+
+/* Static, human-readable text for a status code. */
+USP_API const char *usp_strerror(int status);
+
+/* ABI version: (major << 16) | minor. */
+USP_API int usp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* USP_H */

@@ -1,0 +1,228 @@
+"""USP-Attention forward (zigzag Ulysses x Ring) on one GB300, over a virtual rank grid.
+
+Thin Python binding of the C ABI in include/usp.h: functions with the ABI's names take torch CUDA
+tensors, check their shapes, and pass raw device pointers and the current CUDA stream to libusp.so.
+Every step of the path runs in the library's CUDA kernels; torch only allocates memory and supplies
+streams. There is no CPU fallback: if libusp.so cannot be loaded, every call raises.
+
+Layouts (all row-major; see include/usp.h for the index formulas):
+  natural            (bs, L, H, hd)                      token order of the model
+  local              [rd][ud][bs][Lu][H][hd]             after the zigzag split (Algorithm 2)
+  head-sharded       [rd][ud][H/ud][bs][Lr][hd]          after AllToAll4D
+  lse (head-sharded) [rd][ud][hq/ud][bs][Lr] fp32; lse (natural) (bs, L, hq)
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from . import _abi
+from ._abi import (USP_BF16, USP_F32, USP_MODE_ACCUM, USP_MODE_FUSED, USP_MODE_STEP, UspAttnDesc, UspDims,
+                   UspError)
+
+__all__ = ["usp_extract_local", "usp_a2a4d", "usp_attn_fwd", "usp_lse_merge", "usp_check", "usp_attention",
+           "UspAttention", "UspError", "USP_MODE_FUSED", "USP_MODE_STEP", "USP_MODE_ACCUM", "lib_path"]
+
+lib_path = _abi.LIB_PATH
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return USP_BF16
+    if t.dtype == torch.float32:
+        return USP_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(*ts):
+    for t in ts:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError("expected CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("expected contiguous tensors")
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def usp_extract_local(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, vr: int = -1, inverse: bool = False,
+                      h0: int = 0, H: Optional[int] = None, stream=None) -> torch.Tensor:
+    """Zigzag split (inverse=False: natural -> local) or its inverse (local -> natural).
+
+    natural: (bs, L, H_total, hd), or (bs, L, H_total) for an lse tensor; local:
+    [rd][ud][bs][Lu][H][hd] (or (bs, Lu, H, hd) when vr >= 0). Heads [h0, h0+H) of the natural tensor.
+    """
+    _dev(src, dst)
+    nat, loc = (dst, src) if inverse else (src, dst)
+    _need(nat.dtype == loc.dtype, "dtype mismatch")
+    if nat.dim() == 3:
+        bs, L, Ht = nat.shape
+        hd = 1
+    else:
+        _need(nat.dim() == 4, "natural tensor must be (bs, L, H, hd) or (bs, L, H)")
+        bs, L, Ht, hd = nat.shape
+    H = Ht - h0 if H is None else H
+    _need(0 <= h0 and h0 + H <= Ht, "head window out of range")
+    _need(L % (2 * rd) == 0 and (L // rd) % ud == 0, "L must split into 2*rd chunks and L/rd into ud parts")
+    Lu = L // (rd * ud)
+    ranks = rd * ud if vr < 0 else 1
+    _need(loc.numel() == ranks * bs * Lu * H * hd, f"local tensor has {loc.numel()} elements, "
+          f"expected {ranks * bs * Lu * H * hd}")
+    d = UspDims(bs, L, H, hd, _dtype_code(nat), rd, ud, Ht, h0)
+    _abi.check("usp_extract_local", _abi.load().usp_extract_local(
+        _ptr(src), _ptr(dst), d, int(vr), int(bool(inverse)), _stream(stream)))
+    return dst
+
+
+def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int = 1, h0: int = 0,
+              H: Optional[int] = None, stream=None) -> torch.Tensor:
+    """AllToAll4D inside every Ulysses group: dir=+1 sequence-sharded [rd][ud][bs][Lu][H_total][hd]
+    -> head-sharded [rd][ud][H/ud][bs][Lr][hd]; dir=-1 back. lse tensors drop the trailing hd axis."""
+    _dev(src, dst)
+    seq, hs = (src, dst) if dir > 0 else (dst, src)
+    _need(seq.dtype == hs.dtype, "dtype mismatch")
+    if seq.dim() == 5:
+        rd_, ud_, bs, Lu, Ht = seq.shape
+        hd = 1
+    else:
+        _need(seq.dim() == 6, "sequence-sharded tensor must be [rd][ud][bs][Lu][H][hd]")
+        rd_, ud_, bs, Lu, Ht, hd = seq.shape
+    _need(rd_ == rd and ud_ == ud, "grid mismatch")
+    H = Ht - h0 if H is None else H
+    _need(0 <= h0 and h0 + H <= Ht, "head window out of range")
+    _need(H % ud == 0, "heads must divide by ud")
+    L = Lu * ud * rd
+    _need(hs.numel() == rd * ud * (H // ud) * bs * ud * Lu * hd, "head-sharded tensor has the wrong size")
+    d = UspDims(bs, L, H, hd, _dtype_code(seq), rd, ud, Ht, h0)
+    _abi.check("usp_a2a4d", _abi.load().usp_a2a4d(_ptr(src), _ptr(dst), d, 1 if dir > 0 else -1,
+                                                 _stream(stream)))
+    return dst
+
+
+def usp_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+                 causal: bool = True, scale: Optional[float] = None, mode: int = USP_MODE_FUSED, step: int = 0,
+                 stream=None):
+    """Ring attention over all virtual ring ranks. q/out [rd][ud][hq/ud][bs][Lr][hd], k/v
+    [rd][ud][hkv/ud][bs][Lr][hd], lse [rd][ud][hq/ud][bs][Lr] fp32."""
+    _dev(q, k, v, out, lse)
+    _need(q.dim() == 6 and k.dim() == 6 and v.dim() == 6, "q, k, v must be [rd][ud][H/ud][bs][Lr][hd]")
+    rd, ud, Hl, bs, Lr, hd = q.shape
+    Hkl = k.shape[2]
+    _need(k.shape == (rd, ud, Hkl, bs, Lr, hd) and v.shape == k.shape, "k/v shape mismatch")
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    _need(lse.shape == (rd, ud, Hl, bs, Lr) and lse.dtype == torch.float32, "lse must be fp32 [rd][ud][Hl][bs][Lr]")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype, "dtype mismatch")
+    L = Lr * rd
+    d = UspAttnDesc(bs, L, Hl * ud, Hkl * ud, hd, rd, ud, _dtype_code(q), int(bool(causal)),
+                    float(scale) if scale is not None else 0.0, int(mode), int(step))
+    _abi.check("usp_attn_fwd", _abi.load().usp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d,
+                                                       _stream(stream)))
+    return out, lse
+
+
+def usp_lse_merge(o_acc: torch.Tensor, lse_acc: torch.Tensor, o_new: torch.Tensor, lse_new: torch.Tensor,
+                  stream=None):
+    """In place: (o_acc, lse_acc) <- LSE-merge((o_acc, lse_acc), (o_new, lse_new)); o (..., hd)."""
+    _dev(o_acc, lse_acc, o_new, lse_new)
+    _need(o_acc.shape == o_new.shape and o_acc.dtype == o_new.dtype, "o shapes/dtypes differ")
+    _need(lse_acc.dtype == torch.float32 and lse_new.dtype == torch.float32, "lse must be fp32")
+    hd = o_acc.shape[-1]
+    rows = o_acc.numel() // hd
+    _need(lse_acc.numel() == rows and lse_new.numel() == rows, "lse must hold one value per row")
+    _abi.check("usp_lse_merge", _abi.load().usp_lse_merge(_ptr(o_acc), _ptr(lse_acc), _ptr(o_new), _ptr(lse_new),
+                                                         rows, hd, _dtype_code(o_acc), _stream(stream)))
+    return o_acc, lse_acc
+
+
+def usp_check(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel's bounded device-side wait ran out."""
+    _abi.check("usp_check", _abi.load().usp_check(_stream(stream)))
+
+
+def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd: int, causal: bool = True,
+                  scale: Optional[float] = None, head_chunk: Optional[int] = None, natural_output: bool = True,
+                  stream=None):
+    """USP-Attention forward (Algorithm 1 of the USP review) over a virtual ud x rd grid on one GPU.
+
+    q: (bs, L, hq, hd), k/v: (bs, L, hkv, hd) CUDA tensors in natural token order. For every head group
+    of ``head_chunk`` query heads (all heads when None): zigzag split, AllToAll4D, ring attention with
+    LSE merging, inverse AllToAll4D (steps a1-a6). Returns (out, lse): natural (bs, L, hq, hd) and
+    (bs, L, hq) when ``natural_output``, else the sequence-sharded [rd][ud][bs][Lu][hq][hd] and
+    [rd][ud][bs][Lu][hq] a model would keep.
+    """
+    _dev(q, k, v)
+    bs, L, hq, hd = q.shape
+    hkv = k.shape[2]
+    _need(k.shape == (bs, L, hkv, hd) and v.shape == k.shape, "k/v shape mismatch")
+    _need(hq % hkv == 0, "hq must divide by hkv")
+    G = hq // hkv
+    hc = hq if head_chunk is None else head_chunk
+    _need(hq % hc == 0 and hc % G == 0, "head_chunk must divide hq and be a multiple of hq/hkv")
+    hkc = hc // G
+    _need(hc % ud == 0 and hkc % ud == 0, "head groups must divide by ud")
+    _need(L % (2 * rd) == 0 and (L // rd) % ud == 0, "L must split into 2*rd chunks and L/rd into ud parts")
+    Lu, Lr = L // (rd * ud), L // rd
+    dev, dt = q.device, q.dtype
+    o_loc = torch.empty(rd, ud, bs, Lu, hq, hd, device=dev, dtype=dt)
+    l_loc = torch.empty(rd, ud, bs, Lu, hq, device=dev, dtype=torch.float32)
+    # per-group workspace, reused across groups
+    ql = torch.empty(rd, ud, bs, Lu, hc, hd, device=dev, dtype=dt)
+    kl = torch.empty(rd, ud, bs, Lu, hkc, hd, device=dev, dtype=dt)
+    vl = torch.empty_like(kl)
+    qh = torch.empty(rd, ud, hc // ud, bs, Lr, hd, device=dev, dtype=dt)
+    kh = torch.empty(rd, ud, hkc // ud, bs, Lr, hd, device=dev, dtype=dt)
+    vh = torch.empty_like(kh)
+    oh = torch.empty_like(qh)
+    lh = torch.empty(rd, ud, hc // ud, bs, Lr, device=dev, dtype=torch.float32)
+    for g0 in range(0, hq, hc):
+        gk = g0 // G
+        usp_extract_local(q, ql, rd, ud, h0=g0, H=hc, stream=stream)
+        usp_extract_local(k, kl, rd, ud, h0=gk, H=hkc, stream=stream)
+        usp_extract_local(v, vl, rd, ud, h0=gk, H=hkc, stream=stream)
+        usp_a2a4d(ql, qh, rd, ud, 1, stream=stream)
+        usp_a2a4d(kl, kh, rd, ud, 1, stream=stream)
+        usp_a2a4d(vl, vh, rd, ud, 1, stream=stream)
+        usp_attn_fwd(qh, kh, vh, oh, lh, causal=causal, scale=scale, stream=stream)
+        usp_a2a4d(oh, o_loc, rd, ud, -1, h0=g0, H=hc, stream=stream)
+        usp_a2a4d(lh, l_loc, rd, ud, -1, h0=g0, H=hc, stream=stream)
+    if not natural_output:
+        return o_loc, l_loc
+    out = torch.empty(bs, L, hq, hd, device=dev, dtype=dt)
+    lse = torch.empty(bs, L, hq, device=dev, dtype=torch.float32)
+    usp_extract_local(o_loc, out, rd, ud, inverse=True, stream=stream)
+    usp_extract_local(l_loc, lse, rd, ud, inverse=True, stream=stream)
+    return out, lse
+
+
+class UspAttention:
+    """Callable form of :func:`usp_attention` with the grid fixed at construction, in the spirit of
+    the pages' ``LongContextAttention(ring_impl_type="zigzag")`` (one device, virtual ranks)."""
+
+    def __init__(self, ulysses_degree: int, ring_degree: int, causal: bool = True, scale: Optional[float] = None,
+                 head_chunk: Optional[int] = None):
+        self.ud, self.rd = int(ulysses_degree), int(ring_degree)
+        self.causal, self.scale, self.head_chunk = causal, scale, head_chunk
+
+    def __call__(self, q, k, v, natural_output: bool = True):
+        return usp_attention(q, k, v, self.ud, self.rd, causal=self.causal, scale=self.scale,
+                             head_chunk=self.head_chunk, natural_output=natural_output)
+
+
+def default_scale(hd: int) -> float:
+    return 1.0 / math.sqrt(hd)

@@ -1,0 +1,635 @@
+// attn_tc.cu -- bf16 LoadBalance-RingAttention forward on the 5th-generation tensor cores (sm_103a).
+//
+// What it computes (USP review, Algorithm 1 step 4; Context-Parallel page, section 先弄清楚 and
+// Fig. 1): for every virtual ring rank r, Ulysses rank u, local query head h and batch b, the rows of
+// rank r's zigzag-local sequence attend to the KV blocks of ring ranks (r - t) mod rd for
+// t = 0 .. rd-1 in that order, under the causal mask on global positions; the per-block partials are
+// folded by the log-sum-exp merge. Here the merge is the online-softmax rescale inside one pass, so
+// no partial ever leaves the chip (the fused-merge epilogue). USP_MODE_STEP / USP_MODE_ACCUM run a
+// single ring step and write its partial, or merge it into (out, lse) in the epilogue.
+//
+// Kernel design (one CTA = 256 query rows = two 128-row Q tiles of one (r, u, h, b)):
+//   warp 8      TMA producer: Q0, Q1 once; K and V tiles (128 keys x hd) through a ring of stages.
+//   warp 9      MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V on tcgen05 (kind::f16, bf16 in,
+//               fp32 accumulators in tensor memory), issue order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
+//               so the tensor core works on one tile while the other tile's softmax runs.
+//   warps 0-3   softmax of Q tile 0, warps 4-7 softmax of Q tile 1: one thread per query row reads
+//               its S row from TMEM, masks partial tiles, updates the running max with a lazy
+//               rescale (O and l are rescaled only when the max grows by more than 2^8), writes
+//               P = 2^(S*scale*log2e - m) as bf16 back into TMEM (the A operand of the PV MMA), and
+//               finally normalises O and writes out (bf16) and lse (fp32).
+//   TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+hd) O1 [256+hd, 256+2hd); P_i aliases S_i.
+// The causal structure is exploited per (Q tile, KV tile) pair from global positions: tiles wholly
+// after the queries are skipped (never loaded), tiles wholly before are unmasked, the rest are
+// masked per element with a per-row key limit (the zigzag map is increasing inside a rank, so the
+// keys a row sees in a rank's block are a prefix of it).
+// Every wait is bounded (2 s): on expiry the kernel records USP_ERR_TIMEOUT in the device status
+// word, drains what it has in flight and returns.
+#include <cuda.h>
+
+#include "tc_ptx.cuh"
+#include "usp_device.cuh"
+#include "usp_internal.cuh"
+
+namespace usp {
+namespace {
+
+constexpr int kM = 128;  // query rows per tile
+constexpr int kN = 128;  // keys per tile
+constexpr int kWarps = 10;
+constexpr int kThreads = kWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+
+template <int HD> struct Cfg {
+    static constexpr int kBoxes = HD / 64;            // 64-column (128-byte) TMA boxes per row
+    static constexpr int kBoxBytes = kM * 128;         // 128 rows x 128 bytes
+    static constexpr int kTileBytes = kM * HD * 2;     // 128 rows x hd bf16
+    static constexpr int kStages = (HD == 128) ? 2 : 4;
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + 2 * kTileBytes;
+    static constexpr int kV = kK + kStages * kTileBytes;
+    static constexpr int kBar = kV + kStages * kTileBytes;
+    // barrier indices
+    static constexpr int Q_FULL = 0;
+    static constexpr int K_FULL = 1;
+    static constexpr int K_EMPTY = K_FULL + kStages;
+    static constexpr int V_FULL = K_EMPTY + kStages;
+    static constexpr int V_EMPTY = V_FULL + kStages;
+    static constexpr int S_FULL = V_EMPTY + kStages;  // [2]
+    static constexpr int P_FULL = S_FULL + 2;         // [2]
+    static constexpr int O_FULL = P_FULL + 2;         // [2]
+    static constexpr int DONE = O_FULL + 2;
+    static constexpr int kNumBars = DONE + 1;
+    static constexpr int kTmemSlot = kBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kTmemSlot + 16 + 1024;  // + slack for 1024-byte alignment
+    __device__ static constexpr uint32_t colS(int i) { return 128u * (uint32_t)i; }
+    __device__ static constexpr uint32_t colO(int i) { return 256u + (uint32_t)(HD * i); }
+};
+
+struct TcParams {
+    CUtensorMap tq, tk, tv;
+    __nv_bfloat16 *out;
+    float *lse;
+    int *status;
+    uint32_t bs, Lr, c, rd, ud, Hl, Hkl, G, npairs;
+    int causal, mode, step, lpt;
+    float scale_log2;
+};
+
+// The work of one CTA and the walk over its KV tiles (identical in every role).
+struct Work {
+    uint32_t r, u, hl, b, kh;
+    int64_t q_row_base;   // row of local row 0 of (r, u, hl, b) in q / out / lse
+    uint32_t q0[2];       // first local row of each Q tile
+    bool valid[2];
+    int64_t qpos_min[2], qpos_max[2];
+    int t_begin, t_end;
+};
+
+struct Tile {
+    uint32_t s, kt;
+    int64_t kv_row;  // first row of the tile in k / v
+    bool act[2];     // the Q tile needs this KV tile
+    bool full[2];    // every key of the tile is visible to every row of the Q tile
+};
+
+struct TileIter {
+    int t;
+    uint32_t kt, nkt, s;
+    int64_t nhi[2], nlo[2];
+};
+
+__device__ __forceinline__ Work decode_work(const TcParams &p) {
+    Work w;
+    uint32_t x = blockIdx.x;
+    const uint32_t inner = p.ud * p.Hl * p.bs;
+    const uint32_t outer = x / inner;
+    uint32_t in = x % inner;
+    w.hl = in % p.Hl;  // heads fastest: CTAs that run together on a GQA group share K/V in L2
+    in /= p.Hl;
+    w.b = in % p.bs;
+    w.u = in / p.bs;
+    uint32_t qp;
+    if (p.lpt) {
+        // heaviest first: global 256-row blocks from the end of the sequence to its start
+        const uint32_t per_chunk = p.c / 256;
+        const uint32_t gp = 2 * p.rd * per_chunk - 1 - outer;
+        const uint32_t a = gp / per_chunk;
+        const uint32_t off = (gp % per_chunk) * 256;
+        w.r = a < p.rd ? a : 2 * p.rd - 1 - a;
+        qp = ((a < p.rd) ? off : p.c + off) / 256;
+    } else {
+        w.r = outer / p.npairs;
+        qp = outer % p.npairs;
+    }
+    w.kh = w.hl / p.G;
+    w.q_row_base = ((((int64_t)w.r * p.ud + w.u) * p.Hl + w.hl) * p.bs + w.b) * p.Lr;
+    for (int i = 0; i < 2; ++i) {
+        w.q0[i] = qp * 256 + i * 128;
+        w.valid[i] = w.q0[i] < p.Lr;
+        const uint32_t last = min(w.q0[i] + 127, p.Lr - 1);
+        w.qpos_min[i] = zig_pos(w.r, min(w.q0[i], p.Lr - 1), p.c, p.rd);
+        w.qpos_max[i] = zig_pos(w.r, last, p.c, p.rd);
+    }
+    w.t_begin = p.mode == USP_MODE_FUSED ? 0 : p.step;
+    w.t_end = p.mode == USP_MODE_FUSED ? (int)p.rd : p.step + 1;
+    return w;
+}
+
+__device__ __forceinline__ void iter_setup(const TcParams &p, const Work &w, TileIter &it) {
+    it.s = (w.r + p.rd - (uint32_t)it.t) % p.rd;
+    int64_t mx = 0;
+    for (int i = 0; i < 2; ++i) {
+        if (!w.valid[i]) {
+            it.nhi[i] = 0;
+            it.nlo[i] = 0;
+        } else if (p.causal) {
+            it.nhi[i] = visible_prefix(w.qpos_max[i], it.s, p.c, p.rd);
+            it.nlo[i] = visible_prefix(w.qpos_min[i], it.s, p.c, p.rd);
+        } else {
+            it.nhi[i] = p.Lr;
+            it.nlo[i] = p.Lr;
+        }
+        mx = max(mx, it.nhi[i]);
+    }
+    it.nkt = (uint32_t)((mx + kN - 1) / kN);
+    it.kt = 0;
+}
+
+__device__ __forceinline__ void iter_init(const TcParams &p, const Work &w, TileIter &it) {
+    it.t = w.t_begin;
+    iter_setup(p, w, it);
+}
+
+__device__ __forceinline__ bool iter_next(const TcParams &p, const Work &w, TileIter &it, Tile &tl) {
+    while (it.kt >= it.nkt) {
+        if (++it.t >= w.t_end) return false;
+        iter_setup(p, w, it);
+    }
+    tl.s = it.s;
+    tl.kt = it.kt;
+    tl.kv_row = ((((int64_t)it.s * p.ud + w.u) * p.Hkl + w.kh) * p.bs + w.b) * p.Lr + (int64_t)it.kt * kN;
+    for (int i = 0; i < 2; ++i) {
+        tl.act[i] = (int64_t)it.kt * kN < it.nhi[i];
+        tl.full[i] = (int64_t)(it.kt + 1) * kN <= it.nlo[i];
+    }
+    ++it.kt;
+    return true;
+}
+
+// ------------------------------------------------------------------------------------------------
+// roles
+// ------------------------------------------------------------------------------------------------
+template <int HD>
+__device__ void producer_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0) {
+    using C = Cfg<HD>;
+    auto BAR = [&](int i) { return bar0 + 8u * i; };
+    const uint32_t sQ = sbase + C::kQ, sK = sbase + C::kK, sV = sbase + C::kV;
+    tc::mbar_arrive_expect_tx(BAR(C::Q_FULL), 2 * C::kTileBytes);
+    for (int i = 0; i < 2; ++i)
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+            tc::tma_load_2d(sQ + i * C::kTileBytes + bx * C::kBoxBytes, &p.tq, bx * 64,
+                            (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
+    uint32_t fills[C::kStages];
+    for (int s = 0; s < C::kStages; ++s) fills[s] = 0;
+    TileIter it;
+    iter_init(p, w, it);
+    Tile tl;
+    uint32_t j = 0;
+    bool ok = true;
+    while (ok && iter_next(p, w, it, tl)) {
+        const uint32_t st = j % C::kStages;
+        const uint32_t ph = ((j / C::kStages) & 1u) ^ 1u;
+        if (!(ok = tc::mbar_wait(BAR(C::K_EMPTY + st), ph, p.status, USP_ERR_TIMEOUT, kWaitLimitNs))) break;
+        tc::mbar_arrive_expect_tx(BAR(C::K_FULL + st), C::kTileBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+            tc::tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.tk, bx * 64, (int32_t)tl.kv_row,
+                            BAR(C::K_FULL + st));
+        if (!(ok = tc::mbar_wait(BAR(C::V_EMPTY + st), ph, p.status, USP_ERR_TIMEOUT, kWaitLimitNs))) {
+            ++fills[st];  // the K fill of this stage is in flight
+            break;
+        }
+        tc::mbar_arrive_expect_tx(BAR(C::V_FULL + st), C::kTileBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+            tc::tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.tv, bx * 64, (int32_t)tl.kv_row,
+                            BAR(C::V_FULL + st));
+        ++fills[st];
+        ++j;
+    }
+    if (!ok) {
+        // drain: wait (bounded) for the copies this warp issued, so none lands after the CTA exits
+        tc::mbar_wait(BAR(C::Q_FULL), 0, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+        for (int s = 0; s < C::kStages; ++s)
+            if (fills[s] > 0) {
+                tc::mbar_wait(BAR(C::K_FULL + s), (fills[s] - 1) & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+                tc::mbar_wait(BAR(C::V_FULL + s), (fills[s] - 1) & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+            }
+    }
+}
+
+template <int HD>
+__device__ __forceinline__ void issue_s(uint32_t tmem, int i, uint32_t sQ, uint32_t sKst) {
+    using C = Cfg<HD>;
+    constexpr uint32_t idS = tc::idesc_bf16_f32(kM, kN, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t koff = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
+        const uint64_t a = tc::sw128_desc(sQ + i * C::kTileBytes + koff, 16, 1024);
+        const uint64_t b = tc::sw128_desc(sKst + koff, 16, 1024);
+        tc::mma_ss(tmem + C::colS(i), a, b, idS, kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int HD>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, int i, uint32_t sVst, uint32_t accumulate) {
+    using C = Cfg<HD>;
+    // B = V viewed as (N = hd) x (K = keys), MN-major: 64-column blocks C::kBoxBytes apart (LBO),
+    // 8-key groups 1024 bytes apart (SBO); 16 keys per MMA = 2048 bytes.
+    constexpr uint32_t idO = tc::idesc_bf16_f32(kM, HD, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < kN / 16; ++kk) {
+        const uint64_t b = tc::sw128_desc(sVst + kk * 2048, C::kBoxBytes, 1024);
+        tc::mma_ts(tmem + C::colO(i), tmem + C::colS(i) + kk * 8, b, idO, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <int HD>
+__device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0, uint32_t tmem) {
+    using C = Cfg<HD>;
+    auto BAR = [&](int i) { return bar0 + 8u * i; };
+    const uint32_t sQ = sbase + C::kQ, sK = sbase + C::kK, sV = sbase + C::kV;
+    auto wait = [&](int bar, uint32_t parity) {
+        return tc::mbar_wait(BAR(bar), parity, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+    };
+    bool ok = wait(C::Q_FULL, 0);
+    tc::fence_after_sync();
+    TileIter it;
+    iter_init(p, w, it);
+    Tile cur, nxt;
+    bool have = ok && iter_next(p, w, it, cur);
+    uint32_t pc[2] = {0, 0}, started[2] = {0, 0};
+    uint32_t j = 0;
+    if (have) {
+        ok = wait(C::K_FULL + 0, 0);
+        tc::fence_after_sync();
+        if (ok) {
+            for (int i = 0; i < 2; ++i)
+                if (cur.act[i]) {
+                    issue_s<HD>(tmem, i, sQ, sK);
+                    tc::mma_commit(BAR(C::S_FULL + i));
+                }
+            tc::mma_commit(BAR(C::K_EMPTY + 0));
+        }
+    }
+    while (ok && have) {
+        const bool have_n = iter_next(p, w, it, nxt);
+        const uint32_t st = j % C::kStages, ph = (j / C::kStages) & 1u;
+        const uint32_t stn = (j + 1) % C::kStages, phn = ((j + 1) / C::kStages) & 1u;
+        if (!(ok = wait(C::V_FULL + st, ph))) break;
+        tc::fence_after_sync();
+        bool kn_ready = false;
+        for (int i = 0; i < 2 && ok; ++i) {
+            if (cur.act[i]) {
+                if (!(ok = wait(C::P_FULL + i, pc[i] & 1u))) break;
+                ++pc[i];
+                tc::fence_after_sync();
+                issue_pv<HD>(tmem, i, sV + st * C::kTileBytes, started[i]);
+                started[i] = 1;
+            }
+            if (have_n && nxt.act[i]) {
+                if (!kn_ready) {
+                    if (!(ok = wait(C::K_FULL + stn, phn))) break;
+                    tc::fence_after_sync();
+                    kn_ready = true;
+                }
+                issue_s<HD>(tmem, i, sQ, sK + stn * C::kTileBytes);
+                tc::mma_commit(BAR(C::S_FULL + i));
+            }
+        }
+        if (!ok) break;
+        tc::mma_commit(BAR(C::V_EMPTY + st));
+        if (have_n) {
+            if (!kn_ready) {
+                if (!(ok = wait(C::K_FULL + stn, phn))) break;
+                tc::fence_after_sync();
+            }
+            tc::mma_commit(BAR(C::K_EMPTY + stn));
+        }
+        cur = nxt;
+        have = have_n;
+        ++j;
+    }
+    tc::mma_commit(BAR(C::O_FULL + 0));
+    tc::mma_commit(BAR(C::O_FULL + 1));
+    // every MMA of this CTA has finished before tensor memory is released
+    tc::mma_commit(BAR(C::DONE));
+    wait(C::DONE, 0);
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+template <int HD>
+__device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem, int i) {
+    using C = Cfg<HD>;
+    auto BAR = [&](int k) { return bar0 + 8u * k; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wq = warp & 3;
+    const uint32_t row = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::colS(i);
+    const uint32_t tO = tmem + lane_off + C::colO(i);
+    const uint32_t row_local = w.q0[i] + row;
+    const bool row_ok = w.valid[i] && row_local < p.Lr;
+    const int64_t qpos_row = zig_pos(w.r, min(row_local, p.Lr - 1), p.c, p.rd);
+    const float sl2 = p.scale_log2;
+
+    float m_used = -INFINITY, l = 0.f;
+    uint32_t n_act = 0;
+    bool ok = true;
+    TileIter it;
+    iter_init(p, w, it);
+    Tile tl;
+    uint32_t s_cur = 0xffffffffu;
+    int64_t lim = 0;
+    while (iter_next(p, w, it, tl)) {
+        if (!tl.act[i]) continue;
+        if (tl.s != s_cur) {
+            s_cur = tl.s;
+            lim = p.causal ? visible_prefix(qpos_row, s_cur, p.c, p.rd) : (int64_t)p.Lr;
+        }
+        ok = tc::mbar_wait(BAR(C::S_FULL + i), n_act & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc::fence_after_sync();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tc::tmem_ld32(tS + cc * 32, sr[cc]);
+        tc::tmem_ld_wait();
+        if (!tl.full[i]) {
+            int64_t ll = lim - (int64_t)tl.kt * kN;
+            const int lim_local = ll < 0 ? 0 : (ll > kN ? kN : (int)ll);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (cc * 32 + e >= lim_local) sr[cc][e] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, u2f(sr[cc][e]));
+        const float m_new = fmaxf(m_used, mx * sl2);
+        const bool need = m_new > m_used + kRescaleThreshold;
+        float alpha = 1.f;
+        if (need) {
+            alpha = tc::ex2(m_used - m_new);  // 0 on the first visible tile (m_used = -inf)
+            m_used = m_new;
+        }
+        if (n_act > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int oc = 0; oc < HD / 32; ++oc) {
+                uint32_t o[32];
+                tc::tmem_ld32(tO + oc * 32, o);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
+                tc::tmem_st32(tO + oc * 32, o);
+            }
+        }
+        l *= alpha;
+        const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+        float sum = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int col = half * 64 + 2 * e;
+                const float x0 = u2f(sr[col / 32][col % 32]);
+                const float x1 = u2f(sr[(col + 1) / 32][(col + 1) % 32]);
+                const float p0 = tc::ex2(fmaf(x0, sl2, -mb));
+                const float p1 = tc::ex2(fmaf(x1, sl2, -mb));
+                sum += p0 + p1;
+                pk[e] = float2_to_bf16x2(p0, p1);
+            }
+            tc::tmem_st32(tS + half * 32, pk);
+        }
+        l += sum;
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(BAR(C::P_FULL + i));
+        ++n_act;
+    }
+    if (!ok) return;
+    // ---- epilogue: normalise, merge (ACCUM), store -------------------------------------------
+    const int64_t grow = w.q_row_base + row_local;
+    const float lse_cur = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+    float w_old = 0.f, w_new = 1.f, lse_out = lse_cur;
+    if (p.mode == USP_MODE_ACCUM && row_ok) merge_weights(p.lse[grow], lse_cur, w_old, w_new, lse_out);
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16 *orow = p.out + grow * HD;
+    if (n_act > 0) {
+        ok = tc::mbar_wait(BAR(C::O_FULL + i), 0, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int oc = 0; oc < HD / 32; ++oc) {
+            uint32_t o[32];
+            tc::tmem_ld32(tO + oc * 32, o);
+            tc::tmem_ld_wait();
+            if (row_ok) {
+                float v[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = u2f(o[e]) * inv_l;
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + oc * 32);
+                if (p.mode == USP_MODE_ACCUM) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 old = dst[q];
+                        const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const float2 f = bf16x2_to_float2(ow[h]);
+                            v[q * 8 + 2 * h] = w_old * f.x + w_new * v[q * 8 + 2 * h];
+                            v[q * 8 + 2 * h + 1] = w_old * f.y + w_new * v[q * 8 + 2 * h + 1];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 pkd;
+                    pkd.x = float2_to_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+                    pkd.y = float2_to_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+                    pkd.z = float2_to_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+                    pkd.w = float2_to_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+                    dst[q] = pkd;
+                }
+            }
+        }
+    } else if (row_ok && p.mode != USP_MODE_ACCUM) {
+        // no visible key in this pass: the empty partial (0, -inf)
+        uint4 *dst = reinterpret_cast<uint4 *>(orow);
+        for (int q = 0; q < HD / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+    }
+    if (row_ok) p.lse[grow] = lse_out;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+    using C = Cfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+    const uint32_t bar0 = sbase + C::kBar;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kTmemSlot);
+    volatile uint32_t *skip_flag = tmem_slot + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        // a bounded wait of an earlier CTA or launch ran out: do no work until usp_check clears it
+        *skip_flag = (*reinterpret_cast<volatile int *>(p.status) != 0) ? 1u : 0u;
+        for (int s = 0; s < C::kStages; ++s) {
+            tc::mbar_init(bar0 + 8u * (C::K_FULL + s), 1);
+            tc::mbar_init(bar0 + 8u * (C::K_EMPTY + s), 1);
+            tc::mbar_init(bar0 + 8u * (C::V_FULL + s), 1);
+            tc::mbar_init(bar0 + 8u * (C::V_EMPTY + s), 1);
+        }
+        tc::mbar_init(bar0 + 8u * C::Q_FULL, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar0 + 8u * (C::S_FULL + i), 1);
+            tc::mbar_init(bar0 + 8u * (C::P_FULL + i), 4);  // one arrive per softmax warp
+            tc::mbar_init(bar0 + 8u * (C::O_FULL + i), 1);
+        }
+        tc::mbar_init(bar0 + 8u * C::DONE, 1);
+        tc::fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+        tc::tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tc::prefetch_tmap(&p.tq);
+        tc::prefetch_tmap(&p.tk);
+        tc::prefetch_tmap(&p.tv);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *skip_flag != 0;
+    const Work w = decode_work(p);
+
+    if (skip) {
+        // nothing to do
+    } else if (warp == kProducerWarp) {
+        if (lane == 0) producer_role<HD>(p, w, sbase, bar0);
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) mma_role<HD>(p, w, sbase, bar0, tmem);
+        __syncwarp();
+    } else {
+        softmax_role<HD>(p, w, bar0, tmem, warp >> 2);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// 2-D view (rows x hd) of a bf16 tensor, 128-row x 64-column boxes, 128-byte swizzle, zero fill
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, int hd) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)hd * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HD>
+int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
+    using C = Cfg<HD>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+            cudaSuccess)
+            return USP_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    attn_tc_kernel<HD><<<grid, kThreads, C::kSmemBytes, s>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
+    const DeviceInfo *di = device_info();
+    if (!di) return USP_ERR_CUDA;
+    TcParams p{};
+    const uint64_t q_rows = (uint64_t)a.hq * a.bs * a.L;
+    const uint64_t kv_rows = (uint64_t)a.hkv * a.bs * a.L;
+    if (!make_tmap(&p.tq, a.q, q_rows, a.hd) || !make_tmap(&p.tk, a.k, kv_rows, a.hd) ||
+        !make_tmap(&p.tv, a.v, kv_rows, a.hd))
+        return USP_ERR_CUDA;
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.lse = a.lse;
+    p.status = di->status;
+    p.bs = (uint32_t)a.bs;
+    p.rd = (uint32_t)a.rd;
+    p.ud = (uint32_t)a.ud;
+    p.Lr = (uint32_t)(a.L / a.rd);
+    p.c = (uint32_t)(a.L / (2 * a.rd));
+    p.Hl = (uint32_t)(a.hq / a.ud);
+    p.Hkl = (uint32_t)(a.hkv / a.ud);
+    p.G = (uint32_t)(a.hq / a.hkv);
+    p.npairs = (p.Lr + 255) / 256;
+    p.causal = a.causal;
+    p.mode = a.mode;
+    p.step = a.step;
+    p.lpt = (p.c % 256 == 0) ? 1 : 0;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const uint64_t grid = (uint64_t)p.rd * p.ud * p.Hl * p.bs * p.npairs;
+    if (grid == 0) return USP_OK;
+    if (grid >= (1ull << 31)) return USP_ERR_UNSUPPORTED;
+    return a.hd == 128 ? launch_typed<128>(p, (uint32_t)grid, s) : launch_typed<64>(p, (uint32_t)grid, s);
+}
+
+}  // namespace usp

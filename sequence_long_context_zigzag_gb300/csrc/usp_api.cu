@@ -1,0 +1,176 @@
+// usp_api.cu -- argument validation and dispatch for the C ABI declared in include/usp.h.
+#include <math.h>
+#include <mutex>
+
+#include "usp_internal.cuh"
+
+// One status word per device: kernels whose bounded waits run out write a nonzero code here.
+static __device__ int g_usp_status;
+
+namespace usp {
+
+static constexpr int kMaxDevices = 64;
+static DeviceInfo g_info[kMaxDevices];
+static bool g_info_ok[kMaxDevices];
+static std::mutex g_info_mu;
+
+const DeviceInfo *device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_info_mu);
+    if (!g_info_ok[dev]) {
+        DeviceInfo di{};
+        if (cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return nullptr;
+        // the symbol's device address for the current device (host code cannot name it directly)
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&di.status), g_usp_status) != cudaSuccess)
+            return nullptr;
+        g_info[dev] = di;
+        g_info_ok[dev] = true;
+    }
+    return &g_info[dev];
+}
+
+static bool overflow31(int64_t x) { return x < 0 || x >= (int64_t(1) << 31); }
+
+// shared checks of a permute's dims; fills the derived sizes
+static int check_dims(const usp_dims &d, int need_head_split) {
+    if (d.bs < 0 || d.L < 0 || d.H < 0 || d.hd <= 0 || d.rd <= 0 || d.ud <= 0 || d.h0 < 0 ||
+        d.H_total < 0)
+        return USP_ERR_INVALID_ARG;
+    if (elem_size(d.dtype) == 0) return USP_ERR_DTYPE;
+    if (d.L % (2 * (int64_t)d.rd) != 0) return USP_ERR_SHAPE;
+    if ((d.L / d.rd) % d.ud != 0) return USP_ERR_SHAPE;
+    int32_t Ht = d.H_total ? d.H_total : d.H;
+    if ((int64_t)d.h0 + d.H > Ht) return USP_ERR_SHAPE;
+    if (need_head_split && d.H % d.ud != 0) return USP_ERR_SHAPE;
+    if (overflow31(d.bs * d.L * (int64_t)Ht) || overflow31(d.L) ||
+        overflow31((int64_t)d.hd * elem_size(d.dtype)))
+        return USP_ERR_UNSUPPORTED;
+    return USP_OK;
+}
+
+static int check_ptr_align(const void *a, const void *b, int64_t row_bytes) {
+    uintptr_t al = (row_bytes % 16 == 0) ? 16 : 4;
+    if (row_bytes % 4 != 0) return USP_ERR_UNSUPPORTED;
+    if (!aligned(a, al) || !aligned(b, al)) return USP_ERR_ALIGN;
+    return USP_OK;
+}
+
+}  // namespace usp
+
+using namespace usp;
+
+extern "C" {
+
+int usp_version(void) { return (1 << 16) | 0; }
+
+const char *usp_strerror(int status) {
+    switch (status) {
+        case USP_OK: return "success";
+        case USP_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad enum)";
+        case USP_ERR_SHAPE: return "shape not divisible (L % 2rd, (L/rd) % ud, heads % ud, hq % hkv)";
+        case USP_ERR_DTYPE: return "unknown dtype code";
+        case USP_ERR_ALIGN: return "pointer not aligned as required";
+        case USP_ERR_UNSUPPORTED: return "unsupported configuration";
+        case USP_ERR_CUDA: return "CUDA runtime error";
+        case USP_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+        default: return "unknown status";
+    }
+}
+
+int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, int inverse, usp_stream_t stream) {
+    int rc = check_dims(d, 0);
+    if (rc) return rc;
+    if (vr < -1 || vr >= d.rd * d.ud) return USP_ERR_INVALID_ARG;
+    if (d.bs == 0 || d.L == 0 || d.H == 0) return USP_OK;
+    if (!src || !dst) return USP_ERR_INVALID_ARG;
+    const int64_t row_bytes = (int64_t)d.hd * elem_size(d.dtype);
+    if ((rc = check_ptr_align(src, dst, row_bytes))) return rc;
+    PermArgs a{};
+    a.src = static_cast<const char *>(src);
+    a.dst = static_cast<char *>(dst);
+    a.mode = inverse ? PERM_EXTRACT_INV : PERM_EXTRACT;
+    a.bs = d.bs; a.L = d.L; a.H = d.H; a.H_total = d.H_total ? d.H_total : d.H; a.h0 = d.h0;
+    a.rd = d.rd; a.ud = d.ud; a.row_bytes = row_bytes;
+    a.r_fixed = vr >= 0 ? vr / d.ud : -1;
+    a.u_fixed = vr >= 0 ? vr % d.ud : -1;
+    return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stream) {
+    int rc = check_dims(d, 1);
+    if (rc) return rc;
+    if (dir != 1 && dir != -1) return USP_ERR_INVALID_ARG;
+    if (d.bs == 0 || d.L == 0 || d.H == 0) return USP_OK;
+    if (!src || !dst) return USP_ERR_INVALID_ARG;
+    const int64_t row_bytes = (int64_t)d.hd * elem_size(d.dtype);
+    if ((rc = check_ptr_align(src, dst, row_bytes))) return rc;
+    PermArgs a{};
+    a.src = static_cast<const char *>(src);
+    a.dst = static_cast<char *>(dst);
+    a.mode = dir > 0 ? PERM_A2A_FWD : PERM_A2A_INV;
+    a.bs = d.bs; a.L = d.L; a.H = d.H; a.H_total = d.H_total ? d.H_total : d.H; a.h0 = d.h0;
+    a.rd = d.rd; a.ud = d.ud; a.row_bytes = row_bytes;
+    a.r_fixed = -1; a.u_fixed = -1;
+    return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d,
+                 usp_stream_t stream) {
+    if (d.bs < 0 || d.L < 0 || d.hq <= 0 || d.hkv <= 0 || d.rd <= 0 || d.ud <= 0)
+        return USP_ERR_INVALID_ARG;
+    if (d.mode < USP_MODE_FUSED || d.mode > USP_MODE_ACCUM) return USP_ERR_INVALID_ARG;
+    if (d.mode != USP_MODE_FUSED && (d.step < 0 || d.step >= d.rd)) return USP_ERR_INVALID_ARG;
+    if (elem_size(d.dtype) == 0) return USP_ERR_DTYPE;
+    if (d.L % (2 * (int64_t)d.rd) != 0 || (d.L / d.rd) % d.ud != 0) return USP_ERR_SHAPE;
+    if (d.hq % d.hkv != 0 || d.hq % d.ud != 0 || d.hkv % d.ud != 0) return USP_ERR_SHAPE;
+    if (d.hd != 64 && d.hd != 128) return USP_ERR_UNSUPPORTED;
+    if (overflow31(d.bs * d.L * (int64_t)d.hq) || overflow31(d.L)) return USP_ERR_UNSUPPORTED;
+    if (!(d.scale == d.scale) || isinf(d.scale)) return USP_ERR_INVALID_ARG;
+    if (d.bs == 0 || d.L == 0) return USP_OK;
+    if (!q || !k || !v || !out || !lse) return USP_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 16))
+        return USP_ERR_ALIGN;
+    AttnArgs a{};
+    a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
+    a.bs = d.bs; a.L = d.L; a.hq = d.hq; a.hkv = d.hkv; a.hd = d.hd; a.rd = d.rd; a.ud = d.ud;
+    a.dtype = d.dtype; a.causal = d.causal ? 1 : 0; a.mode = d.mode; a.step = d.step;
+    a.scale = d.scale > 0.f ? d.scale : 1.0f / sqrtf((float)d.hd);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d.dtype == USP_BF16) return launch_attn_tc(a, s);
+    return launch_attn_simt(a, s);
+}
+
+int usp_lse_merge(void *o_acc, float *lse_acc, const void *o_new, const float *lse_new, int64_t rows,
+                  int32_t hd, int32_t dtype, usp_stream_t stream) {
+    if (rows < 0 || hd <= 0) return USP_ERR_INVALID_ARG;
+    const int es = elem_size(dtype);
+    if (es == 0) return USP_ERR_DTYPE;
+    if (((int64_t)hd * es) % 16 != 0) return USP_ERR_UNSUPPORTED;
+    if (overflow31(rows) || overflow31(rows * hd)) return USP_ERR_UNSUPPORTED;
+    if (rows == 0) return USP_OK;
+    if (!o_acc || !lse_acc || !o_new || !lse_new) return USP_ERR_INVALID_ARG;
+    if (!aligned(o_acc, 16) || !aligned(o_new, 16) || !aligned(lse_acc, 16) || !aligned(lse_new, 16))
+        return USP_ERR_ALIGN;
+    return launch_lse_merge(o_acc, lse_acc, o_new, lse_new, rows, hd, dtype,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_check(usp_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return USP_ERR_CUDA;
+    const DeviceInfo *di = device_info();
+    if (!di) return USP_ERR_CUDA;
+    int st = 0;
+    if (cudaMemcpy(&st, di->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return USP_ERR_CUDA;
+    if (st != 0) {
+        int zero = 0;
+        if (cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return USP_ERR_CUDA;
+        return USP_ERR_TIMEOUT;
+    }
+    return USP_OK;
+}
+
+}  // extern "C"

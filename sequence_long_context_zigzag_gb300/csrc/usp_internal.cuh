@@ -1,0 +1,83 @@
+// usp_internal.cuh -- helpers shared by the library's CUDA translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "usp.h"
+
+namespace usp {
+
+// Division of a 32-bit unsigned numerator n < 2^31 by a runtime divisor d >= 1 with one multiply-high
+// and one shift (Granlund & Montgomery, "Division by invariant integers using multiplication", 1994):
+// with l = ceil(log2 d) and m = ceil(2^(31+l) / d), floor(n m / 2^(31+l)) == floor(n / d). The error
+// term n (m d - 2^(31+l)) / (d 2^(31+l)) is below 2^-l <= 1/d, so it never crosses an integer.
+// m fits in 32 bits because d > 2^(l-1).
+struct FastDiv {
+    uint32_t d;
+    uint32_t m;
+    uint32_t s;  // shift applied to the high word: l - 1
+    FastDiv() : d(1), m(0), s(0) {}
+    explicit FastDiv(uint32_t div) : d(div) {
+        if (div <= 1) { d = 1; m = 0; s = 0; return; }
+        uint32_t l = 0;
+        while ((1ull << l) < div) ++l;
+        m = (uint32_t)(((1ull << (31 + l)) + div - 1) / div);
+        s = l - 1;
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        return d == 1 ? n : (__umulhi(n, m) >> s);
+    }
+    __device__ __forceinline__ void divmod(uint32_t n, uint32_t &q, uint32_t &r) const {
+        q = div(n);
+        r = n - q * d;
+    }
+};
+
+// zigzag position of ring-local row p on ring rank r (chunk length c, ring degree rd):
+// rank r keeps global chunks r and 2 rd - 1 - r, in that order.
+__host__ __device__ __forceinline__ int64_t zig_pos(int64_t r, int64_t p, int64_t c, int64_t rd) {
+    return p < c ? r * c + p : (2 * rd - 1 - r) * c + (p - c);
+}
+
+// per-device cached properties and the device status word address
+struct DeviceInfo {
+    int sm_count;
+    int *status;  // device address of this library's status word on that device
+};
+// returns nullptr on a CUDA failure
+const DeviceInfo *device_info();
+
+inline int elem_size(int dtype) { return dtype == USP_F32 ? 4 : (dtype == USP_BF16 ? 2 : 0); }
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// kernel launchers implemented in separate translation units; return USP_* codes
+enum PermMode { PERM_EXTRACT = 0, PERM_EXTRACT_INV = 1, PERM_A2A_FWD = 2, PERM_A2A_INV = 3 };
+
+struct PermArgs {
+    const char *src;
+    char *dst;
+    int mode;
+    int64_t bs, L;
+    int32_t H, H_total, h0, rd, ud;
+    int32_t r_fixed, u_fixed;  // >= 0 when only one virtual rank takes part (extract only)
+    int64_t row_bytes;
+};
+int launch_permute(const PermArgs &a, cudaStream_t s);
+
+int launch_lse_merge(void *o_acc, float *lse_acc, const void *o_new, const float *lse_new, int64_t rows,
+                     int hd, int dtype, cudaStream_t s);
+
+struct AttnArgs {
+    const void *q, *k, *v;
+    void *out;
+    float *lse;
+    int64_t bs, L;
+    int32_t hq, hkv, hd, rd, ud, dtype, causal, mode, step;
+    float scale;
+};
+int launch_attn_simt(const AttnArgs &a, cudaStream_t s);
+int launch_attn_tc(const AttnArgs &a, cudaStream_t s);
+
+}  // namespace usp

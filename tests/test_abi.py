@@ -1,0 +1,124 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared symbol, and rejects bad
+arguments before anything touches a device. Runs without a GPU: none of these calls launches."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sequence_long_context_zigzag_gb300 as usp
+from sequence_long_context_zigzag_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"USP_API\s+[\w\s\*]*?\b(usp_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = _abi.load()
+    names = declared_symbols()
+    assert {"usp_extract_local", "usp_a2a4d", "usp_attn_fwd", "usp_lse_merge", "usp_check",
+            "usp_strerror", "usp_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_version_and_strerror():
+    lib = _abi.load()
+    assert lib.usp_version() >> 16 == 1
+    for code in range(0, -8, -1):
+        assert _abi.strerror(code)
+    assert _abi.strerror(0) == "success"
+    assert "unknown" in _abi.strerror(12345)
+
+
+def dims(bs=1, L=64, H=4, hd=128, dtype=_abi.USP_BF16, rd=2, ud=2, H_total=0, h0=0):
+    return _abi.UspDims(bs, L, H, hd, dtype, rd, ud, H_total, h0)
+
+
+BAD = 0x1001  # never dereferenced: every case below is rejected before a launch
+
+
+@pytest.mark.parametrize("d,code", [
+    (dims(L=62), _abi.USP_ERR_SHAPE),            # L % (2 rd) != 0
+    (dims(L=68, rd=2, ud=4), _abi.USP_ERR_SHAPE),  # (L/rd) % ud != 0
+    (dims(H=3), _abi.USP_ERR_SHAPE),             # heads % ud != 0 (a2a only)
+    (dims(dtype=7), _abi.USP_ERR_DTYPE),
+    (dims(rd=0), _abi.USP_ERR_INVALID_ARG),
+    (dims(hd=0), _abi.USP_ERR_INVALID_ARG),
+    (dims(H_total=4, h0=2), _abi.USP_ERR_SHAPE),  # window past the end
+])
+def test_a2a_rejects(d, code):
+    assert _abi.load().usp_a2a4d(BAD, BAD, d, 1, None) == code
+
+
+def test_a2a_rejects_direction_and_alignment():
+    lib = _abi.load()
+    assert lib.usp_a2a4d(BAD, BAD, dims(), 0, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_a2a4d(BAD, BAD, dims(), 1, None) == _abi.USP_ERR_ALIGN
+    assert lib.usp_a2a4d(None, BAD, dims(), 1, None) == _abi.USP_ERR_INVALID_ARG
+
+
+def test_extract_rejects():
+    lib = _abi.load()
+    assert lib.usp_extract_local(BAD, BAD, dims(L=62), -1, 0, None) == _abi.USP_ERR_SHAPE
+    assert lib.usp_extract_local(BAD, BAD, dims(), 4, 0, None) == _abi.USP_ERR_INVALID_ARG   # vr >= ud*rd
+    assert lib.usp_extract_local(BAD, BAD, dims(), -2, 0, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_extract_local(BAD, BAD, dims(), -1, 0, None) == _abi.USP_ERR_ALIGN
+    assert lib.usp_extract_local(BAD, BAD, dims(hd=3, dtype=_abi.USP_BF16), -1, 0, None) == \
+        _abi.USP_ERR_UNSUPPORTED   # 6-byte rows
+    # empty work is a no-op that succeeds without touching the device
+    assert lib.usp_extract_local(None, None, dims(L=0), -1, 0, None) == _abi.USP_OK
+    assert lib.usp_extract_local(None, None, dims(bs=0), -1, 1, None) == _abi.USP_OK
+
+
+def desc(**kw):
+    base = dict(bs=1, L=256, hq=4, hkv=2, hd=128, rd=2, ud=2, dtype=_abi.USP_BF16, causal=1, scale=0.0,
+                mode=0, step=0)
+    base.update(kw)
+    return _abi.UspAttnDesc(*[base[f] for f, _ in _abi.UspAttnDesc._fields_])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(hd=96), _abi.USP_ERR_UNSUPPORTED),
+    (dict(hq=6, hkv=4), _abi.USP_ERR_SHAPE),
+    (dict(hq=4, hkv=1, ud=2), _abi.USP_ERR_SHAPE),   # hkv % ud != 0 (MQA with ud > hkv)
+    (dict(L=250), _abi.USP_ERR_SHAPE),
+    (dict(mode=3), _abi.USP_ERR_INVALID_ARG),
+    (dict(mode=1, step=2), _abi.USP_ERR_INVALID_ARG),
+    (dict(dtype=5), _abi.USP_ERR_DTYPE),
+    (dict(scale=float("nan")), _abi.USP_ERR_INVALID_ARG),
+    (dict(), _abi.USP_ERR_ALIGN),
+])
+def test_attn_rejects(kw, code):
+    assert _abi.load().usp_attn_fwd(BAD, BAD, BAD, BAD, BAD, desc(**kw), None) == code
+
+
+def test_attn_null_and_empty():
+    lib = _abi.load()
+    assert lib.usp_attn_fwd(None, None, None, None, None, desc(), None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_attn_fwd(None, None, None, None, None, desc(L=0), None) == _abi.USP_OK
+
+
+def test_merge_rejects():
+    lib = _abi.load()
+    assert lib.usp_lse_merge(BAD, BAD, BAD, BAD, 10, 128, 9, None) == _abi.USP_ERR_DTYPE
+    assert lib.usp_lse_merge(BAD, BAD, BAD, BAD, 10, 4, _abi.USP_BF16, None) == _abi.USP_ERR_UNSUPPORTED
+    assert lib.usp_lse_merge(BAD, BAD, BAD, BAD, -1, 128, _abi.USP_BF16, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_lse_merge(BAD, BAD, BAD, BAD, 10, 128, _abi.USP_BF16, None) == _abi.USP_ERR_ALIGN
+    assert lib.usp_lse_merge(None, None, None, None, 0, 128, _abi.USP_BF16, None) == _abi.USP_OK
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        usp.usp_extract_local(x, x, 2, 1)

@@ -1,0 +1,133 @@
+"""GPU parity of the permutes (zigzag split, AllToAll4D and their inverses): bit-exact against the
+oracle's index maps, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_long_context_zigzag_gb300 as usp
+from seeded_inputs import WORKLOADS
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """Raw bit patterns of a tensor as an integer numpy array (bit-exact comparisons)."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy()
+    if t.dtype == torch.float32:
+        return t.view(torch.int32).numpy()
+    raise TypeError(t.dtype)
+
+
+def rand(shape, dtype, seed):
+    g = torch.Generator("cpu").manual_seed(seed)
+    return torch.randn(*shape, generator=g).to(dtype)
+
+
+CASES = [  # bs, L, H, hd, dtype, rd, ud
+    (1, 64, 4, 128, torch.bfloat16, 2, 2),
+    (2, 1000, 4, 128, torch.bfloat16, 4, 2),   # c = 125, Lu = 125: nothing aligned to 128
+    (1, 768, 6, 64, torch.bfloat16, 3, 2),
+    (1, 1024, 4, 64, torch.float32, 4, 1),
+    (2, 96, 8, 128, torch.float32, 1, 4),
+    (1, 240, 4, 96, torch.bfloat16, 5, 2),     # 192-byte rows: 12 vectors per row
+    (1, 128, 4, 1, torch.float32, 2, 2),       # lse-like 4-byte rows
+    (3, 48, 2, 8, torch.float32, 2, 1),        # 32-byte rows
+]
+
+
+@pytest.mark.parametrize("bs,L,H,hd,dtype,rd,ud", CASES)
+def test_extract_and_inverse_bitexact(bs, L, H, hd, dtype, rd, ud):
+    shape = (bs, L, H) if hd == 1 else (bs, L, H, hd)
+    x = rand(shape, dtype, seed=L + H + hd)
+    xd = x.to(DEV)
+    Lu = L // (rd * ud)
+    loc = torch.empty((rd, ud, bs, Lu, H) + (() if hd == 1 else (hd,)), dtype=dtype, device=DEV)
+    usp.usp_extract_local(xd, loc, rd, ud)
+    assert np.array_equal(bits(loc), oracle.extract_local(bits(x), rd, ud))
+    back = torch.full_like(xd, float("nan"))
+    usp.usp_extract_local(loc, back, rd, ud, inverse=True)
+    assert np.array_equal(bits(back), bits(x))
+    # one virtual rank at a time, as the pages' per-rank extract call does
+    ref = oracle.extract_local(bits(x), rd, ud)
+    for vr in range(rd * ud):
+        one = torch.empty(loc.shape[2:], dtype=dtype, device=DEV)
+        usp.usp_extract_local(xd, one, rd, ud, vr=vr)
+        assert np.array_equal(bits(one), ref[vr // ud, vr % ud])
+    usp.usp_check()
+
+
+@pytest.mark.parametrize("bs,L,H,hd,dtype,rd,ud", CASES)
+def test_a2a_and_inverse_bitexact(bs, L, H, hd, dtype, rd, ud):
+    Lu, Lr = L // (rd * ud), L // rd
+    tail = () if hd == 1 else (hd,)
+    loc = rand((rd, ud, bs, Lu, H) + tail, dtype, seed=7 * L + H)
+    locd = loc.to(DEV)
+    hs = torch.empty((rd, ud, H // ud, bs, Lr) + tail, dtype=dtype, device=DEV)
+    usp.usp_a2a4d(locd, hs, rd, ud, 1)
+    assert np.array_equal(bits(hs), oracle.a2a_fwd(bits(loc), ud))
+    back = torch.full_like(locd, float("nan"))
+    usp.usp_a2a4d(hs, back, rd, ud, -1)
+    assert np.array_equal(bits(back), bits(loc))
+    usp.usp_check()
+
+
+def test_head_windows_bitexact():
+    """Head groups (the head-chunk loop) read and write windows of the full tensors."""
+    bs, L, Ht, hd, rd, ud = 1, 256, 12, 128, 2, 2
+    x = rand((bs, L, Ht, hd), torch.bfloat16, seed=11)
+    xd = x.to(DEV)
+    Lu, Lr = L // (rd * ud), L // rd
+    for h0, H in ((0, 4), (4, 4), (8, 4), (2, 6)):
+        loc = torch.empty(rd, ud, bs, Lu, H, hd, dtype=torch.bfloat16, device=DEV)
+        usp.usp_extract_local(xd, loc, rd, ud, h0=h0, H=H)
+        assert np.array_equal(bits(loc), oracle.extract_local(bits(x), rd, ud, h0=h0, H=H))
+        hs = torch.empty(rd, ud, H // ud, bs, Lr, hd, dtype=torch.bfloat16, device=DEV)
+        usp.usp_a2a4d(loc, hs, rd, ud, 1)
+        # windowed inverse all-to-all into a full sequence-sharded tensor leaves other heads alone
+        full = torch.zeros(rd, ud, bs, Lu, Ht, hd, dtype=torch.bfloat16, device=DEV)
+        usp.usp_a2a4d(hs, full, rd, ud, -1, h0=h0, H=H)
+        f = bits(full)
+        assert np.array_equal(f[:, :, :, :, h0:h0 + H], bits(loc))
+        assert not f[:, :, :, :, :h0].any() and not f[:, :, :, :, h0 + H:].any()
+        # windowed inverse split into a natural tensor
+        nat = torch.zeros_like(xd)
+        usp.usp_extract_local(loc, nat, rd, ud, inverse=True, h0=h0, H=H)
+        n = bits(nat)
+        assert np.array_equal(n[:, :, h0:h0 + H], bits(x)[:, :, h0:h0 + H])
+        assert not n[:, :, :h0].any() and not n[:, :, h0 + H:].any()
+    usp.usp_check()
+
+
+@pytest.mark.parametrize("wi", [1, 2, 3, 4])
+def test_full_size_permutes(wi):
+    """At the workloads' full sizes and launch configuration: the composed split -> AllToAll4D ->
+    inverse AllToAll4D -> inverse split is the identity, and both intermediates equal the oracle's
+    index maps applied to the same bytes (bit-exact)."""
+    w = WORKLOADS[wi]
+    H = w.head_chunk or w.hq
+    rd, ud, bs, L, hd = w.rd, w.ud, w.bs, w.L, w.hd
+    Lu, Lr = L // (rd * ud), L // rd
+    # arbitrary 16-bit patterns moved as bf16 rows
+    g = torch.Generator(device=DEV).manual_seed(wi)
+    x = torch.randint(-30000, 30000, (bs, L, w.hq, hd), generator=g, device=DEV, dtype=torch.int16)
+    h0 = w.hq - H  # last head group
+    loc = torch.empty(rd, ud, bs, Lu, H, hd, dtype=torch.int16, device=DEV)
+    hs = torch.empty(rd, ud, H // ud, bs, Lr, hd, dtype=torch.int16, device=DEV)
+    bf = torch.bfloat16
+    usp.usp_extract_local(x.view(bf), loc.view(bf), rd, ud, h0=h0, H=H)
+    usp.usp_a2a4d(loc.view(bf), hs.view(bf), rd, ud, 1)
+    loc2 = torch.empty_like(loc)
+    usp.usp_a2a4d(hs.view(bf), loc2.view(bf), rd, ud, -1)
+    nat = torch.zeros_like(x)
+    usp.usp_extract_local(loc2.view(bf), nat.view(bf), rd, ud, inverse=True, h0=h0, H=H)
+    usp.usp_check()
+    assert torch.equal(nat[:, :, h0:], x[:, :, h0:])
+    assert torch.equal(loc2, loc)
+    xs = x.cpu().numpy()
+    ref_loc = oracle.extract_local(xs, rd, ud, h0=h0, H=H)
+    assert np.array_equal(loc.cpu().numpy(), ref_loc)
+    assert np.array_equal(hs.cpu().numpy(), oracle.a2a_fwd(ref_loc, ud))
