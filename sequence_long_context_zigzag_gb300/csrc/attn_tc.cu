@@ -277,6 +277,7 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
         ok = wait(C::K_FULL + 0, 0);
         tc::fence_after_sync();
         if (ok) {
+#pragma unroll
             for (int i = 0; i < 2; ++i)
                 if (cur.act[i]) {
                     issue_s<HD>(tmem, i, sQ, sK);
@@ -292,22 +293,27 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
         if (!(ok = wait(C::V_FULL + st, ph))) break;
         tc::fence_after_sync();
         bool kn_ready = false;
-        for (int i = 0; i < 2 && ok; ++i) {
-            if (cur.act[i]) {
-                if (!(ok = wait(C::P_FULL + i, pc[i] & 1u))) break;
-                ++pc[i];
-                tc::fence_after_sync();
-                issue_pv<HD>(tmem, i, sV + st * C::kTileBytes, started[i]);
-                started[i] = 1;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if (ok && cur.act[i]) {
+                ok = wait(C::P_FULL + i, pc[i] & 1u);
+                if (ok) {
+                    ++pc[i];
+                    tc::fence_after_sync();
+                    issue_pv<HD>(tmem, i, sV + st * C::kTileBytes, started[i]);
+                    started[i] = 1;
+                }
             }
-            if (have_n && nxt.act[i]) {
+            if (ok && have_n && nxt.act[i]) {
                 if (!kn_ready) {
-                    if (!(ok = wait(C::K_FULL + stn, phn))) break;
+                    ok = wait(C::K_FULL + stn, phn);
                     tc::fence_after_sync();
                     kn_ready = true;
                 }
-                issue_s<HD>(tmem, i, sQ, sK + stn * C::kTileBytes);
-                tc::mma_commit(BAR(C::S_FULL + i));
+                if (ok) {
+                    issue_s<HD>(tmem, i, sQ, sK + stn * C::kTileBytes);
+                    tc::mma_commit(BAR(C::S_FULL + i));
+                }
             }
         }
         if (!ok) break;
@@ -332,8 +338,8 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
-template <int HD>
-__device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem, int i) {
+template <int HD, int i>
+__device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem) {
     using C = Cfg<HD>;
     auto BAR = [&](int k) { return bar0 + 8u * k; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -537,7 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (lane == 0) mma_role<HD>(p, w, sbase, bar0, tmem);
         __syncwarp();
     } else {
-        softmax_role<HD>(p, w, bar0, tmem, warp >> 2);
+        if (warp < 4)
+            softmax_role<HD, 0>(p, w, bar0, tmem);
+        else
+            softmax_role<HD, 1>(p, w, bar0, tmem);
     }
     tc::fence_before_sync();
     __syncthreads();
