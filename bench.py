@@ -33,7 +33,7 @@ from seeded_inputs import WORKLOADS, default_seed, make_rows, make_workload_qkv 
 DEFAULT_WORKLOAD = 1
 L2_BYTES = 129 * 10 ** 6
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_tc_kernel_mha_L8192.md")
 ATTN_SRC = os.path.join(ROOT, "sequence_long_context_zigzag_gb300", "csrc", "attn_tc.cu")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -219,19 +219,25 @@ class Step:
                 self.perm_events.append((e0, e1, e2, e3))
 
 
-def traffic_for_current_kernel():
-    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on the
-    attention kernel source as it is now (else None)."""
+def traffic_for_current_kernel(workload_index):
+    """DRAM bytes per attention launch (read + write) from the committed ncu summary, if it was taken
+    on this workload and on the attention kernel source as it is now (else None)."""
+    if workload_index != DEFAULT_WORKLOAD:
+        return None
     try:
+        rec = {}
         with open(TRAFFIC_FILE) as f:
-            rec = json.load(f)
+            for line in f:
+                k, sep, v = line.partition(":")
+                if sep:
+                    rec[k.strip()] = v.strip()
         with open(ATTN_SRC, "rb") as f:
             h = hashlib.sha256(f.read()).hexdigest()[:16]
-    except (OSError, ValueError):
+    except OSError:
         return None
-    if rec.get("attn_src_sha256_16") != h:
+    if rec.get("attn_src_sha256_16") != h or "dram_bytes_per_launch" not in rec:
         return None
-    return rec.get("dram_bytes_per_launch")
+    return int(rec["dram_bytes_per_launch"])
 
 
 # ------------------------------------------------------------------------------------------------
@@ -415,7 +421,7 @@ def main():
             "permute_gbs": perm_gbs,
             "permute_frac_of_hbm": perm_gbs / hbm,
             "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": attn_tflops / peak, "traffic": traffic_for_current_kernel(),
+                         "frac": attn_tflops / peak, "traffic": traffic_for_current_kernel(wi),
                          "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)",
                          "kernel": "usp_attn_fwd (bf16 ring attention)",
                          "algorithmic_flops_per_launch": per_group_flops},

@@ -338,20 +338,64 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
-template <int HD, int i>
-__device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem) {
+// columns at or beyond the row's key limit (relative to the tile) get score -inf
+__device__ __forceinline__ void mask_chunk(uint32_t (&r)[32], int col0, int lim_local) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        if (col0 + e >= lim_local) r[e] = __float_as_uint(-INFINITY);
+}
+
+__device__ __forceinline__ float chunk_max(const uint32_t (&r)[32]) {
+    float a = u2f(r[0]), b = u2f(r[1]);
+#pragma unroll
+    for (int e = 2; e < 30; e += 4) {
+        a = tc::max3(a, u2f(r[e]), u2f(r[e + 1]));
+        b = tc::max3(b, u2f(r[e + 2]), u2f(r[e + 3]));
+    }
+    a = tc::max3(a, u2f(r[30]), u2f(r[31]));
+    return fmaxf(a, b);
+}
+
+// P = 2^(s * scale*log2e - mb) for one 32-column chunk: accumulate the row sum, pack to bf16 pairs
+__device__ __forceinline__ void chunk_exp(const uint32_t (&r)[32], uint64_t sl22, uint64_t nmb2, uint64_t &sacc,
+                                          uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const uint64_t y = tc::fma2(tc::pack2(u2f(r[2 * e]), u2f(r[2 * e + 1])), sl22, nmb2);
+        float y0, y1;
+        tc::unpack2(y, y0, y1);
+        const float p0 = tc::ex2(y0), p1 = tc::ex2(y1);
+        sacc = tc::add2(sacc, tc::pack2(p0, p1));
+        pk[e] = float2_to_bf16x2(p0, p1);
+    }
+}
+
+// One softmax warpgroup (i = 0 or 1, one thread per query row of Q tile i). S is streamed through
+// registers 32 columns at a time, the next chunk's TMEM load overlapping the current chunk's math.
+// Exponentials use the running max m_used; a row whose tile max exceeds m_used + 2^8 takes the rare
+// path, which raises m_used to the max of the remaining chunks and rescales what was already
+// produced with the old max (P chunks in TMEM, O in TMEM, the sums). At most one rare path per tile:
+// afterwards no remaining column exceeds the new max. The first visible tile computes its exact max
+// first (a separate pass), so it never takes the rare path.
+template <int HD>
+__device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem, int i) {
     using C = Cfg<HD>;
-    auto BAR = [&](int k) { return bar0 + 8u * k; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wq = warp & 3;
     const uint32_t row = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::colS(i);
-    const uint32_t tO = tmem + lane_off + C::colO(i);
-    const uint32_t row_local = w.q0[i] + row;
-    const bool row_ok = w.valid[i] && row_local < p.Lr;
+    const uint32_t tS = tmem + lane_off + 128u * (uint32_t)i;
+    const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(HD * i);
+    const uint32_t barS = bar0 + 8u * (C::S_FULL + i);
+    const uint32_t barP = bar0 + 8u * (C::P_FULL + i);
+    const uint32_t barO = bar0 + 8u * (C::O_FULL + i);
+    const uint32_t q0 = i ? w.q0[1] : w.q0[0];
+    const bool valid = i ? w.valid[1] : w.valid[0];
+    const uint32_t row_local = q0 + row;
+    const bool row_ok = valid && row_local < p.Lr;
     const int64_t qpos_row = zig_pos(w.r, min(row_local, p.Lr - 1), p.c, p.rd);
     const float sl2 = p.scale_log2;
+    const uint64_t sl22 = tc::pack2(sl2, sl2);
 
     float m_used = -INFINITY, l = 0.f;
     uint32_t n_act = 0;
@@ -362,74 +406,108 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     uint32_t s_cur = 0xffffffffu;
     int64_t lim = 0;
     while (iter_next(p, w, it, tl)) {
-        if (!tl.act[i]) continue;
+        const bool act = i ? tl.act[1] : tl.act[0];
+        if (!act) continue;
+        const bool full = i ? tl.full[1] : tl.full[0];
         if (tl.s != s_cur) {
             s_cur = tl.s;
             lim = p.causal ? visible_prefix(qpos_row, s_cur, p.c, p.rd) : (int64_t)p.Lr;
         }
-        ok = tc::mbar_wait(BAR(C::S_FULL + i), n_act & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+        ok = tc::mbar_wait(barS, n_act & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc::fence_after_sync();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tc::tmem_ld32(tS + cc * 32, sr[cc]);
-        tc::tmem_ld_wait();
-        if (!tl.full[i]) {
-            int64_t ll = lim - (int64_t)tl.kt * kN;
-            const int lim_local = ll < 0 ? 0 : (ll > kN ? kN : (int)ll);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (cc * 32 + e >= lim_local) sr[cc][e] = __float_as_uint(-INFINITY);
+        int lim_local = kN;
+        if (!full) {
+            const int64_t ll = lim - (int64_t)tl.kt * kN;
+            lim_local = ll < 0 ? 0 : (ll > kN ? kN : (int)ll);
         }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, u2f(sr[cc][e]));
-        const float m_new = fmaxf(m_used, mx * sl2);
-        const bool need = m_new > m_used + kRescaleThreshold;
-        float alpha = 1.f;
-        if (need) {
-            alpha = tc::ex2(m_used - m_new);  // 0 on the first visible tile (m_used = -inf)
-            m_used = m_new;
-        }
-        if (n_act > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-            for (int oc = 0; oc < HD / 32; ++oc) {
-                uint32_t o[32];
-                tc::tmem_ld32(tO + oc * 32, o);
+        if (n_act == 0) {
+            // first visible tile: the exact row max first
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t r[32];
+                tc::tmem_ld32(tS + cc * 32, r);
                 tc::tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
-                tc::tmem_st32(tO + oc * 32, o);
+                if (!full) mask_chunk(r, cc * 32, lim_local);
+                mx = fmaxf(mx, chunk_max(r));
             }
+            m_used = mx * sl2;
         }
-        l *= alpha;
-        const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-        float sum = 0.f;
+        uint64_t sacc = tc::pack2(0.f, 0.f);
+        uint32_t ra[32], rb[32];
+        tc::tmem_ld32(tS, ra);
+        tc::tmem_ld_wait();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t pk[32];
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t(&cur)[32] = (cc & 1) ? rb : ra;
+            uint32_t(&nxt)[32] = (cc & 1) ? ra : rb;
+            if (cc < 3) tc::tmem_ld32(tS + (cc + 1) * 32, nxt);
+            if (!full) mask_chunk(cur, cc * 32, lim_local);
+            const float cmax = chunk_max(cur) * sl2;
+            if (__any_sync(0xffffffffu, cmax > m_used + kRescaleThreshold)) {
+                // rare path (warp-uniform): new max over the remaining chunks of this tile
+                tc::tmem_ld_wait();
+                float mrest = -INFINITY;
+#pragma unroll 1
+                for (int c2 = cc; c2 < 4; ++c2) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(tS + c2 * 32, r);
+                    tc::tmem_ld_wait();
+                    if (!full) mask_chunk(r, c2 * 32, lim_local);
+                    mrest = fmaxf(mrest, chunk_max(r));
+                }
+                const float m_new = fmaxf(m_used, mrest * sl2);
+                const bool need = m_new > m_used + kRescaleThreshold;
+                const float alpha = need ? tc::ex2(m_used - m_new) : 1.f;  // 0 when m_used = -inf
+                if (need) m_used = m_new;
+                // rescale the P chunks already written with the old max
+                tc::tmem_st_wait();
+#pragma unroll 1
+                for (int c2 = 0; c2 < cc; ++c2) {
+                    uint32_t pr[16];
+                    tc::tmem_ld16(tS + c2 * 16, pr);
+                    tc::tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int col = half * 64 + 2 * e;
-                const float x0 = u2f(sr[col / 32][col % 32]);
-                const float x1 = u2f(sr[(col + 1) / 32][(col + 1) % 32]);
-                const float p0 = tc::ex2(fmaf(x0, sl2, -mb));
-                const float p1 = tc::ex2(fmaf(x1, sl2, -mb));
-                sum += p0 + p1;
-                pk[e] = float2_to_bf16x2(p0, p1);
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 f = bf16x2_to_float2(pr[e]);
+                        pr[e] = float2_to_bf16x2(f.x * alpha, f.y * alpha);
+                    }
+                    tc::tmem_st16(tS + c2 * 16, pr);
+                }
+                if (n_act > 0) {
+#pragma unroll 1
+                    for (int oc = 0; oc < HD / 32; ++oc) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(tO + oc * 32, o);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
+                        tc::tmem_st32(tO + oc * 32, o);
+                    }
+                }
+                l *= alpha;
+                sacc = tc::fma2(sacc, tc::pack2(alpha, alpha), tc::pack2(0.f, 0.f));
+                // reload the current chunk and the prefetched next one
+                tc::tmem_ld32(tS + cc * 32, cur);
+                if (cc < 3) tc::tmem_ld32(tS + (cc + 1) * 32, nxt);
+                tc::tmem_ld_wait();
+                if (!full) mask_chunk(cur, cc * 32, lim_local);
             }
-            tc::tmem_st32(tS + half * 32, pk);
+            const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+            uint32_t pk[16];
+            chunk_exp(cur, sl22, tc::pack2(-mb, -mb), sacc, pk);
+            tc::tmem_st16(tS + cc * 16, pk);
+            if (cc < 3) tc::tmem_ld_wait();
         }
-        l += sum;
+        float s0, s1;
+        tc::unpack2(sacc, s0, s1);
+        l += s0 + s1;
         tc::tmem_st_wait();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(BAR(C::P_FULL + i));
+        if (lane == 0) tc::mbar_arrive(barP);
         ++n_act;
     }
     if (!ok) return;
@@ -441,7 +519,7 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16 *orow = p.out + grow * HD;
     if (n_act > 0) {
-        ok = tc::mbar_wait(BAR(C::O_FULL + i), 0, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+        ok = tc::mbar_wait(barO, 0, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) return;
         tc::fence_after_sync();
@@ -543,10 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (lane == 0) mma_role<HD>(p, w, sbase, bar0, tmem);
         __syncwarp();
     } else {
-        if (warp < 4)
-            softmax_role<HD, 0>(p, w, bar0, tmem);
-        else
-            softmax_role<HD, 1>(p, w, bar0, tmem);
+        softmax_role<HD>(p, w, bar0, tmem, warp >> 2);
     }
     tc::fence_before_sync();
     __syncthreads();
