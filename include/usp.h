@@ -28,6 +28,7 @@
 #ifndef USP_H
 #define USP_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -102,6 +103,27 @@ USP_API int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, in
  */
 USP_API int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stream);
 
+/*
+ * usp_extract_a2a -- the zigzag split followed by AllToAll4D (steps a1 + a2) in one pass, for up to
+ * four tensors (e.g. Q, K and V) in one launch; inverse != 0 runs AllToAll4D's inverse followed by
+ * the inverse split (a5 + a7).
+ * Source: USP review, Algorithm 2 and section 三 (AllToAll4D). Composing the two maps gives
+ *   head-sharded[r][u'][h'][b][p] = natural[b][zig(r, p)][h0 + u' Hl + h'],
+ * i.e. row p of ring rank r is global token zig(r, p) (the all-to-all gathers the Ulysses ranks'
+ * pieces in rank order, which restores Algorithm 2's ring-local sequence). Bit-exactly the result of
+ * usp_extract_local (vr = -1) then usp_a2a4d (dir = +1), with one read and one write per tensor.
+ *
+ *   n         : number of tensors, 1 <= n <= 4
+ *   src, dst  : HOST arrays of n DEVICE pointers. inverse == 0: src[k] natural (bs, L, H_total, hd),
+ *               dst[k] head-sharded [rd][ud][H/ud][bs][Lr][hd]; inverse != 0: the other way round
+ *               (heads outside the window of the natural tensor are left untouched).
+ *   d         : HOST array of n dims; bs, L, rd, ud, hd and dtype must agree (USP_ERR_SHAPE
+ *               otherwise); H, H_total and h0 may differ (Q and K/V head counts under GQA).
+ * Alignment and overlap rules as for usp_extract_local.
+ */
+USP_API int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_dims *d, int inverse,
+                            usp_stream_t stream);
+
 /* Attention modes (step a3 with the merge of step a4). */
 typedef enum {
     USP_MODE_FUSED = 0, /* the whole ring: every ring step folded into one online softmax */
@@ -153,6 +175,45 @@ USP_API int usp_attn_fwd(const void *q, const void *k, const void *v, void *out,
  */
 USP_API int usp_lse_merge(void *o_acc, float *lse_acc, const void *o_new, const float *lse_new, int64_t rows,
                   int32_t hd, int32_t dtype, usp_stream_t stream);
+
+/*
+ * usp_forward -- the whole USP-Attention forward on device buffers: for every head group, the split
+ * and AllToAll4D of Q, K, V (usp_extract_a2a), the ring attention (usp_attn_fwd, USP_MODE_FUSED) and
+ * the inverse AllToAll4D + inverse split of out and lse back to natural order.
+ * Source: USP review, Algorithm 1 (steps 1-5) and Algorithm 2; the head groups follow the UPipe
+ * page's headwise chunking (the result does not depend on the grouping).
+ *
+ *   q                : (bs, L, hq, hd) natural order;  k, v : (bs, L, hkv, hd)
+ *   out              : (bs, L, hq, hd) natural order;  lse  : (bs, L, hq) fp32, natural log
+ *   d                : as for usp_attn_fwd; d.mode must be USP_MODE_FUSED
+ *   head_chunk       : query heads per group (0 = all); must divide hq and be a multiple of hq/hkv;
+ *                      the group's query and KV head counts must divide by ud
+ *   workspace        : DEVICE buffer, 256-byte aligned, at least usp_forward_workspace_size(d,
+ *                      head_chunk, 0) bytes; owned by the caller, clobbered by the call
+ * Asynchronous on `stream`; calls that share a workspace must be ordered on one stream.
+ */
+USP_API int usp_forward(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d,
+                        int head_chunk, void *workspace, size_t workspace_bytes, usp_stream_t stream);
+
+/*
+ * usp_forward_host -- usp_forward from HOST input buffers to HOST output buffers (same layouts),
+ * pipelined per head group: the host-to-device copy of group g+1 and the device-to-host copy of
+ * group g-1 overlap the kernels of group g, on three streams the library keeps per device. The whole
+ * call is ordered after earlier work on `stream`, and later work on `stream` waits for it (the host
+ * outputs are complete once `stream` is synchronised). Host buffers should be pinned
+ * (cudaHostAlloc / cudaHostRegister); pageable buffers work but the copies then do not overlap.
+ *   workspace : DEVICE buffer of at least usp_forward_workspace_size(d, head_chunk, 1) bytes
+ *               (two staging slots per direction plus the full lse), 256-byte aligned.
+ * Calls on one device are serialised on the library's streams; calls that share a workspace must be
+ * ordered on one stream.
+ */
+USP_API int usp_forward_host(const void *q_host, const void *k_host, const void *v_host, void *out_host,
+                             float *lse_host, usp_attn_desc d, int head_chunk, void *workspace,
+                             size_t workspace_bytes, usp_stream_t stream);
+
+/* Bytes of workspace usp_forward (host_buffers == 0) or usp_forward_host (host_buffers != 0) needs;
+ * 0 if the arguments are invalid. */
+USP_API size_t usp_forward_workspace_size(usp_attn_desc d, int head_chunk, int host_buffers);
 
 /* Synchronise `stream`, then report (and clear) the device status word of the current device:
  * USP_OK, USP_ERR_TIMEOUT, or USP_ERR_CUDA if the synchronisation itself failed. */

@@ -13,6 +13,7 @@ Layouts (all row-major; see include/usp.h for the index formulas):
 """
 from __future__ import annotations
 
+import ctypes
 import math
 from typing import Optional
 
@@ -22,7 +23,8 @@ from . import _abi
 from ._abi import (USP_BF16, USP_F32, USP_MODE_ACCUM, USP_MODE_FUSED, USP_MODE_STEP, UspAttnDesc, UspDims,
                    UspError)
 
-__all__ = ["usp_extract_local", "usp_a2a4d", "usp_attn_fwd", "usp_lse_merge", "usp_check", "usp_attention",
+__all__ = ["usp_extract_local", "usp_a2a4d", "usp_extract_a2a", "usp_attn_fwd", "usp_lse_merge", "usp_check", "usp_attention",
+           "usp_attention_host", "usp_forward", "usp_forward_host", "usp_forward_workspace_size",
            "UspAttention", "UspError", "USP_MODE_FUSED", "USP_MODE_STEP", "USP_MODE_ACCUM", "lib_path"]
 
 lib_path = _abi.LIB_PATH
@@ -115,6 +117,41 @@ def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int =
     return dst
 
 
+def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=None, Hs=None, stream=None):
+    """Zigzag split then AllToAll4D in one pass (inverse: AllToAll4D's inverse then the inverse split),
+    for up to four tensors in one launch. inverse=False: srcs[k] natural (bs, L, H_total, hd) (or
+    (bs, L, H_total) for lse) -> dsts[k] head-sharded [rd][ud][H/ud][bs][Lr](, hd); inverse=True the
+    other way round. Tensor k moves heads [h0s[k], h0s[k] + Hs[k]) of its natural tensor."""
+    srcs, dsts = list(srcs), list(dsts)
+    n = len(srcs)
+    _need(1 <= n <= 4 and len(dsts) == n, "one to four tensors")
+    h0s = [0] * n if h0s is None else list(h0s)
+    Hs = [None] * n if Hs is None else list(Hs)
+    dims, sp, dp = [], [], []
+    for k in range(n):
+        src, dst = srcs[k], dsts[k]
+        _dev(src, dst)
+        nat, hs = (dst, src) if inverse else (src, dst)
+        _need(nat.dtype == hs.dtype, "dtype mismatch")
+        if nat.dim() == 3:
+            bs, L, Ht = nat.shape
+            hd = 1
+        else:
+            _need(nat.dim() == 4, "natural tensor must be (bs, L, H, hd) or (bs, L, H)")
+            bs, L, Ht, hd = nat.shape
+        H = Ht - h0s[k] if Hs[k] is None else Hs[k]
+        _need(0 <= h0s[k] and h0s[k] + H <= Ht, "head window out of range")
+        _need(L % (2 * rd) == 0 and (L // rd) % ud == 0 and H % ud == 0, "shape not divisible")
+        _need(hs.numel() == bs * L * H * hd, "head-sharded tensor has the wrong size")
+        dims.append(UspDims(bs, L, H, hd, _dtype_code(nat), rd, ud, Ht, h0s[k]))
+        sp.append(_ptr(src))
+        dp.append(_ptr(dst))
+    vp = ctypes.c_void_p
+    _abi.check("usp_extract_a2a", _abi.load().usp_extract_a2a(
+        n, (vp * n)(*sp), (vp * n)(*dp), (UspDims * n)(*dims), int(bool(inverse)), _stream(stream)))
+    return dsts
+
+
 def usp_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
                  causal: bool = True, scale: Optional[float] = None, mode: int = USP_MODE_FUSED, step: int = 0,
                  stream=None):
@@ -179,12 +216,14 @@ def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd
     _need(L % (2 * rd) == 0 and (L // rd) % ud == 0, "L must split into 2*rd chunks and L/rd into ud parts")
     Lu, Lr = L // (rd * ud), L // rd
     dev, dt = q.device, q.dtype
-    o_loc = torch.empty(rd, ud, bs, Lu, hq, hd, device=dev, dtype=dt)
-    l_loc = torch.empty(rd, ud, bs, Lu, hq, device=dev, dtype=torch.float32)
+    if natural_output:
+        out = torch.empty(bs, L, hq, hd, device=dev, dtype=dt)
+        lse = torch.empty(bs, L, hq, device=dev, dtype=torch.float32)
+        usp_forward(q, k, v, out, lse, ud, rd, causal=causal, scale=scale, head_chunk=head_chunk, stream=stream)
+        return out, lse
+    out = torch.empty(rd, ud, bs, Lu, hq, hd, device=dev, dtype=dt)
+    lse = torch.empty(rd, ud, bs, Lu, hq, device=dev, dtype=torch.float32)
     # per-group workspace, reused across groups
-    ql = torch.empty(rd, ud, bs, Lu, hc, hd, device=dev, dtype=dt)
-    kl = torch.empty(rd, ud, bs, Lu, hkc, hd, device=dev, dtype=dt)
-    vl = torch.empty_like(kl)
     qh = torch.empty(rd, ud, hc // ud, bs, Lr, hd, device=dev, dtype=dt)
     kh = torch.empty(rd, ud, hkc // ud, bs, Lr, hd, device=dev, dtype=dt)
     vh = torch.empty_like(kh)
@@ -192,21 +231,87 @@ def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd
     lh = torch.empty(rd, ud, hc // ud, bs, Lr, device=dev, dtype=torch.float32)
     for g0 in range(0, hq, hc):
         gk = g0 // G
-        usp_extract_local(q, ql, rd, ud, h0=g0, H=hc, stream=stream)
-        usp_extract_local(k, kl, rd, ud, h0=gk, H=hkc, stream=stream)
-        usp_extract_local(v, vl, rd, ud, h0=gk, H=hkc, stream=stream)
-        usp_a2a4d(ql, qh, rd, ud, 1, stream=stream)
-        usp_a2a4d(kl, kh, rd, ud, 1, stream=stream)
-        usp_a2a4d(vl, vh, rd, ud, 1, stream=stream)
+        # a1 + a2: zigzag split and AllToAll4D of Q, K, V in one launch
+        usp_extract_a2a([q, k, v], [qh, kh, vh], rd, ud, h0s=[g0, gk, gk], Hs=[hc, hkc, hkc], stream=stream)
+        # a3 + a4: the ring with the fused LSE merge
         usp_attn_fwd(qh, kh, vh, oh, lh, causal=causal, scale=scale, stream=stream)
-        usp_a2a4d(oh, o_loc, rd, ud, -1, h0=g0, H=hc, stream=stream)
-        usp_a2a4d(lh, l_loc, rd, ud, -1, h0=g0, H=hc, stream=stream)
-    if not natural_output:
-        return o_loc, l_loc
-    out = torch.empty(bs, L, hq, hd, device=dev, dtype=dt)
-    lse = torch.empty(bs, L, hq, device=dev, dtype=torch.float32)
-    usp_extract_local(o_loc, out, rd, ud, inverse=True, stream=stream)
-    usp_extract_local(l_loc, lse, rd, ud, inverse=True, stream=stream)
+        # a5 on out and lse: back to the sequence-sharded layout a model keeps
+        usp_a2a4d(oh, out, rd, ud, -1, h0=g0, H=hc, stream=stream)
+        usp_a2a4d(lh, lse, rd, ud, -1, h0=g0, H=hc, stream=stream)
+    return out, lse
+
+
+def _forward_desc(q, k, ud, rd, causal, scale):
+    bs, L, hq, hd = q.shape
+    hkv = k.shape[2]
+    return UspAttnDesc(bs, L, hq, hkv, hd, rd, ud, _dtype_code(q), int(bool(causal)),
+                       float(scale) if scale is not None else 0.0, USP_MODE_FUSED, 0)
+
+
+def usp_forward_workspace_size(q, k, ud: int, rd: int, head_chunk: Optional[int] = None, host: bool = False,
+                               causal: bool = True) -> int:
+    """Workspace bytes usp_forward / usp_forward_host need for these shapes."""
+    d = _forward_desc(q, k, ud, rd, causal, None)
+    n = _abi.load().usp_forward_workspace_size(d, int(head_chunk or 0), int(bool(host)))
+    _need(n > 0, "invalid forward shapes")
+    return int(n)
+
+
+def _check_natural(q, k, v, out, lse):
+    bs, L, hq, hd = q.shape
+    hkv = k.shape[2]
+    _need(k.shape == (bs, L, hkv, hd) and v.shape == k.shape, "k/v shape mismatch")
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    _need(lse.shape == (bs, L, hq) and lse.dtype == torch.float32, "lse must be fp32 (bs, L, hq)")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype, "dtype mismatch")
+
+
+def usp_forward(q, k, v, out, lse, ud: int, rd: int, causal: bool = True, scale: Optional[float] = None,
+                head_chunk: Optional[int] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """The whole forward on device buffers in one C call (natural-order in and out)."""
+    _dev(q, k, v, out, lse)
+    _check_natural(q, k, v, out, lse)
+    d = _forward_desc(q, k, ud, rd, causal, scale)
+    n = usp_forward_workspace_size(q, k, ud, rd, head_chunk, host=False, causal=causal)
+    if workspace is None:
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _need(workspace.numel() >= n and workspace.is_cuda, "workspace too small")
+    _abi.check("usp_forward", _abi.load().usp_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d,
+                                                     int(head_chunk or 0), _ptr(workspace), workspace.numel(),
+                                                     _stream(stream)))
+    return out, lse
+
+
+def usp_forward_host(q, k, v, out, lse, ud: int, rd: int, causal: bool = True, scale: Optional[float] = None,
+                     head_chunk: Optional[int] = None, workspace: Optional[torch.Tensor] = None, device=None,
+                     stream=None):
+    """The whole forward from host tensors to host tensors (pin them for overlapped copies), pipelined
+    per head group inside the library. Work is queued on ``stream`` (the current stream of ``device``);
+    synchronise it before reading ``out`` / ``lse``."""
+    for t in (q, k, v, out, lse):
+        _need(isinstance(t, torch.Tensor) and not t.is_cuda and t.is_contiguous(), "expected contiguous host tensors")
+    _check_natural(q, k, v, out, lse)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    d = _forward_desc(q, k, ud, rd, causal, scale)
+    n = usp_forward_workspace_size(q, k, ud, rd, head_chunk, host=True, causal=causal)
+    if workspace is None:
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    _need(workspace.numel() >= n and workspace.is_cuda, "workspace too small")
+    with torch.cuda.device(dev):
+        _abi.check("usp_forward_host", _abi.load().usp_forward_host(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d, int(head_chunk or 0), _ptr(workspace),
+            workspace.numel(), _stream(stream)))
+    return out, lse
+
+
+def usp_attention_host(q, k, v, ud: int, rd: int, causal: bool = True, scale: Optional[float] = None,
+                       head_chunk: Optional[int] = None, device=None):
+    """usp_attention for host tensors: allocates pinned outputs, runs usp_forward_host, waits."""
+    bs, L, hq, hd = q.shape
+    out = torch.empty(bs, L, hq, hd, dtype=q.dtype).pin_memory()
+    lse = torch.empty(bs, L, hq, dtype=torch.float32).pin_memory()
+    usp_forward_host(q, k, v, out, lse, ud, rd, causal=causal, scale=scale, head_chunk=head_chunk, device=device)
+    torch.cuda.current_stream(device).synchronize()
     return out, lse
 
 

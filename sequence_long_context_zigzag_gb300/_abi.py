@@ -61,6 +61,15 @@ def load():
     lib.usp_extract_local.restype = ctypes.c_int
     lib.usp_a2a4d.argtypes = [vp, vp, UspDims, ctypes.c_int, vp]
     lib.usp_a2a4d.restype = ctypes.c_int
+    lib.usp_extract_a2a.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(UspDims),
+                                    ctypes.c_int, vp]
+    lib.usp_extract_a2a.restype = ctypes.c_int
+    lib.usp_forward.argtypes = [vp, vp, vp, vp, vp, UspAttnDesc, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.usp_forward.restype = ctypes.c_int
+    lib.usp_forward_host.argtypes = [vp, vp, vp, vp, vp, UspAttnDesc, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.usp_forward_host.restype = ctypes.c_int
+    lib.usp_forward_workspace_size.argtypes = [UspAttnDesc, ctypes.c_int, ctypes.c_int]
+    lib.usp_forward_workspace_size.restype = ctypes.c_size_t
     lib.usp_attn_fwd.argtypes = [vp, vp, vp, vp, vp, UspAttnDesc, vp]
     lib.usp_attn_fwd.restype = ctypes.c_int
     lib.usp_lse_merge.argtypes = [vp, vp, vp, vp, i64, i32, i32, vp]

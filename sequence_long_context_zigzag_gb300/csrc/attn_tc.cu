@@ -10,6 +10,7 @@
 //
 // Kernel design (one CTA = 256 query rows = two 128-row Q tiles of one (r, u, h, b)):
 //   warp 8      TMA producer: Q0, Q1 once; K and V tiles (128 keys x hd) through a ring of stages.
+//               The producer and MMA warps run their loops warp-wide; one lane issues the copies/MMAs.
 //   warp 9      MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V on tcgen05 (kind::f16, bf16 in,
 //               fp32 accumulators in tensor memory), issue order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
 //               so the tensor core works on one tile while the other tile's softmax runs.
@@ -18,6 +19,8 @@
 //               rescale (O and l are rescaled only when the max grows by more than 2^8), writes
 //               P = 2^(S*scale*log2e - m) as bf16 back into TMEM (the A operand of the PV MMA), and
 //               finally normalises O and writes out (bf16) and lse (fp32).
+//   warps 10-11 hold no role; with warps 8-9 they form the control warpgroup that hands registers
+//               to the softmax warpgroups (setmaxnreg).
 //   TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+hd) O1 [256+hd, 256+2hd); P_i aliases S_i.
 // The causal structure is exploited per (Q tile, KV tile) pair from global positions: tiles wholly
 // after the queries are skipped (never loaded), tiles wholly before are unmasked, the rest are
@@ -36,10 +39,15 @@ namespace {
 
 constexpr int kM = 128;  // query rows per tile
 constexpr int kN = 128;  // keys per tile
-constexpr int kWarps = 10;
+constexpr int kWarps = 12;  // warpgroups: softmax 0 (warps 0-3), softmax 1 (4-7), control (8-11)
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// Register split per warpgroup (setmaxnreg). The launch grants 384 threads x 168 registers = 64512;
+// the softmax warpgroups take 2 x 128 x 208 = 53248 and the control warpgroup keeps 128 x 88 = 11264:
+// 64512 in total, so the increase can always be granted.
+constexpr int kSoftmaxRegs = 208;
+constexpr int kControlRegs = 88;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
@@ -80,28 +88,42 @@ struct TcParams {
     float scale_log2;
 };
 
-// The work of one CTA and the walk over its KV tiles (identical in every role).
+// The work of one CTA and the walk over its KV tiles (identical in every role). Positions and row
+// indices fit in 31 bits (the entry point rejects larger tensors), so 32-bit arithmetic is used.
 struct Work {
     uint32_t r, u, hl, b, kh;
-    int64_t q_row_base;   // row of local row 0 of (r, u, hl, b) in q / out / lse
+    uint32_t q_row_base;  // row of local row 0 of (r, u, hl, b) in q / out / lse
     uint32_t q0[2];       // first local row of each Q tile
     bool valid[2];
-    int64_t qpos_min[2], qpos_max[2];
+    uint32_t qpos_min[2], qpos_max[2];
     int t_begin, t_end;
 };
 
 struct Tile {
     uint32_t s, kt;
-    int64_t kv_row;  // first row of the tile in k / v
-    bool act[2];     // the Q tile needs this KV tile
-    bool full[2];    // every key of the tile is visible to every row of the Q tile
+    uint32_t kv_row;  // first row of the tile in k / v
+    bool act[2];      // the Q tile needs this KV tile
+    bool full[2];     // every key of the tile is visible to every row of the Q tile
 };
 
 struct TileIter {
     int t;
     uint32_t kt, nkt, s;
-    int64_t nhi[2], nlo[2];
+    uint32_t nhi[2], nlo[2];
 };
+
+// global position of ring-local row p on ring rank r (chunk length c): chunks r and 2 rd - 1 - r
+__device__ __forceinline__ uint32_t zig32(uint32_t r, uint32_t p, uint32_t c, uint32_t rd) {
+    return p < c ? r * c + p : (2 * rd - 1 - r) * c + (p - c);
+}
+
+// number of ring-local rows of rank s whose global position is <= qpos (a prefix: zig is increasing)
+__device__ __forceinline__ uint32_t vis32(uint32_t qpos, uint32_t s, uint32_t c, uint32_t rd) {
+    const uint32_t a0 = s * c, a1 = (2 * rd - 1 - s) * c;
+    const uint32_t c0 = qpos < a0 ? 0u : min(qpos - a0 + 1, c);
+    const uint32_t c1 = qpos < a1 ? 0u : min(qpos - a1 + 1, c);
+    return c0 + c1;
+}
 
 __device__ __forceinline__ Work decode_work(const TcParams &p) {
     Work w;
@@ -127,13 +149,13 @@ __device__ __forceinline__ Work decode_work(const TcParams &p) {
         qp = outer % p.npairs;
     }
     w.kh = w.hl / p.G;
-    w.q_row_base = ((((int64_t)w.r * p.ud + w.u) * p.Hl + w.hl) * p.bs + w.b) * p.Lr;
+    w.q_row_base = (((w.r * p.ud + w.u) * p.Hl + w.hl) * p.bs + w.b) * p.Lr;
     for (int i = 0; i < 2; ++i) {
         w.q0[i] = qp * 256 + i * 128;
         w.valid[i] = w.q0[i] < p.Lr;
         const uint32_t last = min(w.q0[i] + 127, p.Lr - 1);
-        w.qpos_min[i] = zig_pos(w.r, min(w.q0[i], p.Lr - 1), p.c, p.rd);
-        w.qpos_max[i] = zig_pos(w.r, last, p.c, p.rd);
+        w.qpos_min[i] = zig32(w.r, min(w.q0[i], p.Lr - 1), p.c, p.rd);
+        w.qpos_max[i] = zig32(w.r, last, p.c, p.rd);
     }
     w.t_begin = p.mode == USP_MODE_FUSED ? 0 : p.step;
     w.t_end = p.mode == USP_MODE_FUSED ? (int)p.rd : p.step + 1;
@@ -142,14 +164,14 @@ __device__ __forceinline__ Work decode_work(const TcParams &p) {
 
 __device__ __forceinline__ void iter_setup(const TcParams &p, const Work &w, TileIter &it) {
     it.s = (w.r + p.rd - (uint32_t)it.t) % p.rd;
-    int64_t mx = 0;
+    uint32_t mx = 0;
     for (int i = 0; i < 2; ++i) {
         if (!w.valid[i]) {
             it.nhi[i] = 0;
             it.nlo[i] = 0;
         } else if (p.causal) {
-            it.nhi[i] = visible_prefix(w.qpos_max[i], it.s, p.c, p.rd);
-            it.nlo[i] = visible_prefix(w.qpos_min[i], it.s, p.c, p.rd);
+            it.nhi[i] = vis32(w.qpos_max[i], it.s, p.c, p.rd);
+            it.nlo[i] = vis32(w.qpos_min[i], it.s, p.c, p.rd);
         } else {
             it.nhi[i] = p.Lr;
             it.nlo[i] = p.Lr;
@@ -172,10 +194,10 @@ __device__ __forceinline__ bool iter_next(const TcParams &p, const Work &w, Tile
     }
     tl.s = it.s;
     tl.kt = it.kt;
-    tl.kv_row = ((((int64_t)it.s * p.ud + w.u) * p.Hkl + w.kh) * p.bs + w.b) * p.Lr + (int64_t)it.kt * kN;
+    tl.kv_row = (((it.s * p.ud + w.u) * p.Hkl + w.kh) * p.bs + w.b) * p.Lr + it.kt * kN;
     for (int i = 0; i < 2; ++i) {
-        tl.act[i] = (int64_t)it.kt * kN < it.nhi[i];
-        tl.full[i] = (int64_t)(it.kt + 1) * kN <= it.nlo[i];
+        tl.act[i] = it.kt * kN < it.nhi[i];
+        tl.full[i] = (it.kt + 1) * kN <= it.nlo[i];
     }
     ++it.kt;
     return true;
@@ -184,16 +206,25 @@ __device__ __forceinline__ bool iter_next(const TcParams &p, const Work &w, Tile
 // ------------------------------------------------------------------------------------------------
 // roles
 // ------------------------------------------------------------------------------------------------
+// Every lane of the warp runs the loop (uniform control flow and values); one lane issues the copies.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *status) {
+    const bool ok = tc::mbar_wait(bar, parity, status, USP_ERR_TIMEOUT, kWaitLimitNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
 template <int HD>
 __device__ void producer_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0) {
     using C = Cfg<HD>;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
+    const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t sQ = sbase + C::kQ, sK = sbase + C::kK, sV = sbase + C::kV;
-    tc::mbar_arrive_expect_tx(BAR(C::Q_FULL), 2 * C::kTileBytes);
-    for (int i = 0; i < 2; ++i)
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-            tc::tma_load_2d(sQ + i * C::kTileBytes + bx * C::kBoxBytes, &p.tq, bx * 64,
-                            (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
+    if (leader) {
+        tc::mbar_arrive_expect_tx(BAR(C::Q_FULL), 2 * C::kTileBytes);
+        for (int i = 0; i < 2; ++i)
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+                tc::tma_load_2d(sQ + i * C::kTileBytes + bx * C::kBoxBytes, &p.tq, bx * 64,
+                                (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
+    }
     uint32_t fills[C::kStages];
     for (int s = 0; s < C::kStages; ++s) fills[s] = 0;
     TileIter it;
@@ -204,67 +235,74 @@ __device__ void producer_role(const TcParams &p, const Work &w, uint32_t sbase, 
     while (ok && iter_next(p, w, it, tl)) {
         const uint32_t st = j % C::kStages;
         const uint32_t ph = ((j / C::kStages) & 1u) ^ 1u;
-        if (!(ok = tc::mbar_wait(BAR(C::K_EMPTY + st), ph, p.status, USP_ERR_TIMEOUT, kWaitLimitNs))) break;
-        tc::mbar_arrive_expect_tx(BAR(C::K_FULL + st), C::kTileBytes);
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-            tc::tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.tk, bx * 64, (int32_t)tl.kv_row,
-                            BAR(C::K_FULL + st));
-        if (!(ok = tc::mbar_wait(BAR(C::V_EMPTY + st), ph, p.status, USP_ERR_TIMEOUT, kWaitLimitNs))) {
+        if (!(ok = warp_wait(BAR(C::K_EMPTY + st), ph, p.status))) break;
+        if (leader) {
+            tc::mbar_arrive_expect_tx(BAR(C::K_FULL + st), C::kTileBytes);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+                tc::tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.tk, bx * 64, (int32_t)tl.kv_row,
+                                BAR(C::K_FULL + st));
+        }
+        if (!(ok = warp_wait(BAR(C::V_EMPTY + st), ph, p.status))) {
             ++fills[st];  // the K fill of this stage is in flight
             break;
         }
-        tc::mbar_arrive_expect_tx(BAR(C::V_FULL + st), C::kTileBytes);
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-            tc::tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.tv, bx * 64, (int32_t)tl.kv_row,
-                            BAR(C::V_FULL + st));
+        if (leader) {
+            tc::mbar_arrive_expect_tx(BAR(C::V_FULL + st), C::kTileBytes);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+                tc::tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.tv, bx * 64, (int32_t)tl.kv_row,
+                                BAR(C::V_FULL + st));
+        }
         ++fills[st];
         ++j;
     }
     if (!ok) {
         // drain: wait (bounded) for the copies this warp issued, so none lands after the CTA exits
-        tc::mbar_wait(BAR(C::Q_FULL), 0, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+        warp_wait(BAR(C::Q_FULL), 0, p.status);
         for (int s = 0; s < C::kStages; ++s)
             if (fills[s] > 0) {
-                tc::mbar_wait(BAR(C::K_FULL + s), (fills[s] - 1) & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
-                tc::mbar_wait(BAR(C::V_FULL + s), (fills[s] - 1) & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+                warp_wait(BAR(C::K_FULL + s), (fills[s] - 1) & 1u, p.status);
+                warp_wait(BAR(C::V_FULL + s), (fills[s] - 1) & 1u, p.status);
             }
     }
 }
 
+// The descriptors' start-address field holds (shared address >> 4) in its low 14 bits; shared
+// memory is below 256 KB, so adding (byte offset >> 4) to a base descriptor moves its start address.
 template <int HD>
-__device__ __forceinline__ void issue_s(uint32_t tmem, int i, uint32_t sQ, uint32_t sKst) {
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
     using C = Cfg<HD>;
     constexpr uint32_t idS = tc::idesc_bf16_f32(kM, kN, 0, 0);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t koff = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-        const uint64_t a = tc::sw128_desc(sQ + i * C::kTileBytes + koff, 16, 1024);
-        const uint64_t b = tc::sw128_desc(sKst + koff, 16, 1024);
-        tc::mma_ss(tmem + C::colS(i), a, b, idS, kk > 0 ? 1u : 0u);
+        const uint64_t koff = (uint64_t)(((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4);
+        tc::mma_ss(d_tmem, qdesc + koff, kdesc + koff, idS, kk > 0 ? 1u : 0u);
     }
 }
 
 template <int HD>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, int i, uint32_t sVst, uint32_t accumulate) {
-    using C = Cfg<HD>;
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc, uint32_t accumulate) {
     // B = V viewed as (N = hd) x (K = keys), MN-major: 64-column blocks C::kBoxBytes apart (LBO),
     // 8-key groups 1024 bytes apart (SBO); 16 keys per MMA = 2048 bytes.
     constexpr uint32_t idO = tc::idesc_bf16_f32(kM, HD, 0, 1);
 #pragma unroll
-    for (int kk = 0; kk < kN / 16; ++kk) {
-        const uint64_t b = tc::sw128_desc(sVst + kk * 2048, C::kBoxBytes, 1024);
-        tc::mma_ts(tmem + C::colO(i), tmem + C::colS(i) + kk * 8, b, idO, (accumulate || kk > 0) ? 1u : 0u);
-    }
+    for (int kk = 0; kk < kN / 16; ++kk)
+        tc::mma_ts(d_tmem, p_tmem + kk * 8, vdesc + (uint64_t)((kk * 2048) >> 4), idO,
+                   (accumulate || kk > 0) ? 1u : 0u);
 }
 
 template <int HD>
 __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0, uint32_t tmem) {
     using C = Cfg<HD>;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
+    const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t sQ = sbase + C::kQ, sK = sbase + C::kK, sV = sbase + C::kV;
-    auto wait = [&](int bar, uint32_t parity) {
-        return tc::mbar_wait(BAR(bar), parity, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
-    };
+    auto wait = [&](int bar, uint32_t parity) { return warp_wait(BAR(bar), parity, p.status); };
+    // base descriptors: Q tiles and stage 0 of K / V (K-major: LBO unused, SBO = 8 rows x 128 B;
+    // V as MN-major: LBO = next 64-column block, SBO = next 8-key group)
+    const uint64_t qdesc[2] = {tc::sw128_desc(sQ, 16, 1024), tc::sw128_desc(sQ + C::kTileBytes, 16, 1024)};
+    const uint64_t kdesc0 = tc::sw128_desc(sK, 16, 1024);
+    const uint64_t vdesc0 = tc::sw128_desc(sV, C::kBoxBytes, 1024);
+    auto stage_off = [](uint32_t st) { return (uint64_t)((st * C::kTileBytes) >> 4); };
     bool ok = wait(C::Q_FULL, 0);
     tc::fence_after_sync();
     TileIter it;
@@ -276,15 +314,16 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
     if (have) {
         ok = wait(C::K_FULL + 0, 0);
         tc::fence_after_sync();
-        if (ok) {
+        if (ok && leader) {
 #pragma unroll
             for (int i = 0; i < 2; ++i)
                 if (cur.act[i]) {
-                    issue_s<HD>(tmem, i, sQ, sK);
+                    issue_s<HD>(tmem + C::colS(i), qdesc[i], kdesc0);
                     tc::mma_commit(BAR(C::S_FULL + i));
                 }
             tc::mma_commit(BAR(C::K_EMPTY + 0));
         }
+        __syncwarp();
     }
     while (ok && have) {
         const bool have_n = iter_next(p, w, it, nxt);
@@ -300,7 +339,8 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
                 if (ok) {
                     ++pc[i];
                     tc::fence_after_sync();
-                    issue_pv<HD>(tmem, i, sV + st * C::kTileBytes, started[i]);
+                    if (leader) issue_pv<HD>(tmem + C::colO(i), tmem + C::colS(i), vdesc0 + stage_off(st), started[i]);
+                    __syncwarp();
                     started[i] = 1;
                 }
             }
@@ -311,28 +351,36 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
                     kn_ready = true;
                 }
                 if (ok) {
-                    issue_s<HD>(tmem, i, sQ, sK + stn * C::kTileBytes);
-                    tc::mma_commit(BAR(C::S_FULL + i));
+                    if (leader) {
+                        issue_s<HD>(tmem + C::colS(i), qdesc[i], kdesc0 + stage_off(stn));
+                        tc::mma_commit(BAR(C::S_FULL + i));
+                    }
+                    __syncwarp();
                 }
             }
         }
         if (!ok) break;
-        tc::mma_commit(BAR(C::V_EMPTY + st));
+        if (leader) tc::mma_commit(BAR(C::V_EMPTY + st));
+        __syncwarp();
         if (have_n) {
             if (!kn_ready) {
                 if (!(ok = wait(C::K_FULL + stn, phn))) break;
                 tc::fence_after_sync();
             }
-            tc::mma_commit(BAR(C::K_EMPTY + stn));
+            if (leader) tc::mma_commit(BAR(C::K_EMPTY + stn));
+            __syncwarp();
         }
         cur = nxt;
         have = have_n;
         ++j;
     }
-    tc::mma_commit(BAR(C::O_FULL + 0));
-    tc::mma_commit(BAR(C::O_FULL + 1));
-    // every MMA of this CTA has finished before tensor memory is released
-    tc::mma_commit(BAR(C::DONE));
+    if (leader) {
+        tc::mma_commit(BAR(C::O_FULL + 0));
+        tc::mma_commit(BAR(C::O_FULL + 1));
+        // every MMA of this CTA has finished before tensor memory is released
+        tc::mma_commit(BAR(C::DONE));
+    }
+    __syncwarp();
     wait(C::DONE, 0);
 }
 
@@ -370,13 +418,11 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&r)[32], uint64_t sl22
     }
 }
 
-// One softmax warpgroup (i = 0 or 1, one thread per query row of Q tile i). S is streamed through
-// registers 32 columns at a time, the next chunk's TMEM load overlapping the current chunk's math.
-// Exponentials use the running max m_used; a row whose tile max exceeds m_used + 2^8 takes the rare
-// path, which raises m_used to the max of the remaining chunks and rescales what was already
-// produced with the old max (P chunks in TMEM, O in TMEM, the sums). At most one rare path per tile:
-// afterwards no remaining column exceeds the new max. The first visible tile computes its exact max
-// first (a separate pass), so it never takes the rare path.
+// One softmax warpgroup (i = 0 or 1, one thread per query row of Q tile i). Per KV tile the whole
+// S row comes out of TMEM in one round trip (four 32-column loads, one wait), the tile's row max is
+// exact, and O and l are rescaled only when the running max grows by more than 2^8 (lazy rescale:
+// exact, because the final normalisation uses the same stale max). P = 2^(s*scale*log2e - m) is
+// packed to bf16 and written over the start of S, where the PV MMA reads it as its A operand.
 template <int HD>
 __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem, int i) {
     using C = Cfg<HD>;
@@ -393,7 +439,7 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     const bool valid = i ? w.valid[1] : w.valid[0];
     const uint32_t row_local = q0 + row;
     const bool row_ok = valid && row_local < p.Lr;
-    const int64_t qpos_row = zig_pos(w.r, min(row_local, p.Lr - 1), p.c, p.rd);
+    const uint32_t qpos_row = zig32(w.r, min(row_local, p.Lr - 1), p.c, p.rd);
     const float sl2 = p.scale_log2;
     const uint64_t sl22 = tc::pack2(sl2, sl2);
 
@@ -404,14 +450,14 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     iter_init(p, w, it);
     Tile tl;
     uint32_t s_cur = 0xffffffffu;
-    int64_t lim = 0;
+    uint32_t lim = 0;
     while (iter_next(p, w, it, tl)) {
         const bool act = i ? tl.act[1] : tl.act[0];
         if (!act) continue;
         const bool full = i ? tl.full[1] : tl.full[0];
         if (tl.s != s_cur) {
             s_cur = tl.s;
-            lim = p.causal ? visible_prefix(qpos_row, s_cur, p.c, p.rd) : (int64_t)p.Lr;
+            lim = p.causal ? vis32(qpos_row, s_cur, p.c, p.rd) : p.Lr;
         }
         ok = tc::mbar_wait(barS, n_act & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
@@ -419,87 +465,45 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
         tc::fence_after_sync();
         int lim_local = kN;
         if (!full) {
-            const int64_t ll = lim - (int64_t)tl.kt * kN;
-            lim_local = ll < 0 ? 0 : (ll > kN ? kN : (int)ll);
+            const int ll = (int)lim - (int)(tl.kt * kN);
+            lim_local = ll < 0 ? 0 : (ll > kN ? kN : ll);
         }
-        if (n_act == 0) {
-            // first visible tile: the exact row max first
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t r[32];
-                tc::tmem_ld32(tS + cc * 32, r);
-                tc::tmem_ld_wait();
-                if (!full) mask_chunk(r, cc * 32, lim_local);
-                mx = fmaxf(mx, chunk_max(r));
-            }
-            m_used = mx * sl2;
-        }
-        uint64_t sacc = tc::pack2(0.f, 0.f);
-        uint32_t ra[32], rb[32];
-        tc::tmem_ld32(tS, ra);
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tc::tmem_ld32(tS + cc * 32, sr[cc]);
         tc::tmem_ld_wait();
+        if (!full) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) mask_chunk(sr[cc], cc * 32, lim_local);
+        }
+        const float mx =
+            fmaxf(fmaxf(chunk_max(sr[0]), chunk_max(sr[1])), fmaxf(chunk_max(sr[2]), chunk_max(sr[3]))) * sl2;
+        const bool need = mx > m_used + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(m_used, mx);
+            const float alpha = need ? tc::ex2(m_used - m_new) : 1.f;  // 0 on the first visible tile
+            if (need) m_used = m_new;
+            if (n_act > 0) {
+#pragma unroll 1
+                for (int oc = 0; oc < HD / 32; ++oc) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tO + oc * 32, o);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
+                    tc::tmem_st32(tO + oc * 32, o);
+                }
+            }
+            l *= alpha;
+        }
+        const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+        const uint64_t nmb2 = tc::pack2(-mb, -mb);
+        uint64_t sacc = tc::pack2(0.f, 0.f);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-            uint32_t(&cur)[32] = (cc & 1) ? rb : ra;
-            uint32_t(&nxt)[32] = (cc & 1) ? ra : rb;
-            if (cc < 3) tc::tmem_ld32(tS + (cc + 1) * 32, nxt);
-            if (!full) mask_chunk(cur, cc * 32, lim_local);
-            const float cmax = chunk_max(cur) * sl2;
-            if (__any_sync(0xffffffffu, cmax > m_used + kRescaleThreshold)) {
-                // rare path (warp-uniform): new max over the remaining chunks of this tile
-                tc::tmem_ld_wait();
-                float mrest = -INFINITY;
-#pragma unroll 1
-                for (int c2 = cc; c2 < 4; ++c2) {
-                    uint32_t r[32];
-                    tc::tmem_ld32(tS + c2 * 32, r);
-                    tc::tmem_ld_wait();
-                    if (!full) mask_chunk(r, c2 * 32, lim_local);
-                    mrest = fmaxf(mrest, chunk_max(r));
-                }
-                const float m_new = fmaxf(m_used, mrest * sl2);
-                const bool need = m_new > m_used + kRescaleThreshold;
-                const float alpha = need ? tc::ex2(m_used - m_new) : 1.f;  // 0 when m_used = -inf
-                if (need) m_used = m_new;
-                // rescale the P chunks already written with the old max
-                tc::tmem_st_wait();
-#pragma unroll 1
-                for (int c2 = 0; c2 < cc; ++c2) {
-                    uint32_t pr[16];
-                    tc::tmem_ld16(tS + c2 * 16, pr);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 f = bf16x2_to_float2(pr[e]);
-                        pr[e] = float2_to_bf16x2(f.x * alpha, f.y * alpha);
-                    }
-                    tc::tmem_st16(tS + c2 * 16, pr);
-                }
-                if (n_act > 0) {
-#pragma unroll 1
-                    for (int oc = 0; oc < HD / 32; ++oc) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(tO + oc * 32, o);
-                        tc::tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
-                        tc::tmem_st32(tO + oc * 32, o);
-                    }
-                }
-                l *= alpha;
-                sacc = tc::fma2(sacc, tc::pack2(alpha, alpha), tc::pack2(0.f, 0.f));
-                // reload the current chunk and the prefetched next one
-                tc::tmem_ld32(tS + cc * 32, cur);
-                if (cc < 3) tc::tmem_ld32(tS + (cc + 1) * 32, nxt);
-                tc::tmem_ld_wait();
-                if (!full) mask_chunk(cur, cc * 32, lim_local);
-            }
-            const float mb = (m_used == -INFINITY) ? 0.f : m_used;
             uint32_t pk[16];
-            chunk_exp(cur, sl22, tc::pack2(-mb, -mb), sacc, pk);
+            chunk_exp(sr[cc], sl22, nmb2, sacc, pk);
             tc::tmem_st16(tS + cc * 16, pk);
-            if (cc < 3) tc::tmem_ld_wait();
         }
         float s0, s1;
         tc::unpack2(sacc, s0, s1);
@@ -512,7 +516,7 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     }
     if (!ok) return;
     // ---- epilogue: normalise, merge (ACCUM), store -------------------------------------------
-    const int64_t grow = w.q_row_base + row_local;
+    const size_t grow = (size_t)w.q_row_base + row_local;
     const float lse_cur = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     float w_old = 0.f, w_new = 1.f, lse_out = lse_cur;
     if (p.mode == USP_MODE_ACCUM && row_ok) merge_weights(p.lse[grow], lse_cur, w_old, w_new, lse_out);
@@ -612,16 +616,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const bool skip = *skip_flag != 0;
     const Work w = decode_work(p);
 
-    if (skip) {
-        // nothing to do
-    } else if (warp == kProducerWarp) {
-        if (lane == 0) producer_role<HD>(p, w, sbase, bar0);
-        __syncwarp();
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_role<HD>(p, w, sbase, bar0, tmem);
-        __syncwarp();
+    if (warp >= 8) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+        if (!skip) {
+            if (warp == kProducerWarp)
+                producer_role<HD>(p, w, sbase, bar0);
+            else if (warp == kMmaWarp)
+                mma_role<HD>(p, w, sbase, bar0, tmem);
+        }
     } else {
-        softmax_role<HD>(p, w, bar0, tmem, warp >> 2);
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+        if (!skip) softmax_role<HD>(p, w, bar0, tmem, warp >> 2);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -673,6 +678,11 @@ int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        // setmaxnreg.inc can only be granted from registers the launch already holds: never launch a
+        // build whose register count would make the warpgroup split wait forever
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, attn_tc_kernel<HD>) != cudaSuccess) return USP_ERR_CUDA;
+        if ((long)fa.numRegs * kThreads < 2L * 128 * kSoftmaxRegs + 128L * kControlRegs) return USP_ERR_UNSUPPORTED;
         if (cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
             cudaSuccess)
             return USP_ERR_CUDA;

@@ -1,0 +1,245 @@
+// forward.cu -- the whole USP-Attention forward (steps a1-a5, plus the inverse split a7 back to
+// natural order) as one call, on device buffers or pipelined from pinned host buffers.
+//
+// Per head group (UPipe-style head chunking): the composed zigzag split + AllToAll4D of Q, K, V, the
+// fused ring attention, and the composed inverse of out and lse. The host-buffer variant overlaps,
+// on three internal streams, the host-to-device copy of group g+1 and the device-to-host copy of
+// group g-1 with the kernels of group g (two staging slots per direction).
+#include <mutex>
+
+#include "usp_internal.cuh"
+
+namespace usp {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct FwdShape {
+    int64_t bs, L;
+    int hq, hkv, hd, rd, ud, hc, hkc, G, es;
+    size_t q_grp, kv_grp, lse_grp;  // bytes of one group's q / k (or v) / lse, any layout
+};
+
+int fwd_shape(const usp_attn_desc &d, int head_chunk, FwdShape &s) {
+    if (d.bs < 0 || d.L < 0 || d.hq <= 0 || d.hkv <= 0 || d.rd <= 0 || d.ud <= 0) return USP_ERR_INVALID_ARG;
+    if (d.mode != USP_MODE_FUSED) return USP_ERR_INVALID_ARG;
+    s.es = elem_size(d.dtype);
+    if (s.es == 0) return USP_ERR_DTYPE;
+    if (d.hq % d.hkv != 0) return USP_ERR_SHAPE;
+    s.bs = d.bs; s.L = d.L; s.hq = d.hq; s.hkv = d.hkv; s.hd = d.hd; s.rd = d.rd; s.ud = d.ud;
+    s.G = d.hq / d.hkv;
+    s.hc = head_chunk > 0 ? head_chunk : d.hq;
+    if (s.hc > d.hq || d.hq % s.hc != 0 || s.hc % s.G != 0) return USP_ERR_SHAPE;
+    s.hkc = s.hc / s.G;
+    if (s.hc % d.ud != 0 || s.hkc % d.ud != 0) return USP_ERR_SHAPE;
+    const size_t tok = (size_t)d.bs * (size_t)d.L;
+    s.q_grp = tok * s.hc * d.hd * s.es;
+    s.kv_grp = tok * s.hkc * d.hd * s.es;
+    s.lse_grp = tok * s.hc * 4;
+    return USP_OK;
+}
+
+// workspace of the device-buffer forward: head-sharded q, k, v, out, lse of one group
+size_t ws_device(const FwdShape &s) {
+    return align_up(s.q_grp) * 2 + align_up(s.kv_grp) * 2 + align_up(s.lse_grp);
+}
+
+// the host-buffer forward adds two slots of compact natural-order staging for q, k, v and out, and
+// the full natural lse (copied back once at the end)
+size_t ws_host(const FwdShape &s) {
+    const size_t lse_all = (size_t)s.bs * s.L * s.hq * 4;
+    return ws_device(s) + 2 * (align_up(s.q_grp) * 2 + align_up(s.kv_grp) * 2) + align_up(lse_all);
+}
+
+struct Carve {
+    char *p;
+    size_t left;
+    void *take(size_t n) {
+        n = align_up(n);
+        if (n > left) return nullptr;
+        void *r = p;
+        p += n;
+        left -= n;
+        return r;
+    }
+};
+
+usp_dims dims_of(const FwdShape &s, int H, int H_total, int h0, int hd, int dtype) {
+    usp_dims d{};
+    d.bs = s.bs; d.L = s.L; d.H = H; d.hd = hd; d.dtype = dtype; d.rd = s.rd; d.ud = s.ud;
+    d.H_total = H_total; d.h0 = h0;
+    return d;
+}
+
+struct HostPipe {
+    cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, in_ready[2] = {}, in_free[2] = {}, out_ready[2] = {}, out_free[2] = {},
+                comp_done = nullptr, d2h_done = nullptr;
+    bool ok = false;
+};
+
+constexpr int kMaxDev = 64;
+HostPipe g_pipe[kMaxDev];
+std::mutex g_pipe_mu[kMaxDev];
+
+bool pipe_init(HostPipe &hp) {
+    if (hp.ok) return true;
+    const unsigned fl = cudaStreamNonBlocking;
+    if (cudaStreamCreateWithFlags(&hp.h2d, fl) || cudaStreamCreateWithFlags(&hp.comp, fl) ||
+        cudaStreamCreateWithFlags(&hp.d2h, fl))
+        return false;
+    cudaEvent_t *evs[] = {&hp.start, &hp.in_ready[0], &hp.in_ready[1], &hp.in_free[0], &hp.in_free[1],
+                          &hp.out_ready[0], &hp.out_ready[1], &hp.out_free[0], &hp.out_free[1], &hp.comp_done,
+                          &hp.d2h_done};
+    for (cudaEvent_t *e : evs)
+        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+    hp.ok = true;
+    return true;
+}
+
+// 2-D copy of a head window: `rows` rows of `width` bytes, source / destination pitches in bytes
+inline bool copy2d(void *dst, size_t dpitch, const void *src, size_t spitch, size_t width, size_t rows,
+                   cudaMemcpyKind kind, cudaStream_t s) {
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, s) == cudaSuccess;
+}
+
+}  // namespace
+}  // namespace usp
+
+using namespace usp;
+
+extern "C" {
+
+size_t usp_forward_workspace_size(usp_attn_desc d, int head_chunk, int host_buffers) {
+    FwdShape s{};
+    if (fwd_shape(d, head_chunk, s) != USP_OK) return 0;
+    return host_buffers ? ws_host(s) : ws_device(s);
+}
+
+int usp_forward(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d, int head_chunk,
+                void *workspace, size_t workspace_bytes, usp_stream_t stream) {
+    FwdShape s{};
+    int rc = fwd_shape(d, head_chunk, s);
+    if (rc) return rc;
+    if (d.bs == 0 || d.L == 0) return USP_OK;
+    if (!q || !k || !v || !out || !lse || !workspace) return USP_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_device(s)) return USP_ERR_INVALID_ARG;
+    if (!aligned(workspace, kAlign)) return USP_ERR_ALIGN;
+    Carve cv{static_cast<char *>(workspace), workspace_bytes};
+    void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_grp), *vh = cv.take(s.kv_grp), *oh = cv.take(s.q_grp);
+    float *lh = static_cast<float *>(cv.take(s.lse_grp));
+    for (int g0 = 0; g0 < s.hq; g0 += s.hc) {
+        const int gk = g0 / s.G;
+        const void *srcs[3] = {q, k, v};
+        void *dsts[3] = {qh, kh, vh};
+        usp_dims dd[3] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype), dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype),
+                          dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype)};
+        if ((rc = usp_extract_a2a(3, srcs, dsts, dd, 0, stream))) return rc;
+        usp_attn_desc ad = d;
+        ad.hq = s.hc;
+        ad.hkv = s.hkc;
+        if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, stream))) return rc;
+        const void *os[1] = {oh};
+        void *od[1] = {out};
+        usp_dims odims[1] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype)};
+        if ((rc = usp_extract_a2a(1, os, od, odims, 1, stream))) return rc;
+        const void *ls[1] = {lh};
+        void *ld[1] = {lse};
+        usp_dims ldims[1] = {dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
+        if ((rc = usp_extract_a2a(1, ls, ld, ldims, 1, stream))) return rc;
+    }
+    return USP_OK;
+}
+
+int usp_forward_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, float *lse_host,
+                     usp_attn_desc d, int head_chunk, void *workspace, size_t workspace_bytes, usp_stream_t stream) {
+    FwdShape s{};
+    int rc = fwd_shape(d, head_chunk, s);
+    if (rc) return rc;
+    if (d.bs == 0 || d.L == 0) return USP_OK;
+    if (!q_host || !k_host || !v_host || !out_host || !lse_host || !workspace) return USP_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_host(s)) return USP_ERR_INVALID_ARG;
+    if (!aligned(workspace, kAlign)) return USP_ERR_ALIGN;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return USP_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_pipe_mu[dev]);
+    HostPipe &hp = g_pipe[dev];
+    if (!pipe_init(hp)) return USP_ERR_CUDA;
+    cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
+
+    Carve cv{static_cast<char *>(workspace), workspace_bytes};
+    void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_grp), *vh = cv.take(s.kv_grp), *oh = cv.take(s.q_grp);
+    float *lh = static_cast<float *>(cv.take(s.lse_grp));
+    void *in_q[2], *in_k[2], *in_v[2], *out_o[2];
+    for (int sl = 0; sl < 2; ++sl) {
+        in_q[sl] = cv.take(s.q_grp);
+        in_k[sl] = cv.take(s.kv_grp);
+        in_v[sl] = cv.take(s.kv_grp);
+        out_o[sl] = cv.take(s.q_grp);
+    }
+    float *lse_all = static_cast<float *>(cv.take((size_t)s.bs * s.L * s.hq * 4));
+    if (!lse_all) return USP_ERR_INVALID_ARG;
+
+    const size_t rows = (size_t)s.bs * s.L;
+    const size_t row_q = (size_t)s.hd * s.es;  // bytes of one (token, head) row
+    bool okc = true;
+    auto chk = [&](bool c) { okc = okc && c; };
+    chk(cudaEventRecord(hp.start, user) == cudaSuccess);
+    chk(cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess);
+    chk(cudaStreamWaitEvent(hp.comp, hp.start, 0) == cudaSuccess);
+    chk(cudaStreamWaitEvent(hp.d2h, hp.start, 0) == cudaSuccess);
+    const int ngroups = s.hq / s.hc;
+    for (int g = 0; g < ngroups && okc; ++g) {
+        const int sl = g & 1;
+        const int g0 = g * s.hc, gk = g0 / s.G;
+        // host -> device: this group's head windows into compact natural-order staging
+        if (g >= 2) chk(cudaStreamWaitEvent(hp.h2d, hp.in_free[sl], 0) == cudaSuccess);
+        chk(copy2d(in_q[sl], s.hc * row_q, static_cast<const char *>(q_host) + g0 * row_q, s.hq * row_q,
+                   s.hc * row_q, rows, cudaMemcpyHostToDevice, hp.h2d));
+        chk(copy2d(in_k[sl], s.hkc * row_q, static_cast<const char *>(k_host) + gk * row_q, s.hkv * row_q,
+                   s.hkc * row_q, rows, cudaMemcpyHostToDevice, hp.h2d));
+        chk(copy2d(in_v[sl], s.hkc * row_q, static_cast<const char *>(v_host) + gk * row_q, s.hkv * row_q,
+                   s.hkc * row_q, rows, cudaMemcpyHostToDevice, hp.h2d));
+        chk(cudaEventRecord(hp.in_ready[sl], hp.h2d) == cudaSuccess);
+        // kernels
+        usp_stream_t cs = reinterpret_cast<usp_stream_t>(hp.comp);
+        chk(cudaStreamWaitEvent(hp.comp, hp.in_ready[sl], 0) == cudaSuccess);
+        const void *srcs[3] = {in_q[sl], in_k[sl], in_v[sl]};
+        void *dsts[3] = {qh, kh, vh};
+        usp_dims dd[3] = {dims_of(s, s.hc, s.hc, 0, s.hd, d.dtype), dims_of(s, s.hkc, s.hkc, 0, s.hd, d.dtype),
+                          dims_of(s, s.hkc, s.hkc, 0, s.hd, d.dtype)};
+        if ((rc = usp_extract_a2a(3, srcs, dsts, dd, 0, cs))) return rc;
+        chk(cudaEventRecord(hp.in_free[sl], hp.comp) == cudaSuccess);
+        usp_attn_desc ad = d;
+        ad.hq = s.hc;
+        ad.hkv = s.hkc;
+        if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, cs))) return rc;
+        if (g >= 2) chk(cudaStreamWaitEvent(hp.comp, hp.out_free[sl], 0) == cudaSuccess);
+        const void *os[1] = {oh};
+        void *od[1] = {out_o[sl]};
+        usp_dims odims[1] = {dims_of(s, s.hc, s.hc, 0, s.hd, d.dtype)};
+        if ((rc = usp_extract_a2a(1, os, od, odims, 1, cs))) return rc;
+        const void *ls[1] = {lh};
+        void *ldst[1] = {lse_all};
+        usp_dims ldims[1] = {dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
+        if ((rc = usp_extract_a2a(1, ls, ldst, ldims, 1, cs))) return rc;
+        chk(cudaEventRecord(hp.out_ready[sl], hp.comp) == cudaSuccess);
+        // device -> host: this group's output window
+        chk(cudaStreamWaitEvent(hp.d2h, hp.out_ready[sl], 0) == cudaSuccess);
+        chk(copy2d(static_cast<char *>(out_host) + g0 * row_q, s.hq * row_q, out_o[sl], s.hc * row_q, s.hc * row_q,
+                   rows, cudaMemcpyDeviceToHost, hp.d2h));
+        chk(cudaEventRecord(hp.out_free[sl], hp.d2h) == cudaSuccess);
+    }
+    // lse (small) in one copy once every group has written its window
+    chk(cudaEventRecord(hp.comp_done, hp.comp) == cudaSuccess);
+    chk(cudaStreamWaitEvent(hp.d2h, hp.comp_done, 0) == cudaSuccess);
+    chk(cudaMemcpyAsync(lse_host, lse_all, (size_t)s.bs * s.L * s.hq * 4, cudaMemcpyDeviceToHost, hp.d2h) ==
+        cudaSuccess);
+    chk(cudaEventRecord(hp.d2h_done, hp.d2h) == cudaSuccess);
+    chk(cudaStreamWaitEvent(user, hp.d2h_done, 0) == cudaSuccess);
+    return okc ? USP_OK : USP_ERR_CUDA;
+}
+
+}  // extern "C"

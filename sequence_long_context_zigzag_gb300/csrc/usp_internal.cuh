@@ -53,14 +53,31 @@ inline int elem_size(int dtype) { return dtype == USP_F32 ? 4 : (dtype == USP_BF
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // kernel launchers implemented in separate translation units; return USP_* codes
-enum PermMode { PERM_EXTRACT = 0, PERM_EXTRACT_INV = 1, PERM_A2A_FWD = 2, PERM_A2A_INV = 3 };
+enum PermMode {
+    PERM_EXTRACT = 0,      // natural -> local (a1)
+    PERM_EXTRACT_INV = 1,  // local -> natural (a7)
+    PERM_A2A_FWD = 2,      // local -> head-sharded (a2)
+    PERM_A2A_INV = 3,      // head-sharded -> local (a5)
+    PERM_FUSED_FWD = 4,    // natural -> head-sharded (a2 after a1)
+    PERM_FUSED_INV = 5     // head-sharded -> natural (a7 after a5)
+};
 
-struct PermArgs {
+constexpr int kMaxPermJobs = 4;
+
+// One tensor moved by a permute launch; every tensor of a launch shares the mode, the grid and the
+// row size, and may differ in its head window.
+struct PermJob {
     const char *src;
     char *dst;
+    int32_t H, H_total, h0;
+};
+
+struct PermArgs {
     int mode;
+    int njobs;
+    PermJob job[kMaxPermJobs];
     int64_t bs, L;
-    int32_t H, H_total, h0, rd, ud;
+    int32_t rd, ud;
     int32_t r_fixed, u_fixed;  // >= 0 when only one virtual rank takes part (extract only)
     int64_t row_bytes;
 };

@@ -122,3 +122,36 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         usp.usp_extract_local(x, x, 2, 1)
+
+
+def test_extract_a2a_rejects():
+    import ctypes
+    lib = _abi.load()
+    vp = ctypes.c_void_p
+    two = (vp * 2)(BAD, BAD)
+    d_ok = dims()
+    assert lib.usp_extract_a2a(0, two, two, (_abi.UspDims * 1)(d_ok), 0, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_extract_a2a(5, two, two, (_abi.UspDims * 1)(d_ok), 0, None) == _abi.USP_ERR_INVALID_ARG
+    # tensors of one launch must share L / grid / row size
+    mixed = (_abi.UspDims * 2)(dims(), dims(L=128))
+    assert lib.usp_extract_a2a(2, two, two, mixed, 0, None) == _abi.USP_ERR_SHAPE
+    # a head count the Ulysses degree does not divide
+    assert lib.usp_extract_a2a(1, two, two, (_abi.UspDims * 1)(dims(H=3)), 0, None) == _abi.USP_ERR_SHAPE
+    assert lib.usp_extract_a2a(2, two, two, (_abi.UspDims * 2)(dims(), dims(H=2)), 0, None) == _abi.USP_ERR_ALIGN
+
+
+def test_forward_workspace_and_rejects():
+    lib = _abi.load()
+    d = desc(L=1024, hq=8, hkv=2, ud=2, rd=2)
+    n_dev = lib.usp_forward_workspace_size(d, 8, 0)
+    n_host = lib.usp_forward_workspace_size(d, 8, 1)
+    # q group 1024*8*128*2 = 2 MiB, kv group 512 KiB, lse group 32 KiB: q, out, k, v, lse on the device
+    assert n_dev == 2 * 2 ** 21 + 2 * 2 ** 19 + 2 ** 15
+    assert n_host > n_dev
+    assert lib.usp_forward_workspace_size(d, 3, 0) == 0            # 3 does not divide 8
+    assert lib.usp_forward_workspace_size(d, 4, 0) == 0            # 1 KV head per group, ud = 2
+    assert lib.usp_forward_workspace_size(desc(mode=1), 0, 0) == 0  # only the fused mode
+    ws = BAD - 1  # 0x1000: 256-byte aligned, never dereferenced (rejected before any launch)
+    assert lib.usp_forward(BAD, BAD, BAD, BAD, BAD, d, 8, ws, n_dev - 1, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_forward(BAD, BAD, BAD, BAD, BAD, d, 8, BAD, n_dev, None) == _abi.USP_ERR_ALIGN
+    assert lib.usp_forward_host(BAD, BAD, BAD, BAD, BAD, d, 8, ws, n_host - 1, None) == _abi.USP_ERR_INVALID_ARG

@@ -131,3 +131,46 @@ def test_full_size_permutes(wi):
     ref_loc = oracle.extract_local(xs, rd, ud, h0=h0, H=H)
     assert np.array_equal(loc.cpu().numpy(), ref_loc)
     assert np.array_equal(hs.cpu().numpy(), oracle.a2a_fwd(ref_loc, ud))
+
+
+FUSED_CASES = [  # bs, L, hq, hkv, hd, dtype, rd, ud
+    (1, 256, 4, 2, 128, torch.bfloat16, 2, 2),
+    (2, 1000, 4, 4, 128, torch.bfloat16, 4, 2),
+    (1, 768, 8, 2, 64, torch.bfloat16, 3, 2),
+    (1, 1024, 4, 4, 64, torch.float32, 4, 1),
+    (1, 240, 4, 4, 96, torch.bfloat16, 5, 2),
+]
+
+
+@pytest.mark.parametrize("bs,L,hq,hkv,hd,dtype,rd,ud", FUSED_CASES)
+def test_fused_extract_a2a_bitexact(bs, L, hq, hkv, hd, dtype, rd, ud):
+    """One launch moves Q, K, V natural -> head-sharded; equal to the oracle's split then all-to-all."""
+    nat = [rand((bs, L, h, hd), dtype, seed=L + h + i) for i, h in enumerate((hq, hkv, hkv))]
+    natd = [x.to(DEV) for x in nat]
+    hs = [torch.empty(rd, ud, h // ud, bs, L // rd, hd, dtype=dtype, device=DEV) for h in (hq, hkv, hkv)]
+    usp.usp_extract_a2a(natd, hs, rd, ud)
+    for x, h in zip(nat, hs):
+        assert np.array_equal(bits(h), oracle.a2a_fwd(oracle.extract_local(bits(x), rd, ud), ud))
+    back = [torch.full_like(x, float("nan")) for x in natd]
+    usp.usp_extract_a2a(hs, back, rd, ud, inverse=True)
+    for x, b in zip(nat, back):
+        assert np.array_equal(bits(b), bits(x))
+    usp.usp_check()
+
+
+def test_fused_head_windows_and_lse_rows():
+    """Head windows of a wider natural tensor, and 4-byte lse rows through the inverse."""
+    bs, L, Ht, hd, rd, ud = 1, 512, 12, 128, 4, 2
+    x = rand((bs, L, Ht, hd), torch.bfloat16, seed=3)
+    xd = x.to(DEV)
+    hs = torch.empty(rd, ud, 3, bs, L // rd, hd, dtype=torch.bfloat16, device=DEV)
+    usp.usp_extract_a2a([xd], [hs], rd, ud, h0s=[6], Hs=[6])
+    ref = oracle.a2a_fwd(oracle.extract_local(bits(x), rd, ud, h0=6, H=6), ud)
+    assert np.array_equal(bits(hs), ref)
+    lse_hs = rand((rd, ud, 3, bs, L // rd), torch.float32, seed=4)
+    lse_nat = torch.zeros(bs, L, Ht, device=DEV)
+    usp.usp_extract_a2a([lse_hs.to(DEV)], [lse_nat], rd, ud, inverse=True, h0s=[6], Hs=[6])
+    want = oracle.extract_inverse(oracle.a2a_inv(bits(lse_hs)[..., None], ud), L, rd, ud)[..., 0]
+    got = bits(lse_nat)
+    assert np.array_equal(got[:, :, 6:], want) and not got[:, :, :6].any()
+    usp.usp_check()
