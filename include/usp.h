@@ -215,6 +215,29 @@ USP_API int usp_forward_host(const void *q_host, const void *k_host, const void 
  * 0 if the arguments are invalid. */
 USP_API size_t usp_forward_workspace_size(usp_attn_desc d, int head_chunk, int host_buffers);
 
+/* Size of the library-owned scratch array used by usp_forward_noalloc (32 MiB). */
+#define USP_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * usp_forward_noalloc -- usp_forward without a caller workspace; this entry point allocates nothing.
+ * The pages have no counterpart: it exists for callers that cannot hand out device memory, e.g. a
+ * plugin inside an application whose memory manager owns all device memory and forbids allocations
+ * outside its pool, or a caller on a latency-critical path that must not call cudaMalloc / cudaFree
+ * (they can synchronise the device). The workspace is a fixed array of USP_NOALLOC_SCRATCH_BYTES
+ * that this library places on every GPU that loads it, kept until the process exits.
+ *   Arguments, layouts and shape rules as for usp_forward. Shapes whose workspace
+ *   (usp_forward_workspace_size(d, head_chunk, 0)) exceeds USP_NOALLOC_SCRATCH_BYTES return
+ *   USP_ERR_UNSUPPORTED before anything runs: choose a smaller head_chunk (e.g. L = 8192, hd = 128,
+ *   bf16 fits with 2 query heads per group for MHA).
+ *   The first call on a device looks up the array's device address (once per device, cached); make
+ *   that first call before any stream capture begins.
+ *   Every call on a device uses the same array, and calls that overlap on the GPU race on it (e.g.
+ *   two streams at once): order them on one stream. The array keeps the last call's contents; the
+ *   call writes every workspace byte it reads, so nothing needs to start at zero.
+ */
+USP_API int usp_forward_noalloc(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d,
+                                int head_chunk, usp_stream_t stream);
+
 /* Synchronise `stream`, then report (and clear) the device status word of the current device:
  * USP_OK, USP_ERR_TIMEOUT, or USP_ERR_CUDA if the synchronisation itself failed. */
 USP_API int usp_check(usp_stream_t stream);

@@ -25,6 +25,7 @@ from ._abi import (USP_BF16, USP_F32, USP_MODE_ACCUM, USP_MODE_FUSED, USP_MODE_S
 
 __all__ = ["usp_extract_local", "usp_a2a4d", "usp_extract_a2a", "usp_attn_fwd", "usp_lse_merge", "usp_check", "usp_attention",
            "usp_attention_host", "usp_forward", "usp_forward_host", "usp_forward_workspace_size",
+           "usp_forward_noalloc",
            "UspAttention", "UspError", "USP_MODE_FUSED", "USP_MODE_STEP", "USP_MODE_ACCUM", "lib_path"]
 
 lib_path = _abi.LIB_PATH
@@ -279,6 +280,19 @@ def usp_forward(q, k, v, out, lse, ud: int, rd: int, causal: bool = True, scale:
     _abi.check("usp_forward", _abi.load().usp_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d,
                                                      int(head_chunk or 0), _ptr(workspace), workspace.numel(),
                                                      _stream(stream)))
+    return out, lse
+
+
+def usp_forward_noalloc(q, k, v, out, lse, ud: int, rd: int, causal: bool = True, scale: Optional[float] = None,
+                        head_chunk: Optional[int] = None, stream=None):
+    """usp_forward with the library's own fixed scratch array instead of a caller workspace: for
+    callers that cannot allocate device memory (see include/usp.h). Shapes whose workspace exceeds
+    the array (32 MiB) raise UspError (USP_ERR_UNSUPPORTED); calls must not overlap on the GPU."""
+    _dev(q, k, v, out, lse)
+    _check_natural(q, k, v, out, lse)
+    d = _forward_desc(q, k, ud, rd, causal, scale)
+    _abi.check("usp_forward_noalloc", _abi.load().usp_forward_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d, int(head_chunk or 0), _stream(stream)))
     return out, lse
 
 

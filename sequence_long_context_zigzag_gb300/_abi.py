@@ -19,6 +19,8 @@ USP_ERR_TIMEOUT = -7
 USP_F32 = 0
 USP_BF16 = 1
 
+USP_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
 USP_MODE_FUSED = 0
 USP_MODE_STEP = 1
 USP_MODE_ACCUM = 2
@@ -68,6 +70,8 @@ def load():
     lib.usp_forward.restype = ctypes.c_int
     lib.usp_forward_host.argtypes = [vp, vp, vp, vp, vp, UspAttnDesc, ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.usp_forward_host.restype = ctypes.c_int
+    lib.usp_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, UspAttnDesc, ctypes.c_int, vp]
+    lib.usp_forward_noalloc.restype = ctypes.c_int
     lib.usp_forward_workspace_size.argtypes = [UspAttnDesc, ctypes.c_int, ctypes.c_int]
     lib.usp_forward_workspace_size.restype = ctypes.c_size_t
     lib.usp_attn_fwd.argtypes = [vp, vp, vp, vp, vp, UspAttnDesc, vp]

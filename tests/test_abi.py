@@ -155,3 +155,14 @@ def test_forward_workspace_and_rejects():
     assert lib.usp_forward(BAD, BAD, BAD, BAD, BAD, d, 8, ws, n_dev - 1, None) == _abi.USP_ERR_INVALID_ARG
     assert lib.usp_forward(BAD, BAD, BAD, BAD, BAD, d, 8, BAD, n_dev, None) == _abi.USP_ERR_ALIGN
     assert lib.usp_forward_host(BAD, BAD, BAD, BAD, BAD, d, 8, ws, n_host - 1, None) == _abi.USP_ERR_INVALID_ARG
+
+
+def test_forward_noalloc_rejects_before_launch():
+    lib = _abi.load()
+    # workspace above the fixed scratch: L = 65536 MHA, 16 heads per group, hd 128 bf16 (> 32 MiB)
+    big = desc(L=65536, hq=16, hkv=16, ud=2, rd=2)
+    assert lib.usp_forward_workspace_size(big, 0, 0) > _abi.USP_NOALLOC_SCRATCH_BYTES
+    assert lib.usp_forward_noalloc(BAD, BAD, BAD, BAD, BAD, big, 0, None) == _abi.USP_ERR_UNSUPPORTED
+    # invalid shapes report the same status as usp_forward
+    assert lib.usp_forward_noalloc(BAD, BAD, BAD, BAD, BAD, desc(L=250), 0, None) == _abi.USP_ERR_SHAPE
+    assert lib.usp_forward_noalloc(None, None, None, None, None, desc(L=0), 0, None) == _abi.USP_OK
