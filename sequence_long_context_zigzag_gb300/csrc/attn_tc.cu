@@ -10,7 +10,6 @@
 //
 // Kernel design (one CTA = 256 query rows = two 128-row Q tiles of one (r, u, h, b)):
 //   warp 8      TMA producer: Q0, Q1 once; K and V tiles (128 keys x hd) through a ring of stages.
-//               The producer and MMA warps run their loops warp-wide; one lane issues the copies/MMAs.
 //   warp 9      MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V on tcgen05 (kind::f16, bf16 in,
 //               fp32 accumulators in tensor memory), issue order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
 //               so the tensor core works on one tile while the other tile's softmax runs.
@@ -61,7 +60,8 @@ template <int HD> struct Cfg {
     static constexpr int kK = kQ + 2 * kTileBytes;
     static constexpr int kV = kK + kStages * kTileBytes;
     static constexpr int kBar = kV + kStages * kTileBytes;
-    // barrier indices
+    // barrier indices (K and V stages have their own barriers: K(j+1) is needed one softmax earlier
+    // than V(j+1), and K's stage frees earlier, so split barriers give the copies more lead time)
     static constexpr int Q_FULL = 0;
     static constexpr int K_FULL = 1;
     static constexpr int K_EMPTY = K_FULL + kStages;
@@ -206,63 +206,49 @@ __device__ __forceinline__ bool iter_next(const TcParams &p, const Work &w, Tile
 // ------------------------------------------------------------------------------------------------
 // roles
 // ------------------------------------------------------------------------------------------------
-// Every lane of the warp runs the loop (uniform control flow and values); one lane issues the copies.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *status) {
-    const bool ok = tc::mbar_wait(bar, parity, status, USP_ERR_TIMEOUT, kWaitLimitNs);
-    return __all_sync(0xffffffffu, ok);
-}
-
+// One thread issues every copy: Q0 and Q1 once, then for each KV tile K into a K stage and V into a
+// V stage, each waiting only for its own stage to be released.
 template <int HD>
 __device__ void producer_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0) {
     using C = Cfg<HD>;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
-    const bool leader = (threadIdx.x & 31) == 0;
+    auto wait = [&](int bar, uint32_t parity) {
+        return tc::mbar_wait(BAR(bar), parity, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+    };
     const uint32_t sQ = sbase + C::kQ, sK = sbase + C::kK, sV = sbase + C::kV;
-    if (leader) {
-        tc::mbar_arrive_expect_tx(BAR(C::Q_FULL), 2 * C::kTileBytes);
-        for (int i = 0; i < 2; ++i)
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-                tc::tma_load_2d(sQ + i * C::kTileBytes + bx * C::kBoxBytes, &p.tq, bx * 64,
-                                (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
-    }
-    uint32_t fills[C::kStages];
-    for (int s = 0; s < C::kStages; ++s) fills[s] = 0;
+    tc::mbar_arrive_expect_tx(BAR(C::Q_FULL), 2 * C::kTileBytes);
+    for (int i = 0; i < 2; ++i)
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+            tc::tma_load_2d(sQ + i * C::kTileBytes + bx * C::kBoxBytes, &p.tq, bx * 64,
+                            (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
+    uint32_t kfills = 0, vfills = 0;  // stage fills issued
     TileIter it;
     iter_init(p, w, it);
     Tile tl;
-    uint32_t j = 0;
     bool ok = true;
     while (ok && iter_next(p, w, it, tl)) {
-        const uint32_t st = j % C::kStages;
-        const uint32_t ph = ((j / C::kStages) & 1u) ^ 1u;
-        if (!(ok = warp_wait(BAR(C::K_EMPTY + st), ph, p.status))) break;
-        if (leader) {
-            tc::mbar_arrive_expect_tx(BAR(C::K_FULL + st), C::kTileBytes);
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-                tc::tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.tk, bx * 64, (int32_t)tl.kv_row,
-                                BAR(C::K_FULL + st));
-        }
-        if (!(ok = warp_wait(BAR(C::V_EMPTY + st), ph, p.status))) {
-            ++fills[st];  // the K fill of this stage is in flight
-            break;
-        }
-        if (leader) {
-            tc::mbar_arrive_expect_tx(BAR(C::V_FULL + st), C::kTileBytes);
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-                tc::tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.tv, bx * 64, (int32_t)tl.kv_row,
-                                BAR(C::V_FULL + st));
-        }
-        ++fills[st];
-        ++j;
+        const uint32_t st = kfills % C::kStages;
+        const uint32_t ph = ((kfills / C::kStages) & 1u) ^ 1u;
+        if (!(ok = wait(C::K_EMPTY + st, ph))) break;
+        tc::mbar_arrive_expect_tx(BAR(C::K_FULL + st), C::kTileBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+            tc::tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.tk, bx * 64, (int32_t)tl.kv_row,
+                            BAR(C::K_FULL + st));
+        ++kfills;
+        if (!(ok = wait(C::V_EMPTY + st, ph))) break;
+        tc::mbar_arrive_expect_tx(BAR(C::V_FULL + st), C::kTileBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+            tc::tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.tv, bx * 64, (int32_t)tl.kv_row,
+                            BAR(C::V_FULL + st));
+        ++vfills;
     }
     if (!ok) {
-        // drain: wait (bounded) for the copies this warp issued, so none lands after the CTA exits
-        warp_wait(BAR(C::Q_FULL), 0, p.status);
-        for (int s = 0; s < C::kStages; ++s)
-            if (fills[s] > 0) {
-                warp_wait(BAR(C::K_FULL + s), (fills[s] - 1) & 1u, p.status);
-                warp_wait(BAR(C::V_FULL + s), (fills[s] - 1) & 1u, p.status);
-            }
+        // drain: wait (bounded) for the copies this thread issued, so none lands after the CTA exits
+        wait(C::Q_FULL, 0);
+        for (uint32_t f = kfills > C::kStages ? kfills - C::kStages : 0; f < kfills; ++f)
+            wait(C::K_FULL + f % C::kStages, (f / C::kStages) & 1u);
+        for (uint32_t f = vfills > C::kStages ? vfills - C::kStages : 0; f < vfills; ++f)
+            wait(C::V_FULL + f % C::kStages, (f / C::kStages) & 1u);
     }
 }
 
@@ -290,13 +276,18 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
                    (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// One thread issues every MMA and commit. Per KV tile j, in order: PV_0(j), S_0(j+1) [commit: S_0
+// ready], PV_1(j) [commit: V stage of tile j free], S_1(j+1) [commits: S_1 ready, K stage of tile
+// j+1 free]. The tcgen05 fence follows only the waits on the softmax threads' P (TMA completion is
+// ordered by the mbarrier itself).
 template <int HD>
 __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0, uint32_t tmem) {
     using C = Cfg<HD>;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
-    const bool leader = (threadIdx.x & 31) == 0;
+    auto wait = [&](int bar, uint32_t parity) {
+        return tc::mbar_wait(BAR(bar), parity, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+    };
     const uint32_t sQ = sbase + C::kQ, sK = sbase + C::kK, sV = sbase + C::kV;
-    auto wait = [&](int bar, uint32_t parity) { return warp_wait(BAR(bar), parity, p.status); };
     // base descriptors: Q tiles and stage 0 of K / V (K-major: LBO unused, SBO = 8 rows x 128 B;
     // V as MN-major: LBO = next 64-column block, SBO = next 8-key group)
     const uint64_t qdesc[2] = {tc::sw128_desc(sQ, 16, 1024), tc::sw128_desc(sQ + C::kTileBytes, 16, 1024)};
@@ -304,7 +295,6 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
     const uint64_t vdesc0 = tc::sw128_desc(sV, C::kBoxBytes, 1024);
     auto stage_off = [](uint32_t st) { return (uint64_t)((st * C::kTileBytes) >> 4); };
     bool ok = wait(C::Q_FULL, 0);
-    tc::fence_after_sync();
     TileIter it;
     iter_init(p, w, it);
     Tile cur, nxt;
@@ -313,8 +303,7 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
     uint32_t j = 0;
     if (have) {
         ok = wait(C::K_FULL + 0, 0);
-        tc::fence_after_sync();
-        if (ok && leader) {
+        if (ok) {
 #pragma unroll
             for (int i = 0; i < 2; ++i)
                 if (cur.act[i]) {
@@ -323,14 +312,12 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
                 }
             tc::mma_commit(BAR(C::K_EMPTY + 0));
         }
-        __syncwarp();
     }
     while (ok && have) {
         const bool have_n = iter_next(p, w, it, nxt);
         const uint32_t st = j % C::kStages, ph = (j / C::kStages) & 1u;
         const uint32_t stn = (j + 1) % C::kStages, phn = ((j + 1) / C::kStages) & 1u;
         if (!(ok = wait(C::V_FULL + st, ph))) break;
-        tc::fence_after_sync();
         bool kn_ready = false;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -339,48 +326,37 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
                 if (ok) {
                     ++pc[i];
                     tc::fence_after_sync();
-                    if (leader) issue_pv<HD>(tmem + C::colO(i), tmem + C::colS(i), vdesc0 + stage_off(st), started[i]);
-                    __syncwarp();
+                    issue_pv<HD>(tmem + C::colO(i), tmem + C::colS(i), vdesc0 + stage_off(st), started[i]);
                     started[i] = 1;
                 }
             }
             if (ok && have_n && nxt.act[i]) {
                 if (!kn_ready) {
                     ok = wait(C::K_FULL + stn, phn);
-                    tc::fence_after_sync();
                     kn_ready = true;
                 }
                 if (ok) {
-                    if (leader) {
-                        issue_s<HD>(tmem + C::colS(i), qdesc[i], kdesc0 + stage_off(stn));
-                        tc::mma_commit(BAR(C::S_FULL + i));
-                    }
-                    __syncwarp();
+                    issue_s<HD>(tmem + C::colS(i), qdesc[i], kdesc0 + stage_off(stn));
+                    tc::mma_commit(BAR(C::S_FULL + i));
                 }
             }
         }
         if (!ok) break;
-        if (leader) tc::mma_commit(BAR(C::V_EMPTY + st));
-        __syncwarp();
+        tc::mma_commit(BAR(C::V_EMPTY + st));  // V(j) is no longer read
         if (have_n) {
             if (!kn_ready) {
                 if (!(ok = wait(C::K_FULL + stn, phn))) break;
-                tc::fence_after_sync();
             }
-            if (leader) tc::mma_commit(BAR(C::K_EMPTY + stn));
-            __syncwarp();
+            tc::mma_commit(BAR(C::K_EMPTY + stn));  // K(j+1) is no longer read
         }
         cur = nxt;
         have = have_n;
         ++j;
     }
-    if (leader) {
-        tc::mma_commit(BAR(C::O_FULL + 0));
-        tc::mma_commit(BAR(C::O_FULL + 1));
-        // every MMA of this CTA has finished before tensor memory is released
-        tc::mma_commit(BAR(C::DONE));
-    }
-    __syncwarp();
+    tc::mma_commit(BAR(C::O_FULL + 0));
+    tc::mma_commit(BAR(C::O_FULL + 1));
+    // every MMA of this CTA has finished before tensor memory is released
+    tc::mma_commit(BAR(C::DONE));
     wait(C::DONE, 0);
 }
 
@@ -619,10 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (warp >= 8) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
         if (!skip) {
-            if (warp == kProducerWarp)
+            if (warp == kProducerWarp && lane == 0)
                 producer_role<HD>(p, w, sbase, bar0);
-            else if (warp == kMmaWarp)
+            else if (warp == kMmaWarp && lane == 0)
                 mma_role<HD>(p, w, sbase, bar0, tmem);
+            __syncwarp();
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
