@@ -192,17 +192,42 @@ def zig(r, p, c, rd):
     return np.where(p < c, r * c + p, (2 * rd - 1 - r) * c + (p - c))
 
 
+SPLITS = ("zigzag", "basic", "stripe")
+
+
+def split_pos(split, r, p, L, rd):
+    """Global token position of ring-local row p on ring rank r under a sequence split.
+
+    zigzag: Algorithm 2 (chunks r and 2*rd - r - 1 of 2*rd equal chunks), see zig();
+    basic:  the contiguous split of the plain ring (the USP review's "basic-ring" column, Tables 3-4;
+            the Context-Parallel page's sequential split of section 为什么要一头一尾配对): rank r holds
+            tokens [r L/rd, (r+1) L/rd);
+    stripe: the round-robin split of Striped Attention (USP review, section 七 related work; the YunChang
+            page's ring_impl_type "stripe"): rank r holds tokens r, r + rd, r + 2 rd, ...
+    """
+    r = np.asarray(r, dtype=np.int64)
+    p = np.asarray(p, dtype=np.int64)
+    if split == "zigzag":
+        return zig(r, p, L // (2 * rd), rd)
+    if split == "basic":
+        return r * (L // rd) + p
+    if split == "stripe":
+        return p * rd + r
+    raise ValueError(f"unknown split {split}")
+
+
 def _dims(L, rd, ud):
     if L % (2 * rd) or (L // rd) % ud:
         raise ValueError("L must split into 2*rd chunks and L/rd into ud parts")
     return L // (2 * rd), L // rd, L // (rd * ud)
 
 
-def extract_local(x, rd, ud, h0=0, H=None):
+def extract_local(x, rd, ud, h0=0, H=None, split="zigzag"):
     """a1: natural (bs, L, Ht, ...) -> local [rd][ud][bs][Lu][H][...] for every virtual rank.
 
     Slot (r, u, b, j, h) holds token zig(r, u*Lu + j) of head h0 + h: Algorithm 2 steps 4-6
-    (chunk into 2*rd, keep chunks r and 2*rd-r-1, then the u-th of ud equal parts).
+    (chunk into 2*rd, keep chunks r and 2*rd-r-1, then the u-th of ud equal parts). Other splits put
+    token split_pos(split, r, u*Lu + j) there.
     """
     x = np.asarray(x)
     bs, L, Ht = x.shape[:3]
@@ -213,20 +238,27 @@ def extract_local(x, rd, ud, h0=0, H=None):
     B = np.arange(bs).reshape(1, 1, bs, 1, 1)
     J = np.arange(Lu).reshape(1, 1, 1, Lu, 1)
     Hh = np.arange(H).reshape(1, 1, 1, 1, H)
-    return x[B, zig(R, U * Lu + J, c, rd), h0 + Hh]
+    return x[B, split_pos(split, R, U * Lu + J, L, rd), h0 + Hh]
 
 
-def extract_inverse(loc, L, rd, ud):
+def extract_inverse(loc, L, rd, ud, split="zigzag"):
     """a7: local [rd][ud][bs][Lu][H][...] -> natural (bs, L, H, ...), the inverse of a1."""
     loc = np.asarray(loc)
     _, _, bs, Lu, H = loc.shape[:5]
     c, _, Lu2 = _dims(L, rd, ud)
     assert Lu == Lu2
     g = np.arange(L)
-    a = g // c
-    first = a < rd
-    r = np.where(first, a, 2 * rd - 1 - a)
-    p = np.where(first, g % c, c + g % c)
+    if split == "zigzag":
+        a = g // c
+        first = a < rd
+        r = np.where(first, a, 2 * rd - 1 - a)
+        p = np.where(first, g % c, c + g % c)
+    elif split == "basic":
+        r, p = g // (L // rd), g % (L // rd)
+    elif split == "stripe":
+        r, p = g % rd, g // rd
+    else:
+        raise ValueError(f"unknown split {split}")
     u, j = p // Lu, p % Lu
     B = np.arange(bs).reshape(bs, 1, 1)
     Hh = np.arange(H).reshape(1, 1, H)
@@ -285,7 +317,7 @@ def ring_schedule(cp):
     return [[ring_source(r, t, cp) for r in range(cp)] for t in range(cp)]
 
 
-def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True):
+def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True, split="zigzag"):
     """USP-Attention forward, run rank by rank over the virtual ud x rd grid, in fp64.
 
     Algorithm 2 split (a1), AllToAll4D on Q, K, V (a2), for every ring rank the ring loop in Fig. 1
@@ -302,10 +334,10 @@ def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True):
     c, Lr, _ = _dims(L, rd, ud)
     if hq % ud or hkv % ud or hq % hkv:
         raise ValueError("head counts must divide by ud and hq by hkv")
-    Q = a2a_fwd(extract_local(q, rd, ud), ud)          # [rd][ud][hq/ud][bs][Lr][hd]
-    K = a2a_fwd(extract_local(k, rd, ud), ud)          # [rd][ud][hkv/ud][bs][Lr][hd]
-    V = a2a_fwd(extract_local(v, rd, ud), ud)
-    pos = [zig(r, np.arange(Lr), c, rd) for r in range(rd)]
+    Q = a2a_fwd(extract_local(q, rd, ud, split=split), ud)          # [rd][ud][hq/ud][bs][Lr][hd]
+    K = a2a_fwd(extract_local(k, rd, ud, split=split), ud)          # [rd][ud][hkv/ud][bs][Lr][hd]
+    V = a2a_fwd(extract_local(v, rd, ud, split=split), ud)
+    pos = [split_pos(split, r, np.arange(Lr), L, rd) for r in range(rd)]
     O = np.zeros_like(Q)
     LSE = np.full(Q.shape[:5], -np.inf)
     for r in range(rd):
@@ -320,8 +352,8 @@ def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True):
                     o_acc, l_acc = lse_merge(o_acc, l_acc, o_t, l_t)
                 O[r, u, :, b] = o_acc
                 LSE[r, u, :, b] = l_acc
-    out = extract_inverse(a2a_inv(O, ud), L, rd, ud)
-    lse = extract_inverse(a2a_inv(LSE[..., None], ud), L, rd, ud)[..., 0]
+    out = extract_inverse(a2a_inv(O, ud), L, rd, ud, split=split)
+    lse = extract_inverse(a2a_inv(LSE[..., None], ud), L, rd, ud, split=split)[..., 0]
     return out, lse
 
 
@@ -380,6 +412,12 @@ def contiguous_rank_work(cp, c=4):
     B = 2 * c
     return [sum(pair_class(np.arange(r * B, (r + 1) * B), np.arange(b * B, (b + 1) * B))
                 for b in range(cp)) for r in range(cp)]
+
+
+def split_rank_pairs(split, L, rd):
+    """Exact causal (query, key) pair count of each ring rank's queries under a split."""
+    Lr = L // rd
+    return [visible_pairs(split_pos(split, r, np.arange(Lr), L, rd)) for r in range(rd)]
 
 
 def visible_pairs(positions):

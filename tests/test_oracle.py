@@ -325,3 +325,51 @@ def test_comm_volumes_counted_from_schedule():
         assert oracle.counted_ring_elems(s, heads_kv, hd, cp) == oracle.comm_ring_elems(s, hkv, cp)
         assert oracle.counted_ulysses_elems(s, heads, heads_kv, hd, cp) == \
             oracle.comm_ulysses_elems(s, h, hkv, cp)
+
+
+# ---------------------------------------------------------------------------------------------
+# other sequence splits (the plain ring's contiguous split, Striped Attention's round robin)
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("rd,ud,L", [(2, 1, 16), (4, 2, 32), (3, 2, 36), (1, 1, 8)])
+def test_basic_and_stripe_splits_match_library(rd, ud, L):
+    x = np.arange(2 * L * 3 * 2).reshape(2, L, 3, 2)
+    xt = torch.as_tensor(x)
+    for r in range(rd):
+        basic = xt.chunk(rd, dim=1)[r]              # contiguous: rank r holds its L/rd block
+        stripe = xt[:, r::rd]                       # round robin: tokens r, r + rd, ...
+        for u in range(ud):
+            assert np.array_equal(oracle.extract_local(x, rd, ud, split="basic")[r, u],
+                                  basic.chunk(ud, dim=1)[u].numpy())
+            assert np.array_equal(oracle.extract_local(x, rd, ud, split="stripe")[r, u],
+                                  stripe.chunk(ud, dim=1)[u].numpy())
+    for split in oracle.SPLITS:
+        loc = oracle.extract_local(x, rd, ud, split=split)
+        assert np.array_equal(oracle.extract_inverse(loc, L, rd, ud, split=split), x)
+
+
+@pytest.mark.parametrize("split", ["basic", "stripe"])
+@pytest.mark.parametrize("L,rd,ud", [(16, 2, 1), (32, 4, 2), (24, 3, 2)])
+def test_literal_pipeline_other_splits_equal_direct(split, L, rd, ud):
+    q, k, v = make_qkv(1, L, 4, 2, 8, "f32", seed=L + rd + ud)
+    o_ref, l_ref = oracle.attn_direct(q, k, v, causal=True)
+    o, l = oracle.literal_pipeline(q, k, v, rd, ud, split=split)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    np.testing.assert_allclose(l, l_ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("rd,Lr", [(4, 16), (8, 32), (3, 10)])
+def test_split_rank_pairs_closed_forms(rd, Lr):
+    """Causal pairs per rank: basic r*Lr^2 + Lr(Lr+1)/2 (grows with r, max/mean -> 1.75 at rd = 4 for
+    long blocks, the Context-Parallel page's figure); stripe rd*Lr(Lr-1)/2 + (r+1)*Lr (nearly equal);
+    zigzag identical on every rank."""
+    L = rd * Lr
+    basic = oracle.split_rank_pairs("basic", L, rd)
+    stripe = oracle.split_rank_pairs("stripe", L, rd)
+    assert basic == [r * Lr * Lr + Lr * (Lr + 1) // 2 for r in range(rd)]
+    assert stripe == [rd * Lr * (Lr - 1) // 2 + (r + 1) * Lr for r in range(rd)]
+    if Lr % 2 == 0:
+        zz = oracle.split_rank_pairs("zigzag", L, rd)
+        assert len(set(zz)) == 1 and sum(zz) == sum(basic) == L * (L + 1) // 2
+    if rd == 4:
+        big = oracle.split_rank_pairs("basic", 4 * 4096, 4)
+        assert abs(max(big) / (sum(big) / 4) - 1.75) < 1e-3
