@@ -213,6 +213,41 @@ class Step:
                 self.perm_events.append((e0, e1, e2, e3))
 
 
+def rank_balance(usp, w, q, k, v, reps=5):
+    """Per-ring-rank attention time under each sequence split (each rank's query rows computed alone,
+    median of ``reps`` launches): the load imbalance a multi-GPU ring would see, measured on the device.
+    The pages' claim: a contiguous split leaves the last of 4 ranks with 1.75x the mean work, zigzag
+    balances it exactly."""
+    hc = w.head_chunk or w.hq
+    G = w.hq // w.hkv
+    hkc = hc // G
+    rd, ud, bs, L, hd = w.rd, w.ud, w.bs, w.L, w.hd
+    dev, dt = q.device, q.dtype
+    qh = torch.empty(rd, ud, hc // ud, bs, L // rd, hd, device=dev, dtype=dt)
+    kh = torch.empty(rd, ud, hkc // ud, bs, L // rd, hd, device=dev, dtype=dt)
+    vh = torch.empty_like(kh)
+    oh = torch.empty_like(qh)
+    lh = torch.empty(qh.shape[:5], device=dev, dtype=torch.float32)
+    res = {}
+    for split in ("zigzag", "basic", "stripe"):
+        usp.usp_extract_a2a([q, k, v], [qh, kh, vh], rd, ud, h0s=[0, 0, 0], Hs=[hc, hkc, hkc], split=split)
+        ms = []
+        for r in range(rd):
+            ts = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                usp.usp_attn_fwd(qh, kh, vh, oh, lh, causal=w.causal, split=split, ring_rank=r)
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            ms.append(statistics.median(ts))
+        res[split] = {"rank_ms": [round(x, 4) for x in ms], "max_over_mean": max(ms) / (sum(ms) / len(ms))}
+    usp.usp_check()
+    res["note"] = f"first head group ({hc} query heads), each ring rank's rows alone; median of {reps}"
+    return res
+
+
 def traffic_for_current_kernel(workload_index):
     """DRAM bytes per attention launch (read + write) from the committed ncu summary, if it was taken
     on this workload and on the attention kernel source as it is now (else None)."""
@@ -395,6 +430,9 @@ def main():
     dist.barrier()
     usp.usp_check()
 
+    # ---- per-ring-rank work under the three splits (outside the timed region) ----------------
+    balance = rank_balance(usp, w, q, k, v) if w.rd > 1 else None
+
     # ---- CPU baseline (the oracle on the host cores), rank 0 at N = 1 -----------------------
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -433,6 +471,7 @@ def main():
                     "d2h_bytes_per_step": d2h,
                     "api": f"usp_forward_host (pinned host buffers, head_chunk={chunk}, wall clock)"},
             "gpu_launches": step.launches_per_step * args.steps,
+            "rank_balance": balance,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

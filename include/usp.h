@@ -57,6 +57,14 @@ typedef enum {
 
 typedef enum { USP_F32 = 0, USP_BF16 = 1 } usp_dtype;
 
+/* How the global sequence is divided among the ring ranks (ring-local row p of ring rank r holds
+ * global token pos(r, p); every split keeps pos increasing in p). */
+typedef enum {
+    USP_SPLIT_ZIGZAG = 0, /* Algorithm 2: chunks r and 2 rd - 1 - r of 2 rd equal chunks (load-balanced) */
+    USP_SPLIT_BASIC = 1,  /* the plain ring: tokens [r L/rd, (r+1) L/rd) (USP review, "basic-ring") */
+    USP_SPLIT_STRIPE = 2  /* Striped Attention's round robin: tokens r, r + rd, r + 2 rd, ... */
+} usp_split;
+
 /* Shape of one tensor moved by a permute. */
 typedef struct {
     int64_t bs;      /* batch size */
@@ -68,6 +76,7 @@ typedef struct {
     int32_t ud;      /* Ulysses degree >= 1 */
     int32_t H_total; /* heads per token in the natural / sequence-sharded tensor (0 means H) */
     int32_t h0;      /* first head of the window [h0, h0 + H) in that tensor */
+    int32_t split;   /* usp_split; USP_SPLIT_ZIGZAG (0) unless stated */
 } usp_dims;
 
 /*
@@ -79,7 +88,8 @@ typedef struct {
  *              [h0, h0 + H) of it.
  *   local    : [rd][ud][bs][Lu][H][hd] (all virtual ranks, vr-major), or (bs, Lu, H, hd) for one rank.
  *   Local slot (r, u, b, j, h) holds token zig(r, u Lu + j) of head h0 + h, where
- *   zig(r, p) = r c + p for p < c and (2 rd - 1 - r) c + (p - c) otherwise.
+ *   zig(r, p) = r c + p for p < c and (2 rd - 1 - r) c + (p - c) otherwise (d.split selects the basic
+ *   or stripe split instead: pos(r, p) = r Lr + p or p rd + r).
  *
  * inverse == 0: src = natural, dst = local.  inverse != 0: src = local, dst = natural (restores
  * natural order; heads outside the window are left untouched).
@@ -145,6 +155,9 @@ typedef struct {
     float scale;    /* softmax scale; <= 0 means 1/sqrt(hd) */
     int32_t mode;   /* usp_mode */
     int32_t step;   /* ring step t for USP_MODE_STEP / USP_MODE_ACCUM, 0 <= t < rd */
+    int32_t split;  /* usp_split of q / k / v (must match the split the permutes used) */
+    int32_t ring_rank_only; /* 0: every ring rank; k > 0: only ring rank k - 1's query rows are
+                               computed and written (its share of the work, e.g. to time one rank) */
 } usp_attn_desc;
 
 /*

@@ -39,6 +39,14 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
 
 
+def _split_code(split) -> int:
+    if isinstance(split, str):
+        if split not in _abi.SPLITS:
+            raise ValueError(f"unknown split {split!r} (zigzag, basic or stripe)")
+        return _abi.SPLITS[split]
+    return int(split)
+
+
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -65,7 +73,7 @@ def _need(cond: bool, msg: str):
 
 
 def usp_extract_local(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, vr: int = -1, inverse: bool = False,
-                      h0: int = 0, H: Optional[int] = None, stream=None) -> torch.Tensor:
+                      h0: int = 0, H: Optional[int] = None, split="zigzag", stream=None) -> torch.Tensor:
     """Zigzag split (inverse=False: natural -> local) or its inverse (local -> natural).
 
     natural: (bs, L, H_total, hd), or (bs, L, H_total) for an lse tensor; local:
@@ -87,7 +95,7 @@ def usp_extract_local(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, vr
     ranks = rd * ud if vr < 0 else 1
     _need(loc.numel() == ranks * bs * Lu * H * hd, f"local tensor has {loc.numel()} elements, "
           f"expected {ranks * bs * Lu * H * hd}")
-    d = UspDims(bs, L, H, hd, _dtype_code(nat), rd, ud, Ht, h0)
+    d = UspDims(bs, L, H, hd, _dtype_code(nat), rd, ud, Ht, h0, _split_code(split))
     _abi.check("usp_extract_local", _abi.load().usp_extract_local(
         _ptr(src), _ptr(dst), d, int(vr), int(bool(inverse)), _stream(stream)))
     return dst
@@ -112,13 +120,14 @@ def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int =
     _need(H % ud == 0, "heads must divide by ud")
     L = Lu * ud * rd
     _need(hs.numel() == rd * ud * (H // ud) * bs * ud * Lu * hd, "head-sharded tensor has the wrong size")
-    d = UspDims(bs, L, H, hd, _dtype_code(seq), rd, ud, Ht, h0)
+    d = UspDims(bs, L, H, hd, _dtype_code(seq), rd, ud, Ht, h0, 0)
     _abi.check("usp_a2a4d", _abi.load().usp_a2a4d(_ptr(src), _ptr(dst), d, 1 if dir > 0 else -1,
                                                  _stream(stream)))
     return dst
 
 
-def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=None, Hs=None, stream=None):
+def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=None, Hs=None, split="zigzag",
+                    stream=None):
     """Zigzag split then AllToAll4D in one pass (inverse: AllToAll4D's inverse then the inverse split),
     for up to four tensors in one launch. inverse=False: srcs[k] natural (bs, L, H_total, hd) (or
     (bs, L, H_total) for lse) -> dsts[k] head-sharded [rd][ud][H/ud][bs][Lr](, hd); inverse=True the
@@ -144,7 +153,7 @@ def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=Non
         _need(0 <= h0s[k] and h0s[k] + H <= Ht, "head window out of range")
         _need(L % (2 * rd) == 0 and (L // rd) % ud == 0 and H % ud == 0, "shape not divisible")
         _need(hs.numel() == bs * L * H * hd, "head-sharded tensor has the wrong size")
-        dims.append(UspDims(bs, L, H, hd, _dtype_code(nat), rd, ud, Ht, h0s[k]))
+        dims.append(UspDims(bs, L, H, hd, _dtype_code(nat), rd, ud, Ht, h0s[k], _split_code(split)))
         sp.append(_ptr(src))
         dp.append(_ptr(dst))
     vp = ctypes.c_void_p
@@ -155,9 +164,9 @@ def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=Non
 
 def usp_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
                  causal: bool = True, scale: Optional[float] = None, mode: int = USP_MODE_FUSED, step: int = 0,
-                 stream=None):
-    """Ring attention over all virtual ring ranks. q/out [rd][ud][hq/ud][bs][Lr][hd], k/v
-    [rd][ud][hkv/ud][bs][Lr][hd], lse [rd][ud][hq/ud][bs][Lr] fp32."""
+                 split="zigzag", ring_rank: Optional[int] = None, stream=None):
+    """Ring attention over all virtual ring ranks (or only ring rank ``ring_rank``'s query rows).
+    q/out [rd][ud][hq/ud][bs][Lr][hd], k/v [rd][ud][hkv/ud][bs][Lr][hd], lse [rd][ud][hq/ud][bs][Lr] fp32."""
     _dev(q, k, v, out, lse)
     _need(q.dim() == 6 and k.dim() == 6 and v.dim() == 6, "q, k, v must be [rd][ud][H/ud][bs][Lr][hd]")
     rd, ud, Hl, bs, Lr, hd = q.shape
@@ -168,7 +177,8 @@ def usp_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.T
     _need(k.dtype == q.dtype and v.dtype == q.dtype, "dtype mismatch")
     L = Lr * rd
     d = UspAttnDesc(bs, L, Hl * ud, Hkl * ud, hd, rd, ud, _dtype_code(q), int(bool(causal)),
-                    float(scale) if scale is not None else 0.0, int(mode), int(step))
+                    float(scale) if scale is not None else 0.0, int(mode), int(step), _split_code(split),
+                    0 if ring_rank is None else int(ring_rank) + 1)
     _abi.check("usp_attn_fwd", _abi.load().usp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d,
                                                        _stream(stream)))
     return out, lse
@@ -195,7 +205,7 @@ def usp_check(stream=None) -> None:
 
 def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd: int, causal: bool = True,
                   scale: Optional[float] = None, head_chunk: Optional[int] = None, natural_output: bool = True,
-                  stream=None):
+                  split="zigzag", stream=None):
     """USP-Attention forward (Algorithm 1 of the USP review) over a virtual ud x rd grid on one GPU.
 
     q: (bs, L, hq, hd), k/v: (bs, L, hkv, hd) CUDA tensors in natural token order. For every head group
@@ -220,7 +230,8 @@ def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd
     if natural_output:
         out = torch.empty(bs, L, hq, hd, device=dev, dtype=dt)
         lse = torch.empty(bs, L, hq, device=dev, dtype=torch.float32)
-        usp_forward(q, k, v, out, lse, ud, rd, causal=causal, scale=scale, head_chunk=head_chunk, stream=stream)
+        usp_forward(q, k, v, out, lse, ud, rd, causal=causal, scale=scale, head_chunk=head_chunk, split=split,
+                    stream=stream)
         return out, lse
     out = torch.empty(rd, ud, bs, Lu, hq, hd, device=dev, dtype=dt)
     lse = torch.empty(rd, ud, bs, Lu, hq, device=dev, dtype=torch.float32)
@@ -233,20 +244,21 @@ def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd
     for g0 in range(0, hq, hc):
         gk = g0 // G
         # a1 + a2: zigzag split and AllToAll4D of Q, K, V in one launch
-        usp_extract_a2a([q, k, v], [qh, kh, vh], rd, ud, h0s=[g0, gk, gk], Hs=[hc, hkc, hkc], stream=stream)
+        usp_extract_a2a([q, k, v], [qh, kh, vh], rd, ud, h0s=[g0, gk, gk], Hs=[hc, hkc, hkc], split=split,
+                        stream=stream)
         # a3 + a4: the ring with the fused LSE merge
-        usp_attn_fwd(qh, kh, vh, oh, lh, causal=causal, scale=scale, stream=stream)
+        usp_attn_fwd(qh, kh, vh, oh, lh, causal=causal, scale=scale, split=split, stream=stream)
         # a5 on out and lse: back to the sequence-sharded layout a model keeps
         usp_a2a4d(oh, out, rd, ud, -1, h0=g0, H=hc, stream=stream)
         usp_a2a4d(lh, lse, rd, ud, -1, h0=g0, H=hc, stream=stream)
     return out, lse
 
 
-def _forward_desc(q, k, ud, rd, causal, scale):
+def _forward_desc(q, k, ud, rd, causal, scale, split="zigzag"):
     bs, L, hq, hd = q.shape
     hkv = k.shape[2]
     return UspAttnDesc(bs, L, hq, hkv, hd, rd, ud, _dtype_code(q), int(bool(causal)),
-                       float(scale) if scale is not None else 0.0, USP_MODE_FUSED, 0)
+                       float(scale) if scale is not None else 0.0, USP_MODE_FUSED, 0, _split_code(split), 0)
 
 
 def usp_forward_workspace_size(q, k, ud: int, rd: int, head_chunk: Optional[int] = None, host: bool = False,
@@ -268,11 +280,12 @@ def _check_natural(q, k, v, out, lse):
 
 
 def usp_forward(q, k, v, out, lse, ud: int, rd: int, causal: bool = True, scale: Optional[float] = None,
-                head_chunk: Optional[int] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+                head_chunk: Optional[int] = None, workspace: Optional[torch.Tensor] = None, split="zigzag",
+                stream=None):
     """The whole forward on device buffers in one C call (natural-order in and out)."""
     _dev(q, k, v, out, lse)
     _check_natural(q, k, v, out, lse)
-    d = _forward_desc(q, k, ud, rd, causal, scale)
+    d = _forward_desc(q, k, ud, rd, causal, scale, split)
     n = usp_forward_workspace_size(q, k, ud, rd, head_chunk, host=False, causal=causal)
     if workspace is None:
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device)

@@ -21,6 +21,11 @@ USP_BF16 = 1
 
 USP_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
+USP_SPLIT_ZIGZAG = 0
+USP_SPLIT_BASIC = 1
+USP_SPLIT_STRIPE = 2
+SPLITS = {"zigzag": USP_SPLIT_ZIGZAG, "basic": USP_SPLIT_BASIC, "stripe": USP_SPLIT_STRIPE}
+
 USP_MODE_FUSED = 0
 USP_MODE_STEP = 1
 USP_MODE_ACCUM = 2
@@ -29,14 +34,14 @@ USP_MODE_ACCUM = 2
 class UspDims(ctypes.Structure):
     _fields_ = [("bs", ctypes.c_int64), ("L", ctypes.c_int64), ("H", ctypes.c_int32), ("hd", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("rd", ctypes.c_int32), ("ud", ctypes.c_int32),
-                ("H_total", ctypes.c_int32), ("h0", ctypes.c_int32)]
+                ("H_total", ctypes.c_int32), ("h0", ctypes.c_int32), ("split", ctypes.c_int32)]
 
 
 class UspAttnDesc(ctypes.Structure):
     _fields_ = [("bs", ctypes.c_int64), ("L", ctypes.c_int64), ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32),
                 ("hd", ctypes.c_int32), ("rd", ctypes.c_int32), ("ud", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("causal", ctypes.c_int32), ("scale", ctypes.c_float), ("mode", ctypes.c_int32),
-                ("step", ctypes.c_int32)]
+                ("step", ctypes.c_int32), ("split", ctypes.c_int32), ("ring_rank_only", ctypes.c_int32)]
 
 
 class UspError(RuntimeError):

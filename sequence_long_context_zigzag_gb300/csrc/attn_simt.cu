@@ -3,9 +3,9 @@
 // This is the path for fp32 inputs (and the numerics cross-check for the tensor-core kernel): each
 // warp owns one query row of one virtual rank, walks the ring in the order of the Context-Parallel
 // page's Fig. 1 (step t: KV block of ring rank (r - t) mod rd), and folds every key into a running
-// online softmax (the LSE merge of that page's section 先弄清楚 applied key by key). Because the
-// zigzag position map is increasing within a rank, the keys a causal row sees in a rank's block are
-// a prefix of that block, so masking is a loop bound.
+// online softmax (the LSE merge of that page's section 先弄清楚 applied key by key). Because every
+// split's position map is increasing within a rank, the keys a causal row sees in a rank's block
+// are a prefix of that block, so masking is a loop bound.
 #include <math.h>
 
 #include "usp_device.cuh"
@@ -19,7 +19,7 @@ struct AttnK {
     void *out;
     float *lse;
     uint32_t nrows, bs, Lr, c, rd, ud, Hl, Hkl, G;
-    int causal, mode, step;
+    int causal, mode, step, split, ring_rank_only;
     float scale_log2;  // softmax scale * log2(e)
     FastDiv f_Lr, f_bs, f_Hl, f_ud;
 };
@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnK p) {
     p.f_bs.divmod(t0, t0, b);
     p.f_Hl.divmod(t0, t0, h);
     p.f_ud.divmod(t0, r, u);
-    const int64_t qpos = zig_pos(r, pq, p.c, p.rd);
+    if (p.ring_rank_only > 0 && r != (uint32_t)(p.ring_rank_only - 1)) return;
+    const int64_t qpos = split_pos(p.split, r, pq, p.c, p.rd);
     const uint32_t kh = h / p.G;
 
     float qv[EPL], acc[EPL];
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnK p) {
     const int t_end = p.mode == USP_MODE_FUSED ? (int)p.rd : p.step + 1;
     for (int t = t_begin; t < t_end; ++t) {
         const uint32_t s = (r + p.rd - (uint32_t)t) % p.rd;
-        const int64_t nvis = p.causal ? visible_prefix(qpos, s, p.c, p.rd) : (int64_t)p.Lr;
+        const int64_t nvis = p.causal ? split_visible(p.split, qpos, s, p.c, p.rd) : (int64_t)p.Lr;
         const size_t kv_row0 = ((((size_t)s * p.ud + u) * p.Hkl + kh) * p.bs + b) * p.Lr;
         const T *kp = static_cast<const T *>(p.k) + kv_row0 * HD + lane * EPL;
         const T *vp = static_cast<const T *>(p.v) + kv_row0 * HD + lane * EPL;
@@ -160,6 +161,8 @@ int launch_attn_simt(const AttnArgs &a, cudaStream_t s) {
     k.causal = a.causal;
     k.mode = a.mode;
     k.step = a.step;
+    k.split = a.split;
+    k.ring_rank_only = a.ring_rank_only;
     k.scale_log2 = a.scale * 1.4426950408889634f;
     k.f_Lr = FastDiv(k.Lr);
     k.f_bs = FastDiv(k.bs);

@@ -10,15 +10,15 @@
 //
 // Kernel design (one CTA = 256 query rows = two 128-row Q tiles of one (r, u, h, b)):
 //   warp 8      TMA producer: Q0, Q1 once; K and V tiles (128 keys x hd) through a ring of stages.
-//   warp 9      MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V on tcgen05 (kind::f16, bf16 in,
-//               fp32 accumulators in tensor memory), issue order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
-//               so the tensor core works on one tile while the other tile's softmax runs.
+//   warps 9, 10 MMA issuers, one thread per Q tile i: S_i = Q_i K^T and O_i += P_i V on tcgen05
+//               (kind::f16, bf16 in, fp32 accumulators in tensor memory), issue order PV_i(j),
+//               S_i(j+1), so the tensor core works on one tile while the other tile's softmax runs.
 //   warps 0-3   softmax of Q tile 0, warps 4-7 softmax of Q tile 1: one thread per query row reads
 //               its S row from TMEM, masks partial tiles, updates the running max with a lazy
 //               rescale (O and l are rescaled only when the max grows by more than 2^8), writes
 //               P = 2^(S*scale*log2e - m) as bf16 back into TMEM (the A operand of the PV MMA), and
 //               finally normalises O and writes out (bf16) and lse (fp32).
-//   warps 10-11 hold no role; with warps 8-9 they form the control warpgroup that hands registers
+//   warp 11     holds no role; with warps 8-10 it forms the control warpgroup that hands registers
 //               to the softmax warpgroups (setmaxnreg).
 //   TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+hd) O1 [256+hd, 256+2hd); P_i aliases S_i.
 // The causal structure is exploited per (Q tile, KV tile) pair from global positions: tiles wholly
@@ -41,7 +41,8 @@ constexpr int kN = 128;  // keys per tile
 constexpr int kWarps = 12;  // warpgroups: softmax 0 (warps 0-3), softmax 1 (4-7), control (8-11)
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;     // issues Q tile 0's MMAs; allocates and frees tensor memory
+constexpr int kMmaWarp1 = 10;   // issues Q tile 1's MMAs
 // Register split per warpgroup (setmaxnreg). The launch grants 384 threads x 168 registers = 64512;
 // the softmax warpgroups take 2 x 128 x 208 = 53248 and the control warpgroup keeps 128 x 88 = 11264:
 // 64512 in total, so the increase can always be granted.
@@ -70,8 +71,9 @@ template <int HD> struct Cfg {
     static constexpr int S_FULL = V_EMPTY + kStages;  // [2]
     static constexpr int P_FULL = S_FULL + 2;         // [2]
     static constexpr int O_FULL = P_FULL + 2;         // [2]
-    static constexpr int DONE = O_FULL + 2;
-    static constexpr int kNumBars = DONE + 1;
+    static constexpr int DONE = O_FULL + 2;           // [2]
+    static constexpr int TURN = DONE + 2;             // [2]: issuer i may issue its next burst
+    static constexpr int kNumBars = TURN + 2;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kSmemBytes = kTmemSlot + 16 + 1024;  // + slack for 1024-byte alignment
     __device__ static constexpr uint32_t colS(int i) { return 128u * (uint32_t)i; }
@@ -84,7 +86,7 @@ struct TcParams {
     float *lse;
     int *status;
     uint32_t bs, Lr, c, rd, ud, Hl, Hkl, G, npairs;
-    int causal, mode, step, lpt;
+    int causal, mode, step, lpt, split, ring_rank_only;
     float scale_log2;
 };
 
@@ -112,13 +114,22 @@ struct TileIter {
     uint32_t nhi[2], nlo[2];
 };
 
-// global position of ring-local row p on ring rank r (chunk length c): chunks r and 2 rd - 1 - r
-__device__ __forceinline__ uint32_t zig32(uint32_t r, uint32_t p, uint32_t c, uint32_t rd) {
+// global position of ring-local row p on ring rank r (chunk length c = Lr / 2) under the split:
+// zigzag keeps chunks r and 2 rd - 1 - r, basic the contiguous block r, stripe every rd-th token
+__device__ __forceinline__ uint32_t pos32(int split, uint32_t r, uint32_t p, uint32_t c, uint32_t rd) {
+    if (split == USP_SPLIT_BASIC) return r * 2 * c + p;
+    if (split == USP_SPLIT_STRIPE) return p * rd + r;
     return p < c ? r * c + p : (2 * rd - 1 - r) * c + (p - c);
 }
 
-// number of ring-local rows of rank s whose global position is <= qpos (a prefix: zig is increasing)
-__device__ __forceinline__ uint32_t vis32(uint32_t qpos, uint32_t s, uint32_t c, uint32_t rd) {
+// number of ring-local rows of rank s whose global position is <= qpos (a prefix: every split's
+// position map is increasing in the row)
+__device__ __forceinline__ uint32_t vis32(int split, uint32_t qpos, uint32_t s, uint32_t c, uint32_t rd) {
+    if (split == USP_SPLIT_BASIC) {
+        const uint32_t a0 = s * 2 * c;
+        return qpos < a0 ? 0u : min(qpos - a0 + 1, 2 * c);
+    }
+    if (split == USP_SPLIT_STRIPE) return qpos < s ? 0u : min((qpos - s) / rd + 1, 2 * c);
     const uint32_t a0 = s * c, a1 = (2 * rd - 1 - s) * c;
     const uint32_t c0 = qpos < a0 ? 0u : min(qpos - a0 + 1, c);
     const uint32_t c1 = qpos < a1 ? 0u : min(qpos - a1 + 1, c);
@@ -136,17 +147,27 @@ __device__ __forceinline__ Work decode_work(const TcParams &p) {
     w.b = in % p.bs;
     w.u = in / p.bs;
     uint32_t qp;
-    if (p.lpt) {
-        // heaviest first: global 256-row blocks from the end of the sequence to its start
+    if (p.ring_rank_only > 0) {
+        // one ring rank's share only, its later rows (more keys) first
+        w.r = (uint32_t)(p.ring_rank_only - 1);
+        qp = p.npairs - 1 - outer;
+    } else if (p.lpt) {
+        // zigzag, heaviest first: global 256-row blocks from the end of the sequence to its start
         const uint32_t per_chunk = p.c / 256;
         const uint32_t gp = 2 * p.rd * per_chunk - 1 - outer;
         const uint32_t a = gp / per_chunk;
         const uint32_t off = (gp % per_chunk) * 256;
         w.r = a < p.rd ? a : 2 * p.rd - 1 - a;
         qp = ((a < p.rd) ? off : p.c + off) / 256;
+    } else if (p.split == USP_SPLIT_BASIC) {
+        // contiguous blocks: the last rank's last rows are the heaviest
+        const uint32_t gp = p.rd * p.npairs - 1 - outer;
+        w.r = gp / p.npairs;
+        qp = gp % p.npairs;
     } else {
-        w.r = outer / p.npairs;
-        qp = outer % p.npairs;
+        // stripe (and zigzag with chunks that are not whole 256-row blocks): later rows first
+        w.r = outer % p.rd;
+        qp = p.npairs - 1 - outer / p.rd;
     }
     w.kh = w.hl / p.G;
     w.q_row_base = (((w.r * p.ud + w.u) * p.Hl + w.hl) * p.bs + w.b) * p.Lr;
@@ -154,8 +175,8 @@ __device__ __forceinline__ Work decode_work(const TcParams &p) {
         w.q0[i] = qp * 256 + i * 128;
         w.valid[i] = w.q0[i] < p.Lr;
         const uint32_t last = min(w.q0[i] + 127, p.Lr - 1);
-        w.qpos_min[i] = zig32(w.r, min(w.q0[i], p.Lr - 1), p.c, p.rd);
-        w.qpos_max[i] = zig32(w.r, last, p.c, p.rd);
+        w.qpos_min[i] = pos32(p.split, w.r, min(w.q0[i], p.Lr - 1), p.c, p.rd);
+        w.qpos_max[i] = pos32(p.split, w.r, last, p.c, p.rd);
     }
     w.t_begin = p.mode == USP_MODE_FUSED ? 0 : p.step;
     w.t_end = p.mode == USP_MODE_FUSED ? (int)p.rd : p.step + 1;
@@ -170,8 +191,8 @@ __device__ __forceinline__ void iter_setup(const TcParams &p, const Work &w, Til
             it.nhi[i] = 0;
             it.nlo[i] = 0;
         } else if (p.causal) {
-            it.nhi[i] = vis32(w.qpos_max[i], it.s, p.c, p.rd);
-            it.nlo[i] = vis32(w.qpos_min[i], it.s, p.c, p.rd);
+            it.nhi[i] = vis32(p.split, w.qpos_max[i], it.s, p.c, p.rd);
+            it.nlo[i] = vis32(p.split, w.qpos_min[i], it.s, p.c, p.rd);
         } else {
             it.nhi[i] = p.Lr;
             it.nlo[i] = p.Lr;
@@ -276,88 +297,95 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
                    (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// One thread issues every MMA and commit. Per KV tile j, in order: PV_0(j), S_0(j+1) [commit: S_0
-// ready], PV_1(j) [commit: V stage of tile j free], S_1(j+1) [commits: S_1 ready, K stage of tile
-// j+1 free]. The tcgen05 fence follows only the waits on the softmax threads' P (TMA completion is
-// ordered by the mbarrier itself).
+// One thread per Q tile issues that tile's MMAs and commits, and the two take turns: S_0(0) | S_1(0) |
+// PV_0(0) S_0(1) | PV_1(0) S_1(1) | PV_0(1) S_0(2) | ... Each burst waits for its operands (V, P, K)
+// first and for its turn last, so it issues the moment the other burst has been queued: the tensor
+// core always has one issuer's burst running while the other issuer waits, and the two Q tiles stay
+// half a period apart (one tile's softmax runs while the other tile's MMAs run).
+// Per burst j of issuer i, in order: PV_i(j) [commit: V stage of tile j released by this issuer],
+// S_i(j+1) [commits: S_i ready, K stage of tile j+1 released by this issuer]. Stage barriers count one
+// release from each issuer. PV_i(j) and S_i(j+1) come from the same thread, so the tensor core runs
+// them in that order: S_i(j+1) overwrites the columns where P_i(j) lives only after PV_i(j) has read
+// them, and when the softmax sees S_i(j+1) complete, PV_i(j) is complete too (which makes its
+// in-place rescale of O_i safe). The tcgen05 fence follows only the wait on the softmax threads' P
+// (TMA completion is ordered by the mbarrier).
 template <int HD>
-__device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0, uint32_t tmem) {
+__device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0, uint32_t tmem, int i) {
     using C = Cfg<HD>;
-    auto BAR = [&](int i) { return bar0 + 8u * i; };
+    auto BAR = [&](int k) { return bar0 + 8u * k; };
     auto wait = [&](int bar, uint32_t parity) {
         return tc::mbar_wait(BAR(bar), parity, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
     };
     const uint32_t sQ = sbase + C::kQ, sK = sbase + C::kK, sV = sbase + C::kV;
-    // base descriptors: Q tiles and stage 0 of K / V (K-major: LBO unused, SBO = 8 rows x 128 B;
+    // base descriptors: this Q tile and stage 0 of K / V (K-major: LBO unused, SBO = 8 rows x 128 B;
     // V as MN-major: LBO = next 64-column block, SBO = next 8-key group)
-    const uint64_t qdesc[2] = {tc::sw128_desc(sQ, 16, 1024), tc::sw128_desc(sQ + C::kTileBytes, 16, 1024)};
+    const uint64_t qdesc = tc::sw128_desc(sQ + (uint32_t)i * C::kTileBytes, 16, 1024);
     const uint64_t kdesc0 = tc::sw128_desc(sK, 16, 1024);
     const uint64_t vdesc0 = tc::sw128_desc(sV, C::kBoxBytes, 1024);
     auto stage_off = [](uint32_t st) { return (uint64_t)((st * C::kTileBytes) >> 4); };
+    const uint32_t tS = tmem + C::colS(i), tO = tmem + C::colO(i);
+    const int barS = C::S_FULL + i, barP = C::P_FULL + i;
+    const int my_turn = C::TURN + i, other_turn = C::TURN + (1 - i);
+    // turn phases: issuer 0's burst j (j >= 0) waits for issuer 1's burst j-1; issuer 1's burst j
+    // (j >= -1) waits for issuer 0's burst j
+    uint32_t turns = 0;
+    auto take_turn = [&]() { return wait(my_turn, (turns++) & 1u); };
     bool ok = wait(C::Q_FULL, 0);
     TileIter it;
     iter_init(p, w, it);
     Tile cur, nxt;
     bool have = ok && iter_next(p, w, it, cur);
-    uint32_t pc[2] = {0, 0}, started[2] = {0, 0};
+    uint32_t pc = 0, started = 0;
     uint32_t j = 0;
     if (have) {
         ok = wait(C::K_FULL + 0, 0);
+        if (ok && i == 1) ok = take_turn();
         if (ok) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                if (cur.act[i]) {
-                    issue_s<HD>(tmem + C::colS(i), qdesc[i], kdesc0);
-                    tc::mma_commit(BAR(C::S_FULL + i));
-                }
+            if (i ? cur.act[1] : cur.act[0]) {
+                issue_s<HD>(tS, qdesc, kdesc0);
+                tc::mma_commit(BAR(barS));
+            }
             tc::mma_commit(BAR(C::K_EMPTY + 0));
+            tc::mbar_arrive(BAR(other_turn));
         }
     }
     while (ok && have) {
         const bool have_n = iter_next(p, w, it, nxt);
         const uint32_t st = j % C::kStages, ph = (j / C::kStages) & 1u;
         const uint32_t stn = (j + 1) % C::kStages, phn = ((j + 1) / C::kStages) & 1u;
+        const bool act = i ? cur.act[1] : cur.act[0];
+        // operands first: every issuer waits for a stage's fill before releasing it, even when its Q
+        // tile skips the tile, so neither issuer can release fill f + kStages before the producer has
+        // refilled the stage (which needs both releases of fill f): the shared release barrier never
+        // runs ahead
         if (!(ok = wait(C::V_FULL + st, ph))) break;
-        bool kn_ready = false;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            if (ok && cur.act[i]) {
-                ok = wait(C::P_FULL + i, pc[i] & 1u);
-                if (ok) {
-                    ++pc[i];
-                    tc::fence_after_sync();
-                    issue_pv<HD>(tmem + C::colO(i), tmem + C::colS(i), vdesc0 + stage_off(st), started[i]);
-                    started[i] = 1;
-                }
-            }
-            if (ok && have_n && nxt.act[i]) {
-                if (!kn_ready) {
-                    ok = wait(C::K_FULL + stn, phn);
-                    kn_ready = true;
-                }
-                if (ok) {
-                    issue_s<HD>(tmem + C::colS(i), qdesc[i], kdesc0 + stage_off(stn));
-                    tc::mma_commit(BAR(C::S_FULL + i));
-                }
-            }
+        if (act && !(ok = wait(barP, pc & 1u))) break;
+        if (have_n && !(ok = wait(C::K_FULL + stn, phn))) break;
+        if (!(ok = take_turn())) break;
+        if (act) {
+            ++pc;
+            tc::fence_after_sync();
+            issue_pv<HD>(tO, tS, vdesc0 + stage_off(st), started);
+            started = 1;
         }
-        if (!ok) break;
-        tc::mma_commit(BAR(C::V_EMPTY + st));  // V(j) is no longer read
+        tc::mma_commit(BAR(C::V_EMPTY + st));  // this issuer no longer reads V(j)
         if (have_n) {
-            if (!kn_ready) {
-                if (!(ok = wait(C::K_FULL + stn, phn))) break;
+            if (i ? nxt.act[1] : nxt.act[0]) {
+                issue_s<HD>(tS, qdesc, kdesc0 + stage_off(stn));
+                tc::mma_commit(BAR(barS));
             }
-            tc::mma_commit(BAR(C::K_EMPTY + stn));  // K(j+1) is no longer read
+            tc::mma_commit(BAR(C::K_EMPTY + stn));  // this issuer no longer reads K(j+1)
         }
+        tc::mbar_arrive(BAR(other_turn));
         cur = nxt;
         have = have_n;
         ++j;
     }
-    tc::mma_commit(BAR(C::O_FULL + 0));
-    tc::mma_commit(BAR(C::O_FULL + 1));
-    // every MMA of this CTA has finished before tensor memory is released
-    tc::mma_commit(BAR(C::DONE));
-    wait(C::DONE, 0);
+    if (!ok) tc::mbar_arrive(BAR(other_turn));  // let the other issuer reach its own bounded exit
+    tc::mma_commit(BAR(C::O_FULL + i));
+    // every MMA of this issuer has finished before tensor memory is released
+    tc::mma_commit(BAR(C::DONE + i));
+    wait(C::DONE + i, 0);
 }
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -415,7 +443,7 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     const bool valid = i ? w.valid[1] : w.valid[0];
     const uint32_t row_local = q0 + row;
     const bool row_ok = valid && row_local < p.Lr;
-    const uint32_t qpos_row = zig32(w.r, min(row_local, p.Lr - 1), p.c, p.rd);
+    const uint32_t qpos_row = pos32(p.split, w.r, min(row_local, p.Lr - 1), p.c, p.rd);
     const float sl2 = p.scale_log2;
     const uint64_t sl22 = tc::pack2(sl2, sl2);
 
@@ -433,7 +461,7 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
         const bool full = i ? tl.full[1] : tl.full[0];
         if (tl.s != s_cur) {
             s_cur = tl.s;
-            lim = p.causal ? vis32(qpos_row, s_cur, p.c, p.rd) : p.Lr;
+            lim = p.causal ? vis32(p.split, qpos_row, s_cur, p.c, p.rd) : p.Lr;
         }
         ok = tc::mbar_wait(barS, n_act & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
@@ -563,9 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         *skip_flag = (*reinterpret_cast<volatile int *>(p.status) != 0) ? 1u : 0u;
         for (int s = 0; s < C::kStages; ++s) {
             tc::mbar_init(bar0 + 8u * (C::K_FULL + s), 1);
-            tc::mbar_init(bar0 + 8u * (C::K_EMPTY + s), 1);
+            tc::mbar_init(bar0 + 8u * (C::K_EMPTY + s), 2);  // one release per MMA issuer
             tc::mbar_init(bar0 + 8u * (C::V_FULL + s), 1);
-            tc::mbar_init(bar0 + 8u * (C::V_EMPTY + s), 1);
+            tc::mbar_init(bar0 + 8u * (C::V_EMPTY + s), 2);
         }
         tc::mbar_init(bar0 + 8u * C::Q_FULL, 1);
         for (int i = 0; i < 2; ++i) {
@@ -574,6 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             tc::mbar_init(bar0 + 8u * (C::O_FULL + i), 1);
         }
         tc::mbar_init(bar0 + 8u * C::DONE, 1);
+        tc::mbar_init(bar0 + 8u * (C::DONE + 1), 1);
+        tc::mbar_init(bar0 + 8u * C::TURN, 1);
+        tc::mbar_init(bar0 + 8u * (C::TURN + 1), 1);
         tc::fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -598,7 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             if (warp == kProducerWarp && lane == 0)
                 producer_role<HD>(p, w, sbase, bar0);
             else if (warp == kMmaWarp && lane == 0)
-                mma_role<HD>(p, w, sbase, bar0, tmem);
+                mma_role<HD>(p, w, sbase, bar0, tmem, 0);
+            else if (warp == kMmaWarp1 && lane == 0)
+                mma_role<HD>(p, w, sbase, bar0, tmem, 1);
             __syncwarp();
         }
     } else {
@@ -695,9 +728,12 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     p.causal = a.causal;
     p.mode = a.mode;
     p.step = a.step;
-    p.lpt = (p.c % 256 == 0) ? 1 : 0;
+    p.split = a.split;
+    p.ring_rank_only = a.ring_rank_only;
+    p.lpt = (p.split == USP_SPLIT_ZIGZAG && p.c % 256 == 0) ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const uint64_t grid = (uint64_t)p.rd * p.ud * p.Hl * p.bs * p.npairs;
+    const uint64_t ranks = a.ring_rank_only > 0 ? 1 : (uint64_t)p.rd;
+    const uint64_t grid = ranks * p.ud * p.Hl * p.bs * p.npairs;
     if (grid == 0) return USP_OK;
     if (grid >= (1ull << 31)) return USP_ERR_UNSUPPORTED;
     return a.hd == 128 ? launch_typed<128>(p, (uint32_t)grid, s) : launch_typed<64>(p, (uint32_t)grid, s);

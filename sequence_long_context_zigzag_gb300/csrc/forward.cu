@@ -18,18 +18,19 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct FwdShape {
     int64_t bs, L;
-    int hq, hkv, hd, rd, ud, hc, hkc, G, es;
+    int hq, hkv, hd, rd, ud, hc, hkc, G, es, split;
     size_t q_grp, kv_grp, lse_grp;  // bytes of one group's q / k (or v) / lse, any layout
 };
 
 int fwd_shape(const usp_attn_desc &d, int head_chunk, FwdShape &s) {
     if (d.bs < 0 || d.L < 0 || d.hq <= 0 || d.hkv <= 0 || d.rd <= 0 || d.ud <= 0) return USP_ERR_INVALID_ARG;
-    if (d.mode != USP_MODE_FUSED) return USP_ERR_INVALID_ARG;
+    if (d.mode != USP_MODE_FUSED || d.ring_rank_only != 0) return USP_ERR_INVALID_ARG;
     s.es = elem_size(d.dtype);
     if (s.es == 0) return USP_ERR_DTYPE;
     if (d.hq % d.hkv != 0) return USP_ERR_SHAPE;
     s.bs = d.bs; s.L = d.L; s.hq = d.hq; s.hkv = d.hkv; s.hd = d.hd; s.rd = d.rd; s.ud = d.ud;
     s.G = d.hq / d.hkv;
+    s.split = d.split;
     s.hc = head_chunk > 0 ? head_chunk : d.hq;
     if (s.hc > d.hq || d.hq % s.hc != 0 || s.hc % s.G != 0) return USP_ERR_SHAPE;
     s.hkc = s.hc / s.G;
@@ -69,7 +70,7 @@ struct Carve {
 usp_dims dims_of(const FwdShape &s, int H, int H_total, int h0, int hd, int dtype) {
     usp_dims d{};
     d.bs = s.bs; d.L = s.L; d.H = H; d.hd = hd; d.dtype = dtype; d.rd = s.rd; d.ud = s.ud;
-    d.H_total = H_total; d.h0 = h0;
+    d.H_total = H_total; d.h0 = h0; d.split = s.split;
     return d;
 }
 

@@ -3,10 +3,12 @@
 // bijection between rows, so the kernel maps row indices and copies rows bit-exactly.
 //
 // Modes: the split (natural -> local) and its inverse, the all-to-all (local -> head-sharded) and its
-// inverse, and the two composed in one pass (natural -> head-sharded and back). Composing them
-// gives a direct map: row p of ring rank r in the head-sharded layout is global token zig(r, p),
-// because the all-to-all concatenates the Ulysses ranks' pieces in rank order, which is exactly the
-// ring-local sequence Algorithm 2 chunked. The composed pass reads and writes each tensor once.
+// inverse, and the two composed in one pass (natural -> head-sharded and back). Composing them gives
+// a direct map: row p of ring rank r in the head-sharded layout is global token zig(r, p), because
+// the all-to-all concatenates the Ulysses ranks' pieces in rank order, which is exactly the
+// ring-local sequence Algorithm 2 chunked. The composed pass reads and writes each tensor once. The
+// zigzag split is the default; the plain ring's contiguous split and the round-robin stripe split
+// use the same kernel with another position map.
 //
 // Work split: one warp owns a batch of 32 logical rows. Lane l computes the source and destination
 // row of row l of the batch (integer index math with multiply-high division), publishes them in
@@ -28,7 +30,7 @@ struct PermJobK {
 };
 
 struct PermK {
-    int mode, njobs;
+    int mode, split, njobs;
     PermJobK job[kMaxPermJobs];
     uint32_t nbatch;  // total warp batches over all tensors
     uint32_t bs, L, rd, ud, Lu, Lr, c;
@@ -53,7 +55,7 @@ __device__ __forceinline__ void map_row(const PermK &p, const PermJobK &jb, uint
         } else {
             p.f_ud.divmod(q, r, u);
         }
-        const int64_t g = zig_pos(r, (int64_t)u * p.Lu + j, p.c, p.rd);
+        const int64_t g = split_pos(p.split, r, (int64_t)u * p.Lu + j, p.c, p.rd);
         const int64_t nat = ((int64_t)b * p.L + g) * jb.Ht + jb.h0 + h;
         if (p.mode == PERM_EXTRACT) { srow = nat; drow = i; }
         else { srow = i; drow = nat; }
@@ -71,7 +73,7 @@ __device__ __forceinline__ void map_row(const PermK &p, const PermJobK &jb, uint
             srow = ((((int64_t)r * p.ud + u) * p.bs + b) * p.Lu + j) * jb.Ht + head;
             drow = i;
         } else {
-            const int64_t nat = ((int64_t)b * p.L + zig_pos(r, pp, p.c, p.rd)) * jb.Ht + head;
+            const int64_t nat = ((int64_t)b * p.L + split_pos(p.split, r, pp, p.c, p.rd)) * jb.Ht + head;
             if (p.mode == PERM_FUSED_FWD) { srow = nat; drow = i; }
             else { srow = i; drow = nat; }
         }
@@ -149,6 +151,7 @@ int launch_permute(const PermArgs &a, cudaStream_t s) {
     if (a.njobs < 1 || a.njobs > kMaxPermJobs) return USP_ERR_INVALID_ARG;
     PermK p{};
     p.mode = a.mode;
+    p.split = a.split;
     p.njobs = a.njobs;
     p.bs = (uint32_t)a.bs;
     p.L = (uint32_t)a.L;

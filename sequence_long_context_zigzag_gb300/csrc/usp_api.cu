@@ -39,6 +39,7 @@ static int check_dims(const usp_dims &d, int need_head_split) {
         d.H_total < 0)
         return USP_ERR_INVALID_ARG;
     if (elem_size(d.dtype) == 0) return USP_ERR_DTYPE;
+    if (d.split < USP_SPLIT_ZIGZAG || d.split > USP_SPLIT_STRIPE) return USP_ERR_INVALID_ARG;
     if (d.L % (2 * (int64_t)d.rd) != 0) return USP_ERR_SHAPE;
     if ((d.L / d.rd) % d.ud != 0) return USP_ERR_SHAPE;
     int32_t Ht = d.H_total ? d.H_total : d.H;
@@ -92,6 +93,7 @@ int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, int invers
     a.job[0] = PermJob{static_cast<const char *>(src), static_cast<char *>(dst), d.H, d.H_total ? d.H_total : d.H,
                        d.h0};
     a.mode = inverse ? PERM_EXTRACT_INV : PERM_EXTRACT;
+    a.split = d.split;
     a.bs = d.bs; a.L = d.L;
     a.rd = d.rd; a.ud = d.ud; a.row_bytes = row_bytes;
     a.r_fixed = vr >= 0 ? vr / d.ud : -1;
@@ -132,7 +134,7 @@ int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_d
         int rc = check_dims(dk, 1);
         if (rc) return rc;
         if (dk.bs != d[0].bs || dk.L != d[0].L || dk.rd != d[0].rd || dk.ud != d[0].ud || dk.hd != d[0].hd ||
-            dk.dtype != d[0].dtype)
+            dk.dtype != d[0].dtype || dk.split != d[0].split)
             return USP_ERR_SHAPE;
         work += dk.bs * dk.L * (int64_t)dk.H;
         a.job[k] = PermJob{static_cast<const char *>(src[k]), static_cast<char *>(dst[k]), dk.H,
@@ -146,6 +148,7 @@ int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_d
         int rc = check_ptr_align(src[k], dst[k], row_bytes);
         if (rc) return rc;
     }
+    a.split = d[0].split;
     a.bs = d[0].bs; a.L = d[0].L;
     a.rd = d[0].rd; a.ud = d[0].ud; a.row_bytes = row_bytes;
     return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
@@ -157,6 +160,8 @@ int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *
         return USP_ERR_INVALID_ARG;
     if (d.mode < USP_MODE_FUSED || d.mode > USP_MODE_ACCUM) return USP_ERR_INVALID_ARG;
     if (d.mode != USP_MODE_FUSED && (d.step < 0 || d.step >= d.rd)) return USP_ERR_INVALID_ARG;
+    if (d.split < USP_SPLIT_ZIGZAG || d.split > USP_SPLIT_STRIPE) return USP_ERR_INVALID_ARG;
+    if (d.ring_rank_only < 0 || d.ring_rank_only > d.rd) return USP_ERR_INVALID_ARG;
     if (elem_size(d.dtype) == 0) return USP_ERR_DTYPE;
     if (d.L % (2 * (int64_t)d.rd) != 0 || (d.L / d.rd) % d.ud != 0) return USP_ERR_SHAPE;
     if (d.hq % d.hkv != 0 || d.hq % d.ud != 0 || d.hkv % d.ud != 0) return USP_ERR_SHAPE;
@@ -171,6 +176,7 @@ int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *
     a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
     a.bs = d.bs; a.L = d.L; a.hq = d.hq; a.hkv = d.hkv; a.hd = d.hd; a.rd = d.rd; a.ud = d.ud;
     a.dtype = d.dtype; a.causal = d.causal ? 1 : 0; a.mode = d.mode; a.step = d.step;
+    a.split = d.split; a.ring_rank_only = d.ring_rank_only;
     a.scale = d.scale > 0.f ? d.scale : 1.0f / sqrtf((float)d.hd);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (d.dtype == USP_BF16) return launch_attn_tc(a, s);

@@ -35,14 +35,4 @@ __device__ __forceinline__ void merge_weights(float l1, float l2, float &w1, flo
     w2 = e2 ? 0.f : expf(l2 - l);
 }
 
-// Number of ring-local rows p of ring rank s whose global position zig(s, p) is <= qpos
-// (zig is increasing in p, so the visible keys of a rank form a prefix).
-__device__ __forceinline__ int64_t visible_prefix(int64_t qpos, int64_t s, int64_t c, int64_t rd) {
-    int64_t c0 = qpos - s * c + 1;
-    c0 = c0 < 0 ? 0 : (c0 > c ? c : c0);
-    int64_t c1 = qpos - (2 * rd - 1 - s) * c + 1;
-    c1 = c1 < 0 ? 0 : (c1 > c ? c : c1);
-    return c0 + c1;
-}
-
 }  // namespace usp

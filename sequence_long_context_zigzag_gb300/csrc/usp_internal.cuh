@@ -40,6 +40,34 @@ __host__ __device__ __forceinline__ int64_t zig_pos(int64_t r, int64_t p, int64_
     return p < c ? r * c + p : (2 * rd - 1 - r) * c + (p - c);
 }
 
+// global position of ring-local row p on ring rank r under a split (usp_split); Lr = 2 c rows per rank
+__host__ __device__ __forceinline__ int64_t split_pos(int split, int64_t r, int64_t p, int64_t c, int64_t rd) {
+    if (split == USP_SPLIT_BASIC) return r * 2 * c + p;
+    if (split == USP_SPLIT_STRIPE) return p * rd + r;
+    return zig_pos(r, p, c, rd);
+}
+
+// number of ring-local rows of rank s whose global position is <= qpos; every split's position map
+// is increasing in the row, so those rows are a prefix
+__host__ __device__ __forceinline__ int64_t split_visible(int split, int64_t qpos, int64_t s, int64_t c,
+                                                          int64_t rd) {
+    const int64_t Lr = 2 * c;
+    if (split == USP_SPLIT_BASIC) {
+        const int64_t v = qpos - s * Lr + 1;
+        return v < 0 ? 0 : (v > Lr ? Lr : v);
+    }
+    if (split == USP_SPLIT_STRIPE) {
+        if (qpos < s) return 0;
+        const int64_t v = (qpos - s) / rd + 1;
+        return v > Lr ? Lr : v;
+    }
+    int64_t c0 = qpos - s * c + 1;
+    c0 = c0 < 0 ? 0 : (c0 > c ? c : c0);
+    int64_t c1 = qpos - (2 * rd - 1 - s) * c + 1;
+    c1 = c1 < 0 ? 0 : (c1 > c ? c : c1);
+    return c0 + c1;
+}
+
 // per-device cached properties and the device status word address
 struct DeviceInfo {
     int sm_count;
@@ -74,6 +102,7 @@ struct PermJob {
 
 struct PermArgs {
     int mode;
+    int split;
     int njobs;
     PermJob job[kMaxPermJobs];
     int64_t bs, L;
@@ -91,7 +120,7 @@ struct AttnArgs {
     void *out;
     float *lse;
     int64_t bs, L;
-    int32_t hq, hkv, hd, rd, ud, dtype, causal, mode, step;
+    int32_t hq, hkv, hd, rd, ud, dtype, causal, mode, step, split, ring_rank_only;
     float scale;
 };
 int launch_attn_simt(const AttnArgs &a, cudaStream_t s);

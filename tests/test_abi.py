@@ -40,8 +40,8 @@ def test_version_and_strerror():
     assert "unknown" in _abi.strerror(12345)
 
 
-def dims(bs=1, L=64, H=4, hd=128, dtype=_abi.USP_BF16, rd=2, ud=2, H_total=0, h0=0):
-    return _abi.UspDims(bs, L, H, hd, dtype, rd, ud, H_total, h0)
+def dims(bs=1, L=64, H=4, hd=128, dtype=_abi.USP_BF16, rd=2, ud=2, H_total=0, h0=0, split=0):
+    return _abi.UspDims(bs, L, H, hd, dtype, rd, ud, H_total, h0, split)
 
 
 BAD = 0x1001  # never dereferenced: every case below is rejected before a launch
@@ -55,6 +55,7 @@ BAD = 0x1001  # never dereferenced: every case below is rejected before a launch
     (dims(rd=0), _abi.USP_ERR_INVALID_ARG),
     (dims(hd=0), _abi.USP_ERR_INVALID_ARG),
     (dims(H_total=4, h0=2), _abi.USP_ERR_SHAPE),  # window past the end
+    (dims(split=3), _abi.USP_ERR_INVALID_ARG),     # unknown split
 ])
 def test_a2a_rejects(d, code):
     assert _abi.load().usp_a2a4d(BAD, BAD, d, 1, None) == code
@@ -82,7 +83,7 @@ def test_extract_rejects():
 
 def desc(**kw):
     base = dict(bs=1, L=256, hq=4, hkv=2, hd=128, rd=2, ud=2, dtype=_abi.USP_BF16, causal=1, scale=0.0,
-                mode=0, step=0)
+                mode=0, step=0, split=0, ring_rank_only=0)
     base.update(kw)
     return _abi.UspAttnDesc(*[base[f] for f, _ in _abi.UspAttnDesc._fields_])
 
@@ -96,6 +97,8 @@ def desc(**kw):
     (dict(mode=1, step=2), _abi.USP_ERR_INVALID_ARG),
     (dict(dtype=5), _abi.USP_ERR_DTYPE),
     (dict(scale=float("nan")), _abi.USP_ERR_INVALID_ARG),
+    (dict(split=5), _abi.USP_ERR_INVALID_ARG),
+    (dict(ring_rank_only=3), _abi.USP_ERR_INVALID_ARG),   # rank 2 of rd = 2 does not exist
     (dict(), _abi.USP_ERR_ALIGN),
 ])
 def test_attn_rejects(kw, code):
