@@ -273,17 +273,28 @@ def a2a_fwd(loc, ud):
     tokens, shape (hc/N, bs, L, hd)); out[r,u',h',b,u*Lu+j] = in[r,u,b,j,u'*(H/ud)+h'].
     Gathered pieces are concatenated by source Ulysses rank ascending, which restores the ring-local
     order of Algorithm 2 step 6.
+
+    Fewer heads than Ulysses ranks (K/V of GQA/MQA with hkv < ud; the USP review's section 三 gives
+    the all-to-all the job of handling K/V head counts that differ from Q's): with ud % H == 0,
+    each rank receives the one head its query heads read, head u' // (ud/H), so every head is
+    replicated on ud/H ranks and out is [rd][ud][1][bs][Lr][...]: out[r,u',0,b,u*Lu+j] =
+    in[r,u,b,j,u'//(ud/H)].
     """
     loc = np.asarray(loc)
     rd, ud2, bs, Lu, H = loc.shape[:5]
-    assert ud2 == ud and H % ud == 0
-    Hl, Lr = H // ud, ud * Lu
+    assert ud2 == ud
+    Lr = ud * Lu
     R = np.arange(rd).reshape(rd, 1, 1, 1, 1)
     Uo = np.arange(ud).reshape(1, ud, 1, 1, 1)
-    Ho = np.arange(Hl).reshape(1, 1, Hl, 1, 1)
     B = np.arange(bs).reshape(1, 1, 1, bs, 1)
     P = np.arange(Lr).reshape(1, 1, 1, 1, Lr)
-    return loc[R, P // Lu, B, P % Lu, Uo * Hl + Ho]
+    if H % ud == 0:
+        Hl = H // ud
+        Ho = np.arange(Hl).reshape(1, 1, Hl, 1, 1)
+        return loc[R, P // Lu, B, P % Lu, Uo * Hl + Ho]
+    assert ud % H == 0, "head count must divide by ud or divide ud"
+    rep = ud // H
+    return loc[R, P // Lu, B, P % Lu, Uo // rep]
 
 
 def a2a_inv(hs, ud):
@@ -332,10 +343,10 @@ def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True, split="zigzag"):
     if scale is None:
         scale = 1.0 / math.sqrt(hd)
     c, Lr, _ = _dims(L, rd, ud)
-    if hq % ud or hkv % ud or hq % hkv:
-        raise ValueError("head counts must divide by ud and hq by hkv")
+    if hq % ud or hq % hkv or (hkv % ud and ud % hkv):
+        raise ValueError("hq must divide by ud and by hkv; hkv must divide by ud or divide ud")
     Q = a2a_fwd(extract_local(q, rd, ud, split=split), ud)          # [rd][ud][hq/ud][bs][Lr][hd]
-    K = a2a_fwd(extract_local(k, rd, ud, split=split), ud)          # [rd][ud][hkv/ud][bs][Lr][hd]
+    K = a2a_fwd(extract_local(k, rd, ud, split=split), ud)          # [rd][ud][max(hkv/ud,1)][bs][Lr][hd]
     V = a2a_fwd(extract_local(v, rd, ud, split=split), ud)
     pos = [split_pos(split, r, np.arange(Lr), L, rd) for r in range(rd)]
     O = np.zeros_like(Q)

@@ -239,6 +239,24 @@ def test_a2a_ud1_is_transpose():
     assert np.array_equal(hs[:, 0], loc[:, 0].transpose(0, 3, 1, 2, 4))
 
 
+@pytest.mark.parametrize("rd,ud,H", [(2, 4, 1), (1, 4, 2), (2, 2, 1), (3, 8, 2)])
+def test_a2a_replicates_when_fewer_heads_than_ranks(rd, ud, H):
+    """hkv < ud: rank u' of every Ulysses group receives head u' // (ud/H) for the whole ring-local
+    sequence, i.e. exactly what the ud = 1 split gives for that head (an independent map)."""
+    L = 2 * rd * ud * 2
+    x = np.arange(2 * L * H * 3).reshape(2, L, H, 3)
+    hs = oracle.a2a_fwd(oracle.extract_local(x, rd, ud), ud)
+    assert hs.shape == (rd, ud, 1, 2, L // rd, 3)
+    rep = ud // H
+    for h in range(H):
+        ring_local = oracle.extract_local(x, rd, 1, h0=h, H=1)       # [rd][1][bs][Lr][1][3]
+        for u in range(h * rep, (h + 1) * rep):
+            assert np.array_equal(hs[:, u, 0], ring_local[:, 0, :, :, 0])
+    # every element of x shows up exactly rep times
+    counts = np.bincount(hs.ravel(), minlength=x.size)
+    assert np.all(counts == rep)
+
+
 def test_lse_as_rows_of_one():
     """lse is permuted as a tensor whose rows hold one value: same maps with a trailing axis of 1."""
     hs = np.arange(2 * 2 * 3 * 1 * 8).reshape(2, 2, 3, 1, 8).astype(float)
@@ -263,6 +281,27 @@ def test_literal_pipeline_equals_direct(L, hd, rd, ud, G):
     o, l = oracle.literal_pipeline(q, k, v, rd, ud)
     np.testing.assert_allclose(o, o_ref, atol=1e-12, rtol=0)
     np.testing.assert_allclose(l, l_ref, atol=1e-12, rtol=1e-12)
+
+
+@pytest.mark.parametrize("L,rd,ud,hq,hkv", [(16, 2, 4, 4, 1), (16, 2, 4, 8, 2), (16, 1, 4, 4, 1),
+                                              (24, 3, 2, 2, 1), (32, 2, 8, 8, 2), (32, 4, 2, 4, 1)])
+def test_literal_pipeline_kv_replication_equals_direct(L, rd, ud, hq, hkv):
+    """MQA / GQA with ud > hkv: the replicated K/V all-to-all still gives plain causal attention
+    (checked against torch's CPU flash routine as well)."""
+    q, k, v = make_qkv(1, L, hq, hkv, 4, "f32", seed=L + rd * 10 + ud * 100 + hkv)
+    o_ref, l_ref = oracle.attn_direct(q, k, v, causal=True)
+    o, l = oracle.literal_pipeline(q, k, v, rd, ud)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(l, l_ref, atol=1e-12, rtol=1e-12)
+    o_lib, l_lib = torch_lib_attn(q, k, v, 0.5, True)
+    np.testing.assert_allclose(o, o_lib, atol=1e-10)
+    np.testing.assert_allclose(l, l_lib, atol=1e-10)
+
+
+def test_literal_pipeline_rejects_uneven_kv_heads():
+    q, k, v = make_qkv(1, 16, 6, 3, 4, "f32", seed=5)
+    with pytest.raises(ValueError):
+        oracle.literal_pipeline(q, k, v, 2, 2)
 
 
 def test_literal_pipeline_noncausal_and_batch():
