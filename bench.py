@@ -171,8 +171,9 @@ class Step:
         dev, dt = q.device, q.dtype
         self.groups = [(g0, g0 // G) for g0 in range(0, w.hq, hc)]
         self.hc, self.hkc = hc, hkc
+        hks = usp.heads_per_rank(hkc, ud) * ud  # head-sharded K/V heads (replicas when hkc < ud)
         self.qh = torch.empty(rd, ud, hc // ud, bs, Lr, hd, device=dev, dtype=dt)
-        self.kh = torch.empty(rd, ud, hkc // ud, bs, Lr, hd, device=dev, dtype=dt)
+        self.kh = torch.empty(rd, ud, hks // ud, bs, Lr, hd, device=dev, dtype=dt)
         self.vh = torch.empty_like(self.kh)
         self.oh = torch.empty_like(self.qh)
         self.lh = torch.empty(rd, ud, hc // ud, bs, Lr, device=dev, dtype=torch.float32)
@@ -180,9 +181,11 @@ class Step:
         self.l_loc = torch.empty(rd, ud, bs, Lu, w.hq, device=dev, dtype=torch.float32)
         es = q.element_size()
         # algorithmic permute bytes per step: one read + one write of every moved tensor (the composed
-        # split + all-to-all reads and writes each of Q, K, V once)
+        # split + all-to-all reads and writes each of Q, K, V once; replicated K/V heads are read once
+        # and written once per replica)
         tok = bs * L
-        self.permute_bytes = 2 * (tok * (hc + 2 * hkc) * hd * es + tok * hc * (hd * es + 4)) * len(self.groups)
+        self.permute_bytes = (tok * (2 * hc + 2 * (hkc + hks)) * hd * es
+                              + 2 * tok * hc * (hd * es + 4)) * len(self.groups)
         self.launches_per_step = 4 * len(self.groups)
         self.attn_events = []
         self.perm_events = []
@@ -200,7 +203,7 @@ class Step:
             if record:
                 e1 = torch.cuda.Event(enable_timing=True)
                 e1.record(st)
-            usp.usp_attn_fwd(self.qh, self.kh, self.vh, self.oh, self.lh, causal=w.causal)
+            usp.usp_attn_fwd(self.qh, self.kh, self.vh, self.oh, self.lh, causal=w.causal, hkv=self.hkc)
             if record:
                 e2 = torch.cuda.Event(enable_timing=True)
                 e2.record(st)
@@ -224,7 +227,7 @@ def rank_balance(usp, w, q, k, v, reps=5):
     rd, ud, bs, L, hd = w.rd, w.ud, w.bs, w.L, w.hd
     dev, dt = q.device, q.dtype
     qh = torch.empty(rd, ud, hc // ud, bs, L // rd, hd, device=dev, dtype=dt)
-    kh = torch.empty(rd, ud, hkc // ud, bs, L // rd, hd, device=dev, dtype=dt)
+    kh = torch.empty(rd, ud, usp.heads_per_rank(hkc, ud), bs, L // rd, hd, device=dev, dtype=dt)
     vh = torch.empty_like(kh)
     oh = torch.empty_like(qh)
     lh = torch.empty(qh.shape[:5], device=dev, dtype=torch.float32)
@@ -237,7 +240,7 @@ def rank_balance(usp, w, q, k, v, reps=5):
             for _ in range(reps):
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
-                usp.usp_attn_fwd(qh, kh, vh, oh, lh, causal=w.causal, split=split, ring_rank=r)
+                usp.usp_attn_fwd(qh, kh, vh, oh, lh, causal=w.causal, split=split, ring_rank=r, hkv=hkc)
                 e1.record()
                 torch.cuda.synchronize()
                 ts.append(e0.elapsed_time(e1))
@@ -335,13 +338,13 @@ def run_reference(args, dist):
 
 def e2e_head_chunk(w):
     """Head groups for the host-buffer pipeline: the workload's own chunking, else about four groups
-    (each a multiple of hq/hkv whose KV heads divide by ud), so copies overlap kernels."""
+    (each a multiple of hq/hkv whose KV heads divide by ud or divide ud), so copies overlap kernels."""
     if w.head_chunk:
         return w.head_chunk
     G = w.hq // w.hkv
     for n in (4, 2):
         hc = w.hq // n
-        if w.hq % n == 0 and hc % G == 0 and hc % w.ud == 0 and (hc // G) % w.ud == 0:
+        if w.hq % n == 0 and hc % G == 0 and hc % w.ud == 0 and ((hc // G) % w.ud == 0 or w.ud % (hc // G) == 0):
             return hc
     return None
 

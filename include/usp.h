@@ -22,7 +22,14 @@
  *    Lu = L / (rd ud) tokens per virtual rank, Hl = H / ud heads per Ulysses rank.
  *  - Shapes: L % (2 rd) == 0 and Lr % ud == 0 (equal chunks, as torch.chunk gives in the pages'
  *    setting); H % ud == 0 for an all-to-all (the Ulysses degree divides the head count, the
- *    Context-Parallel page's "head 数整除检查"); hq % hkv == 0. Violations return USP_ERR_SHAPE.
+ *    Context-Parallel page's "head 数整除检查"); hq % hkv == 0. One exception: the forward
+ *    all-to-all of K/V also accepts fewer heads than Ulysses ranks when H divides ud (GQA/MQA,
+ *    below). Violations return USP_ERR_SHAPE.
+ *  - GQA/MQA with hkv < ud: the USP review's section 三 gives AllToAll4D the job of handling K/V
+ *    head counts that differ from Q's, without details. Reading taken here: Ulysses rank u' holds
+ *    query heads [u' Hl, (u' + 1) Hl), which all read KV head u' / (ud / hkv); the forward
+ *    all-to-all sends it that head only, so each KV head is replicated on ud / hkv ranks and the
+ *    head-sharded K/V carries Hkl = 1 head per rank (Hkl = hkv / ud otherwise).
  *  - Sizes: every row count handled by one call must stay below 2^31.
  */
 #ifndef USP_H
@@ -109,6 +116,9 @@ USP_API int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, in
  *   head-sharded[r][u'][h'][b][u Lu + j] = sequence-sharded[r][u][b][j][h0 + u' Hl + h'],
  *   i.e. pieces are gathered by source Ulysses rank ascending.
  * dir == +1: sequence-sharded -> head-sharded.  dir == -1: head-sharded -> sequence-sharded.
+ * dir == +1 with H < ud and ud % H == 0 replicates (K/V under GQA/MQA): head-sharded is
+ *   [rd][ud][1][bs][Lr][hd] and head-sharded[r][u'][0][b][u Lu + j] =
+ *   sequence-sharded[r][u][b][j][h0 + u' / (ud / H)]. dir == -1 needs H % ud == 0.
  * Alignment and overlap rules as for usp_extract_local. An lse tensor is moved with hd = 1, USP_F32.
  */
 USP_API int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stream);
@@ -125,8 +135,10 @@ USP_API int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_strea
  *
  *   n         : number of tensors, 1 <= n <= 4
  *   src, dst  : HOST arrays of n DEVICE pointers. inverse == 0: src[k] natural (bs, L, H_total, hd),
- *               dst[k] head-sharded [rd][ud][H/ud][bs][Lr][hd]; inverse != 0: the other way round
- *               (heads outside the window of the natural tensor are left untouched).
+ *               dst[k] head-sharded [rd][ud][H/ud][bs][Lr][hd] (or, when H < ud and ud % H == 0,
+ *               [rd][ud][1][bs][Lr][hd] holding head u' / (ud / H) on rank u', as usp_a2a4d);
+ *               inverse != 0: the other way round, H % ud == 0 (heads outside the window of the
+ *               natural tensor are left untouched).
  *   d         : HOST array of n dims; bs, L, rd, ud, hd and dtype must agree (USP_ERR_SHAPE
  *               otherwise); H, H_total and h0 may differ (Q and K/V head counts under GQA).
  * Alignment and overlap rules as for usp_extract_local.
@@ -167,7 +179,8 @@ typedef struct {
  * (at step t ring rank r works on the KV block of rank (r - t) mod rd).
  *
  *   q, out : [rd][ud][hq/ud][bs][Lr][hd]   (head-sharded, as usp_a2a4d dir=+1 writes it)
- *   k, v   : [rd][ud][hkv/ud][bs][Lr][hd]
+ *   k, v   : [rd][ud][Hkl][bs][Lr][hd], Hkl = hkv/ud, or 1 when hkv < ud (ud % hkv == 0; each
+ *            Ulysses rank holds the replica of KV head u' / (ud / hkv), as usp_a2a4d writes it)
  *   lse    : [rd][ud][hq/ud][bs][Lr] fp32, natural log of the row's softmax normaliser.
  * Row p of ring rank r is the token at global position zig(r, p); the causal mask compares global
  * positions. Scores are scale * <q, k>; inputs bf16 (tensor cores, fp32 accumulation, bf16 out) or
@@ -200,7 +213,8 @@ USP_API int usp_lse_merge(void *o_acc, float *lse_acc, const void *o_new, const 
  *   out              : (bs, L, hq, hd) natural order;  lse  : (bs, L, hq) fp32, natural log
  *   d                : as for usp_attn_fwd; d.mode must be USP_MODE_FUSED
  *   head_chunk       : query heads per group (0 = all); must divide hq and be a multiple of hq/hkv;
- *                      the group's query and KV head counts must divide by ud
+ *                      the group's query head count must divide by ud and its KV head count
+ *                      divide by ud or divide ud (replicated K/V)
  *   workspace        : DEVICE buffer, 256-byte aligned, at least usp_forward_workspace_size(d,
  *                      head_chunk, 0) bytes; owned by the caller, clobbered by the call
  * Asynchronous on `stream`; calls that share a workspace must be ordered on one stream.

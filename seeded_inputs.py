@@ -67,6 +67,9 @@ WORKLOADS = [
              sample_rows=256),
     Workload("gqa_causal_L262144_h32kv8_d128_bf16_u2r4_chunk8", 1, 262144, 32, 8, 128, "bf16", ud=2, rd=4,
              head_chunk=8, sample_rows=128),
+    # MQA with more Ulysses ranks than KV heads: the all-to-all replicates the KV head on 4 ranks
+    Workload("mqa_causal_L65536_h32kv1_d128_bf16_u4r2", 1, 65536, 32, 1, 128, "bf16", ud=4, rd=2,
+             sample_rows=256),
 ]
 
 

@@ -25,7 +25,7 @@ from ._abi import (USP_BF16, USP_F32, USP_MODE_ACCUM, USP_MODE_FUSED, USP_MODE_S
 
 __all__ = ["usp_extract_local", "usp_a2a4d", "usp_extract_a2a", "usp_attn_fwd", "usp_lse_merge", "usp_check", "usp_attention",
            "usp_attention_host", "usp_forward", "usp_forward_host", "usp_forward_workspace_size",
-           "usp_forward_noalloc",
+           "usp_forward_noalloc", "heads_per_rank",
            "UspAttention", "UspError", "USP_MODE_FUSED", "USP_MODE_STEP", "USP_MODE_ACCUM", "lib_path"]
 
 lib_path = _abi.LIB_PATH
@@ -101,10 +101,22 @@ def usp_extract_local(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, vr
     return dst
 
 
+def heads_per_rank(H: int, ud: int) -> int:
+    """Heads each Ulysses rank holds after the forward all-to-all: H // ud when ud divides H, 1 when
+    H divides ud (K/V replicated for GQA/MQA with fewer KV heads than Ulysses ranks), else 0."""
+    if H <= 0 or ud <= 0:
+        return 0
+    if H % ud == 0:
+        return H // ud
+    return 1 if ud % H == 0 else 0
+
+
 def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int = 1, h0: int = 0,
               H: Optional[int] = None, stream=None) -> torch.Tensor:
     """AllToAll4D inside every Ulysses group: dir=+1 sequence-sharded [rd][ud][bs][Lu][H_total][hd]
-    -> head-sharded [rd][ud][H/ud][bs][Lr][hd]; dir=-1 back. lse tensors drop the trailing hd axis."""
+    -> head-sharded [rd][ud][H/ud][bs][Lr][hd]; dir=-1 back. lse tensors drop the trailing hd axis.
+    dir=+1 with H < ud (ud % H == 0, K/V under GQA/MQA) replicates: head-sharded is
+    [rd][ud][1][bs][Lr][hd], rank u' holding head u' // (ud // H)."""
     _dev(src, dst)
     seq, hs = (src, dst) if dir > 0 else (dst, src)
     _need(seq.dtype == hs.dtype, "dtype mismatch")
@@ -117,9 +129,10 @@ def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int =
     _need(rd_ == rd and ud_ == ud, "grid mismatch")
     H = Ht - h0 if H is None else H
     _need(0 <= h0 and h0 + H <= Ht, "head window out of range")
-    _need(H % ud == 0, "heads must divide by ud")
+    Hl = heads_per_rank(H, ud) if dir > 0 else (H // ud if H % ud == 0 else 0)
+    _need(Hl > 0, "heads must divide by ud (or, forward only, divide ud)")
     L = Lu * ud * rd
-    _need(hs.numel() == rd * ud * (H // ud) * bs * ud * Lu * hd, "head-sharded tensor has the wrong size")
+    _need(hs.numel() == rd * ud * Hl * bs * ud * Lu * hd, "head-sharded tensor has the wrong size")
     d = UspDims(bs, L, H, hd, _dtype_code(seq), rd, ud, Ht, h0, 0)
     _abi.check("usp_a2a4d", _abi.load().usp_a2a4d(_ptr(src), _ptr(dst), d, 1 if dir > 0 else -1,
                                                  _stream(stream)))
@@ -130,8 +143,9 @@ def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=Non
                     stream=None):
     """Zigzag split then AllToAll4D in one pass (inverse: AllToAll4D's inverse then the inverse split),
     for up to four tensors in one launch. inverse=False: srcs[k] natural (bs, L, H_total, hd) (or
-    (bs, L, H_total) for lse) -> dsts[k] head-sharded [rd][ud][H/ud][bs][Lr](, hd); inverse=True the
-    other way round. Tensor k moves heads [h0s[k], h0s[k] + Hs[k]) of its natural tensor."""
+    (bs, L, H_total) for lse) -> dsts[k] head-sharded [rd][ud][H/ud][bs][Lr](, hd) ([rd][ud][1]... with
+    replicated heads when H < ud, as usp_a2a4d); inverse=True the other way round. Tensor k moves heads
+    [h0s[k], h0s[k] + Hs[k]) of its natural tensor."""
     srcs, dsts = list(srcs), list(dsts)
     n = len(srcs)
     _need(1 <= n <= 4 and len(dsts) == n, "one to four tensors")
@@ -151,8 +165,9 @@ def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=Non
             bs, L, Ht, hd = nat.shape
         H = Ht - h0s[k] if Hs[k] is None else Hs[k]
         _need(0 <= h0s[k] and h0s[k] + H <= Ht, "head window out of range")
-        _need(L % (2 * rd) == 0 and (L // rd) % ud == 0 and H % ud == 0, "shape not divisible")
-        _need(hs.numel() == bs * L * H * hd, "head-sharded tensor has the wrong size")
+        Hl = (H // ud if H % ud == 0 else 0) if inverse else heads_per_rank(H, ud)
+        _need(L % (2 * rd) == 0 and (L // rd) % ud == 0 and Hl > 0, "shape not divisible")
+        _need(hs.numel() == bs * L * Hl * ud * hd, "head-sharded tensor has the wrong size")
         dims.append(UspDims(bs, L, H, hd, _dtype_code(nat), rd, ud, Ht, h0s[k], _split_code(split)))
         sp.append(_ptr(src))
         dp.append(_ptr(dst))
@@ -164,9 +179,11 @@ def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=Non
 
 def usp_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
                  causal: bool = True, scale: Optional[float] = None, mode: int = USP_MODE_FUSED, step: int = 0,
-                 split="zigzag", ring_rank: Optional[int] = None, stream=None):
+                 split="zigzag", ring_rank: Optional[int] = None, hkv: Optional[int] = None, stream=None):
     """Ring attention over all virtual ring ranks (or only ring rank ``ring_rank``'s query rows).
-    q/out [rd][ud][hq/ud][bs][Lr][hd], k/v [rd][ud][hkv/ud][bs][Lr][hd], lse [rd][ud][hq/ud][bs][Lr] fp32."""
+    q/out [rd][ud][hq/ud][bs][Lr][hd], k/v [rd][ud][hkv/ud][bs][Lr][hd], lse [rd][ud][hq/ud][bs][Lr] fp32.
+    Replicated K/V (hkv < ud): k/v [rd][ud][1][bs][Lr][hd] and ``hkv`` gives the global KV head count
+    (default: k's heads per rank times ud)."""
     _dev(q, k, v, out, lse)
     _need(q.dim() == 6 and k.dim() == 6 and v.dim() == 6, "q, k, v must be [rd][ud][H/ud][bs][Lr][hd]")
     rd, ud, Hl, bs, Lr, hd = q.shape
@@ -176,7 +193,9 @@ def usp_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.T
     _need(lse.shape == (rd, ud, Hl, bs, Lr) and lse.dtype == torch.float32, "lse must be fp32 [rd][ud][Hl][bs][Lr]")
     _need(k.dtype == q.dtype and v.dtype == q.dtype, "dtype mismatch")
     L = Lr * rd
-    d = UspAttnDesc(bs, L, Hl * ud, Hkl * ud, hd, rd, ud, _dtype_code(q), int(bool(causal)),
+    hkv = Hkl * ud if hkv is None else int(hkv)
+    _need(hkv > 0 and heads_per_rank(hkv, ud) == Hkl, "k/v heads per rank do not match hkv and ud")
+    d = UspAttnDesc(bs, L, Hl * ud, hkv, hd, rd, ud, _dtype_code(q), int(bool(causal)),
                     float(scale) if scale is not None else 0.0, int(mode), int(step), _split_code(split),
                     0 if ring_rank is None else int(ring_rank) + 1)
     _abi.check("usp_attn_fwd", _abi.load().usp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d,
@@ -223,7 +242,8 @@ def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd
     hc = hq if head_chunk is None else head_chunk
     _need(hq % hc == 0 and hc % G == 0, "head_chunk must divide hq and be a multiple of hq/hkv")
     hkc = hc // G
-    _need(hc % ud == 0 and hkc % ud == 0, "head groups must divide by ud")
+    Hkl = heads_per_rank(hkc, ud)
+    _need(hc % ud == 0 and Hkl > 0, "query head groups must divide by ud, KV groups divide or be divided by ud")
     _need(L % (2 * rd) == 0 and (L // rd) % ud == 0, "L must split into 2*rd chunks and L/rd into ud parts")
     Lu, Lr = L // (rd * ud), L // rd
     dev, dt = q.device, q.dtype
@@ -237,7 +257,7 @@ def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd
     lse = torch.empty(rd, ud, bs, Lu, hq, device=dev, dtype=torch.float32)
     # per-group workspace, reused across groups
     qh = torch.empty(rd, ud, hc // ud, bs, Lr, hd, device=dev, dtype=dt)
-    kh = torch.empty(rd, ud, hkc // ud, bs, Lr, hd, device=dev, dtype=dt)
+    kh = torch.empty(rd, ud, Hkl, bs, Lr, hd, device=dev, dtype=dt)
     vh = torch.empty_like(kh)
     oh = torch.empty_like(qh)
     lh = torch.empty(rd, ud, hc // ud, bs, Lr, device=dev, dtype=torch.float32)
@@ -247,7 +267,7 @@ def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd
         usp_extract_a2a([q, k, v], [qh, kh, vh], rd, ud, h0s=[g0, gk, gk], Hs=[hc, hkc, hkc], split=split,
                         stream=stream)
         # a3 + a4: the ring with the fused LSE merge
-        usp_attn_fwd(qh, kh, vh, oh, lh, causal=causal, scale=scale, split=split, stream=stream)
+        usp_attn_fwd(qh, kh, vh, oh, lh, causal=causal, scale=scale, split=split, hkv=hkc, stream=stream)
         # a5 on out and lse: back to the sequence-sharded layout a model keeps
         usp_a2a4d(oh, out, rd, ud, -1, h0=g0, H=hc, stream=stream)
         usp_a2a4d(lh, lse, rd, ud, -1, h0=g0, H=hc, stream=stream)

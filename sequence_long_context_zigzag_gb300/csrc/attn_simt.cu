@@ -156,7 +156,7 @@ int launch_attn_simt(const AttnArgs &a, cudaStream_t s) {
     k.Lr = (uint32_t)(a.L / a.rd);
     k.c = (uint32_t)(a.L / (2 * a.rd));
     k.Hl = (uint32_t)(a.hq / a.ud);
-    k.Hkl = (uint32_t)(a.hkv / a.ud);
+    k.Hkl = (uint32_t)heads_per_rank(a.hkv, a.ud);
     k.G = (uint32_t)(a.hq / a.hkv);
     k.causal = a.causal;
     k.mode = a.mode;

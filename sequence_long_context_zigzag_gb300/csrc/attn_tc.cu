@@ -709,7 +709,8 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     if (!di) return USP_ERR_CUDA;
     TcParams p{};
     const uint64_t q_rows = (uint64_t)a.hq * a.bs * a.L;
-    const uint64_t kv_rows = (uint64_t)a.hkv * a.bs * a.L;
+    // K/V rows in the head-sharded layout [rd][ud][Hkl][bs][Lr]: Hkl * ud heads of bs * L tokens
+    const uint64_t kv_rows = (uint64_t)heads_per_rank(a.hkv, a.ud) * a.ud * a.bs * a.L;
     if (!make_tmap(&p.tq, a.q, q_rows, a.hd) || !make_tmap(&p.tk, a.k, kv_rows, a.hd) ||
         !make_tmap(&p.tv, a.v, kv_rows, a.hd))
         return USP_ERR_CUDA;
@@ -722,7 +723,7 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     p.Lr = (uint32_t)(a.L / a.rd);
     p.c = (uint32_t)(a.L / (2 * a.rd));
     p.Hl = (uint32_t)(a.hq / a.ud);
-    p.Hkl = (uint32_t)(a.hkv / a.ud);
+    p.Hkl = (uint32_t)heads_per_rank(a.hkv, a.ud);
     p.G = (uint32_t)(a.hq / a.hkv);
     p.npairs = (p.Lr + 255) / 256;
     p.causal = a.causal;

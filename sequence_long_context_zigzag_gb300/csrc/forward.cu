@@ -19,7 +19,8 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct FwdShape {
     int64_t bs, L;
     int hq, hkv, hd, rd, ud, hc, hkc, G, es, split;
-    size_t q_grp, kv_grp, lse_grp;  // bytes of one group's q / k (or v) / lse, any layout
+    size_t q_grp, kv_grp, lse_grp;  // bytes of one group's q / k (or v) / lse, natural order
+    size_t kv_hs;                   // bytes of one group's k (or v) head-sharded (more when replicated)
 };
 
 int fwd_shape(const usp_attn_desc &d, int head_chunk, FwdShape &s) {
@@ -34,17 +35,18 @@ int fwd_shape(const usp_attn_desc &d, int head_chunk, FwdShape &s) {
     s.hc = head_chunk > 0 ? head_chunk : d.hq;
     if (s.hc > d.hq || d.hq % s.hc != 0 || s.hc % s.G != 0) return USP_ERR_SHAPE;
     s.hkc = s.hc / s.G;
-    if (s.hc % d.ud != 0 || s.hkc % d.ud != 0) return USP_ERR_SHAPE;
+    if (s.hc % d.ud != 0 || heads_per_rank(s.hkc, d.ud) == 0) return USP_ERR_SHAPE;
     const size_t tok = (size_t)d.bs * (size_t)d.L;
     s.q_grp = tok * s.hc * d.hd * s.es;
     s.kv_grp = tok * s.hkc * d.hd * s.es;
+    s.kv_hs = tok * (size_t)heads_per_rank(s.hkc, d.ud) * d.ud * d.hd * s.es;
     s.lse_grp = tok * s.hc * 4;
     return USP_OK;
 }
 
 // workspace of the device-buffer forward: head-sharded q, k, v, out, lse of one group
 size_t ws_device(const FwdShape &s) {
-    return align_up(s.q_grp) * 2 + align_up(s.kv_grp) * 2 + align_up(s.lse_grp);
+    return align_up(s.q_grp) * 2 + align_up(s.kv_hs) * 2 + align_up(s.lse_grp);
 }
 
 // the host-buffer forward adds two slots of compact natural-order staging for q, k, v and out, and
@@ -129,7 +131,7 @@ int usp_forward(const void *q, const void *k, const void *v, void *out, float *l
     if (workspace_bytes < ws_device(s)) return USP_ERR_INVALID_ARG;
     if (!aligned(workspace, kAlign)) return USP_ERR_ALIGN;
     Carve cv{static_cast<char *>(workspace), workspace_bytes};
-    void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_grp), *vh = cv.take(s.kv_grp), *oh = cv.take(s.q_grp);
+    void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *oh = cv.take(s.q_grp);
     float *lh = static_cast<float *>(cv.take(s.lse_grp));
     for (int g0 = 0; g0 < s.hq; g0 += s.hc) {
         const int gk = g0 / s.G;
@@ -171,7 +173,7 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
     cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
 
     Carve cv{static_cast<char *>(workspace), workspace_bytes};
-    void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_grp), *vh = cv.take(s.kv_grp), *oh = cv.take(s.q_grp);
+    void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *oh = cv.take(s.q_grp);
     float *lh = static_cast<float *>(cv.take(s.lse_grp));
     void *in_q[2], *in_k[2], *in_v[2], *out_o[2];
     for (int sl = 0; sl < 2; ++sl) {

@@ -8,7 +8,9 @@
 // the all-to-all concatenates the Ulysses ranks' pieces in rank order, which is exactly the
 // ring-local sequence Algorithm 2 chunked. The composed pass reads and writes each tensor once. The
 // zigzag split is the default; the plain ring's contiguous split and the round-robin stripe split
-// use the same kernel with another position map.
+// use the same kernel with another position map. A forward all-to-all of fewer heads than Ulysses
+// ranks (K/V of GQA/MQA, hkv < ud) replicates: rank u' receives head u' / (ud / H), the one its query
+// heads read (the USP review's section 三 lists K/V head counts unlike Q's among AllToAll4D's duties).
 //
 // Work split: one warp owns a batch of 32 logical rows. Lane l computes the source and destination
 // row of row l of the batch (integer index math with multiply-high division), publishes them in
@@ -26,7 +28,7 @@ struct PermJobK {
     char *dst;
     uint32_t nrows, batch0;  // logical rows; first warp batch of this tensor
     uint32_t H, Ht, h0, Hl;
-    FastDiv f_H, f_Hl;
+    FastDiv f_H, f_Hl, f_rep;  // f_rep: ranks sharing one head (1 unless H < ud in a forward a2a)
 };
 
 struct PermK {
@@ -66,7 +68,7 @@ __device__ __forceinline__ void map_row(const PermK &p, const PermJobK &jb, uint
         p.f_bs.divmod(q, q, b);
         jb.f_Hl.divmod(q, q, hl);
         p.f_ud.divmod(q, r, up);
-        const int64_t head = (int64_t)jb.h0 + (int64_t)up * jb.Hl + hl;
+        const int64_t head = (int64_t)jb.h0 + (int64_t)jb.f_rep.div(up) * jb.Hl + hl;
         if (p.mode == PERM_A2A_FWD) {
             uint32_t u, j;
             p.f_Lu.divmod(pp, u, j);
@@ -166,6 +168,7 @@ int launch_permute(const PermArgs &a, cudaStream_t s) {
     p.vpr = (uint32_t)(a.row_bytes / (vec16 ? 16 : 4));
     if ((int64_t)32 * p.vpr >= (int64_t(1) << 31)) return USP_ERR_UNSUPPORTED;
     const int64_t ranks = (a.r_fixed >= 0) ? 1 : (int64_t)a.rd * a.ud;
+    const bool to_heads = a.mode == PERM_A2A_FWD || a.mode == PERM_FUSED_FWD;
     int64_t nbatch = 0;
     for (int k = 0; k < a.njobs; ++k) {
         const PermJob &j = a.job[k];
@@ -175,10 +178,15 @@ int launch_permute(const PermArgs &a, cudaStream_t s) {
         jk.H = (uint32_t)j.H;
         jk.Ht = (uint32_t)j.H_total;
         jk.h0 = (uint32_t)j.h0;
-        jk.Hl = jk.H / p.ud;
+        // a forward all-to-all of fewer heads than Ulysses ranks replicates: one head per rank
+        const bool rep = to_heads && jk.H > 0 && jk.H < p.ud;
+        jk.Hl = rep ? 1 : jk.H / p.ud;
         jk.f_H = FastDiv(jk.H ? jk.H : 1);
         jk.f_Hl = FastDiv(jk.Hl ? jk.Hl : 1);
-        const int64_t nrows = ranks * a.bs * (int64_t)p.Lu * j.H;  // same count in every mode
+        jk.f_rep = FastDiv(rep ? p.ud / jk.H : 1);
+        // rows of the destination (= of the source, except when replicating)
+        const int64_t rows_per_tok = rep ? (int64_t)p.ud : (int64_t)j.H;
+        const int64_t nrows = ranks * a.bs * (int64_t)p.Lu * rows_per_tok;
         if (nrows >= (int64_t(1) << 31)) return USP_ERR_UNSUPPORTED;
         jk.nrows = (uint32_t)nrows;
         jk.batch0 = (uint32_t)nbatch;

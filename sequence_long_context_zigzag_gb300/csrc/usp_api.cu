@@ -33,7 +33,8 @@ const DeviceInfo *device_info() {
 
 static bool overflow31(int64_t x) { return x < 0 || x >= (int64_t(1) << 31); }
 
-// shared checks of a permute's dims; fills the derived sizes
+// shared checks of a permute's dims. need_head_split: 0 = none (split only), 1 = ud must divide H
+// (the inverse all-to-all), 2 = ud divides H or H divides ud (the forward all-to-all replicates)
 static int check_dims(const usp_dims &d, int need_head_split) {
     if (d.bs < 0 || d.L < 0 || d.H < 0 || d.hd <= 0 || d.rd <= 0 || d.ud <= 0 || d.h0 < 0 ||
         d.H_total < 0)
@@ -44,7 +45,8 @@ static int check_dims(const usp_dims &d, int need_head_split) {
     if ((d.L / d.rd) % d.ud != 0) return USP_ERR_SHAPE;
     int32_t Ht = d.H_total ? d.H_total : d.H;
     if ((int64_t)d.h0 + d.H > Ht) return USP_ERR_SHAPE;
-    if (need_head_split && d.H % d.ud != 0) return USP_ERR_SHAPE;
+    if (need_head_split == 1 && d.H % d.ud != 0) return USP_ERR_SHAPE;
+    if (need_head_split == 2 && d.H > 0 && heads_per_rank(d.H, d.ud) == 0) return USP_ERR_SHAPE;
     if (overflow31(d.bs * d.L * (int64_t)Ht) || overflow31(d.L) ||
         overflow31((int64_t)d.hd * elem_size(d.dtype)))
         return USP_ERR_UNSUPPORTED;
@@ -70,7 +72,7 @@ const char *usp_strerror(int status) {
     switch (status) {
         case USP_OK: return "success";
         case USP_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad enum)";
-        case USP_ERR_SHAPE: return "shape not divisible (L % 2rd, (L/rd) % ud, heads % ud, hq % hkv)";
+        case USP_ERR_SHAPE: return "shape not divisible (L % 2rd, (L/rd) % ud, hq % ud, hq % hkv, hkv vs ud)";
         case USP_ERR_DTYPE: return "unknown dtype code";
         case USP_ERR_ALIGN: return "pointer not aligned as required";
         case USP_ERR_UNSUPPORTED: return "unsupported configuration";
@@ -102,9 +104,9 @@ int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, int invers
 }
 
 int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stream) {
-    int rc = check_dims(d, 1);
-    if (rc) return rc;
     if (dir != 1 && dir != -1) return USP_ERR_INVALID_ARG;
+    int rc = check_dims(d, dir > 0 ? 2 : 1);
+    if (rc) return rc;
     if (d.bs == 0 || d.L == 0 || d.H == 0) return USP_OK;
     if (!src || !dst) return USP_ERR_INVALID_ARG;
     const int64_t row_bytes = (int64_t)d.hd * elem_size(d.dtype);
@@ -131,7 +133,7 @@ int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_d
     int64_t work = 0;
     for (int k = 0; k < n; ++k) {
         const usp_dims &dk = d[k];
-        int rc = check_dims(dk, 1);
+        int rc = check_dims(dk, inverse ? 1 : 2);
         if (rc) return rc;
         if (dk.bs != d[0].bs || dk.L != d[0].L || dk.rd != d[0].rd || dk.ud != d[0].ud || dk.hd != d[0].hd ||
             dk.dtype != d[0].dtype || dk.split != d[0].split)
@@ -164,7 +166,7 @@ int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *
     if (d.ring_rank_only < 0 || d.ring_rank_only > d.rd) return USP_ERR_INVALID_ARG;
     if (elem_size(d.dtype) == 0) return USP_ERR_DTYPE;
     if (d.L % (2 * (int64_t)d.rd) != 0 || (d.L / d.rd) % d.ud != 0) return USP_ERR_SHAPE;
-    if (d.hq % d.hkv != 0 || d.hq % d.ud != 0 || d.hkv % d.ud != 0) return USP_ERR_SHAPE;
+    if (d.hq % d.hkv != 0 || d.hq % d.ud != 0 || heads_per_rank(d.hkv, d.ud) == 0) return USP_ERR_SHAPE;
     if (d.hd != 64 && d.hd != 128) return USP_ERR_UNSUPPORTED;
     if (overflow31(d.bs * d.L * (int64_t)d.hq) || overflow31(d.L)) return USP_ERR_UNSUPPORTED;
     if (!(d.scale == d.scale) || isinf(d.scale)) return USP_ERR_INVALID_ARG;

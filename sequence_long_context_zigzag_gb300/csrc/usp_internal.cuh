@@ -80,6 +80,15 @@ inline int elem_size(int dtype) { return dtype == USP_F32 ? 4 : (dtype == USP_BF
 
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Heads per Ulysses rank after the forward all-to-all of a tensor with H heads: H / ud when ud
+// divides H; 1 when H divides ud (K/V of GQA/MQA with fewer heads than Ulysses ranks: every rank
+// receives a replica of the one head its query heads read, head u' / (ud / H)); 0 otherwise.
+inline int heads_per_rank(int64_t H, int64_t ud) {
+    if (H <= 0 || ud <= 0) return 0;
+    if (H % ud == 0) return (int)(H / ud);
+    return ud % H == 0 ? 1 : 0;
+}
+
 // kernel launchers implemented in separate translation units; return USP_* codes
 enum PermMode {
     PERM_EXTRACT = 0,      // natural -> local (a1)

@@ -50,7 +50,8 @@ BAD = 0x1001  # never dereferenced: every case below is rejected before a launch
 @pytest.mark.parametrize("d,code", [
     (dims(L=62), _abi.USP_ERR_SHAPE),            # L % (2 rd) != 0
     (dims(L=68, rd=2, ud=4), _abi.USP_ERR_SHAPE),  # (L/rd) % ud != 0
-    (dims(H=3), _abi.USP_ERR_SHAPE),             # heads % ud != 0 (a2a only)
+    (dims(H=3), _abi.USP_ERR_SHAPE),             # heads % ud != 0 and ud % heads != 0 (a2a only)
+    (dims(H=3, ud=4, L=64), _abi.USP_ERR_SHAPE),  # fewer heads than ranks but not a divisor of ud
     (dims(dtype=7), _abi.USP_ERR_DTYPE),
     (dims(rd=0), _abi.USP_ERR_INVALID_ARG),
     (dims(hd=0), _abi.USP_ERR_INVALID_ARG),
@@ -63,6 +64,9 @@ def test_a2a_rejects(d, code):
 
 def test_a2a_rejects_direction_and_alignment():
     lib = _abi.load()
+    # replication (H < ud, ud % H == 0) exists in the forward direction only
+    assert lib.usp_a2a4d(BAD, BAD, dims(H=1, ud=4), 1, None) == _abi.USP_ERR_ALIGN
+    assert lib.usp_a2a4d(BAD, BAD, dims(H=1, ud=4), -1, None) == _abi.USP_ERR_SHAPE
     assert lib.usp_a2a4d(BAD, BAD, dims(), 0, None) == _abi.USP_ERR_INVALID_ARG
     assert lib.usp_a2a4d(BAD, BAD, dims(), 1, None) == _abi.USP_ERR_ALIGN
     assert lib.usp_a2a4d(None, BAD, dims(), 1, None) == _abi.USP_ERR_INVALID_ARG
@@ -91,7 +95,8 @@ def desc(**kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(hd=96), _abi.USP_ERR_UNSUPPORTED),
     (dict(hq=6, hkv=4), _abi.USP_ERR_SHAPE),
-    (dict(hq=4, hkv=1, ud=2), _abi.USP_ERR_SHAPE),   # hkv % ud != 0 (MQA with ud > hkv)
+    (dict(hq=6, hkv=3, ud=2), _abi.USP_ERR_SHAPE),   # hkv neither divides by ud nor divides ud
+    (dict(hq=4, hkv=1, ud=2), _abi.USP_ERR_ALIGN),   # MQA with ud > hkv is accepted (replicated K/V)
     (dict(L=250), _abi.USP_ERR_SHAPE),
     (dict(mode=3), _abi.USP_ERR_INVALID_ARG),
     (dict(mode=1, step=2), _abi.USP_ERR_INVALID_ARG),
@@ -152,7 +157,10 @@ def test_forward_workspace_and_rejects():
     assert n_dev == 2 * 2 ** 21 + 2 * 2 ** 19 + 2 ** 15
     assert n_host > n_dev
     assert lib.usp_forward_workspace_size(d, 3, 0) == 0            # 3 does not divide 8
-    assert lib.usp_forward_workspace_size(d, 4, 0) == 0            # 1 KV head per group, ud = 2
+    # 1 KV head per group with ud = 2: each Ulysses rank gets a replica, so head-sharded k and v
+    # hold 2 heads' worth (2 * 512 KiB) beside q and out (2 * 1 MiB) and lse (16 KiB)
+    assert lib.usp_forward_workspace_size(d, 4, 0) == 2 * 2 ** 20 + 2 * 2 ** 19 + 2 ** 14
+    assert lib.usp_forward_workspace_size(desc(L=1024, hq=6, hkv=3, ud=2), 0, 0) == 0  # 3 vs ud 2
     assert lib.usp_forward_workspace_size(desc(mode=1), 0, 0) == 0  # only the fused mode
     ws = BAD - 1  # 0x1000: 256-byte aligned, never dereferenced (rejected before any launch)
     assert lib.usp_forward(BAD, BAD, BAD, BAD, BAD, d, 8, ws, n_dev - 1, None) == _abi.USP_ERR_INVALID_ARG
