@@ -60,6 +60,12 @@ def _load():
     lib.oracle_attn_direct.restype = i32
     lib.oracle_attn_block.argtypes = [vp, vp, i64, vp, vp, vp, i64, i32, i32, i32, dbl, i32, vp, vp]
     lib.oracle_attn_block.restype = i32
+    lib.oracle_attn_bwd_direct.argtypes = [vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, dbl, i32, vp, i64, vp,
+                                           i64, vp, vp]
+    lib.oracle_attn_bwd_direct.restype = i32
+    lib.oracle_attn_block_bwd.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, vp, i64, i32, i32, i32, dbl, i32, vp,
+                                          vp, vp]
+    lib.oracle_attn_block_bwd.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     _lib = lib
@@ -148,6 +154,59 @@ def attn_block(q, qpos, k, v, kpos, scale, causal=True):
     if rc != 0:
         raise ValueError("oracle_attn_block: bad arguments")
     return o, lse
+
+
+def attn_direct_bwd(q, k, v, dout, scale=None, causal=True, q_rows=None, kv_from=0):
+    """Gradients of direct attention's output with respect to q, k, v for an upstream gradient dout
+    (the chain rule through softmax, written out in usp_oracle.c), natural token order, fp64.
+
+    q, dout: (bs, L, hq, hd), k/v: (bs, L, hkv, hd), one dtype (fp32, bf16 or fp64).
+    q_rows: query rows whose dq is returned (default all); kv_from: dk, dv are returned for key rows
+    [kv_from, L) (default all; L for none). Returns dq (bs, len(q_rows), hq, hd),
+    dk, dv (bs, L - kv_from, hkv, hd).
+    """
+    qa, dt = _raw(q)
+    ka, dk_ = _raw(k)
+    va, dv_ = _raw(v)
+    ga, dg = _raw(dout)
+    if not (dt == dk_ == dv_ == dg):
+        raise TypeError("q, k, v, dout must share a dtype")
+    bs, L, hq, hd = qa.shape
+    hkv = ka.shape[2]
+    if ga.shape != qa.shape:
+        raise ValueError("dout must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(hd)
+    rows = np.arange(L, dtype=np.int64) if q_rows is None else np.ascontiguousarray(q_rows, dtype=np.int64)
+    nkv = L - int(kv_from)
+    dq = np.zeros((bs, len(rows), hq, hd), dtype=np.float64)
+    dk = np.zeros((bs, nkv, hkv, hd), dtype=np.float64)
+    dv = np.zeros((bs, nkv, hkv, hd), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_direct(_p(qa), _p(ka), _p(va), _p(ga), dt, bs, L, hq, hkv, hd, float(scale),
+                                        int(bool(causal)), _p(rows), len(rows), _p(dq), int(kv_from), _p(dk),
+                                        _p(dv))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_direct: bad arguments")
+    return dq, dk, dv
+
+
+def attn_block_bwd(q, dout, qpos, lse, D, k, v, kpos, scale, causal, dq_acc, dk_acc, dv_acc):
+    """One ring step's share of the backward, accumulated in place: dq_acc (hq, nq, hd) += the keys'
+    contribution, dk_acc / dv_acc (hkv, nk, hd) += the queries' contribution, using the rows' final
+    lse and D = <dout, out> (all fp64, head-sharded block layout as attn_block)."""
+    arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (q, dout, lse, D, k, v)]
+    q, dout, lse, D, k, v = arrs
+    qpos = np.ascontiguousarray(qpos, dtype=np.int64)
+    kpos = np.ascontiguousarray(kpos, dtype=np.int64)
+    for a in (dq_acc, dk_acc, dv_acc):
+        assert a.dtype == np.float64 and a.flags.c_contiguous
+    hq, nq, hd = q.shape
+    hkv, nk, _ = k.shape
+    rc = _load().oracle_attn_block_bwd(_p(q), _p(dout), _p(qpos), _p(lse), _p(D), nq, _p(k), _p(v), _p(kpos), nk,
+                                       hq, hkv, hd, float(scale), int(bool(causal)), _p(dq_acc), _p(dk_acc),
+                                       _p(dv_acc))
+    if rc != 0:
+        raise ValueError("oracle_attn_block_bwd: bad arguments")
 
 
 # ----------------------------------------------------------------------------------------------
@@ -315,6 +374,24 @@ def a2a_inv(hs, ud):
     return hs[R, Hh // Hl, Hh % Hl, B, U * Lu + J]
 
 
+def a2a_inv_sum(hs, ud, H):
+    """The adjoint of a2a_fwd for a tensor of H heads: a5 when ud divides H; when H < ud (replicated
+    heads) every head's gradient is the sum of its ud/H replicas:
+    out[r,u,b,j,h] = sum over u' with u' // (ud/H) == h of hs[r,u',0,b,u*Lu+j]."""
+    hs = np.asarray(hs)
+    if H % ud == 0:
+        return a2a_inv(hs, ud)
+    assert ud % H == 0 and hs.shape[2] == 1
+    rd, _, _, bs, Lr = hs.shape[:5]
+    Lu, rep = Lr // ud, ud // H
+    out = np.zeros((rd, ud, bs, Lu, H) + hs.shape[5:], dtype=hs.dtype)
+    for h in range(H):
+        for up in range(h * rep, (h + 1) * rep):
+            for u in range(ud):
+                out[:, u, :, :, h] += hs[:, up, 0, :, u * Lu:(u + 1) * Lu]
+    return out
+
+
 # ----------------------------------------------------------------------------------------------
 # the ring schedule and the literal virtual-rank pipeline
 # ----------------------------------------------------------------------------------------------
@@ -366,6 +443,50 @@ def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True, split="zigzag"):
     out = extract_inverse(a2a_inv(O, ud), L, rd, ud, split=split)
     lse = extract_inverse(a2a_inv(LSE[..., None], ud), L, rd, ud, split=split)[..., 0]
     return out, lse
+
+
+def literal_pipeline_bwd(q, k, v, dout, rd, ud, scale=None, causal=True, split="zigzag"):
+    """USP-Attention backward, run rank by rank over the virtual ud x rd grid, in fp64.
+
+    The forward's layout changes are applied to q, k, v, the upstream gradient dout, and the
+    forward's out and lse (Algorithm 2 split, AllToAll4D). For every ring rank r, the ring runs in
+    Fig. 1 order (step t: KV block of rank (r - t) mod rd): each step adds the block's share of dq
+    to rank r and of dk, dv to the block's owner -- in a multi-GPU ring those two partials travel
+    with the KV block and are home after rd steps. The inverse all-to-all (the replica sum for
+    replicated K/V) and the inverse split return dq, dk, dv in natural order.
+    """
+    q, k, v, dout = (np.asarray(_to_f64(x)) for x in (q, k, v, dout))
+    bs, L, hq, hd = q.shape
+    hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(hd)
+    c, Lr, _ = _dims(L, rd, ud)
+    if hq % ud or hq % hkv or (hkv % ud and ud % hkv):
+        raise ValueError("hq must divide by ud and by hkv; hkv must divide by ud or divide ud")
+    o_nat, l_nat = attn_direct(q, k, v, scale=scale, causal=causal)
+    D_nat = np.einsum("blhd,blhd->blh", dout, o_nat)
+    hs = lambda x: a2a_fwd(extract_local(x, rd, ud, split=split), ud)  # noqa: E731
+    Q, K, V, dO = hs(q), hs(k), hs(v), hs(dout)
+    LSE, DD = hs(l_nat[..., None])[..., 0], hs(D_nat[..., None])[..., 0]
+    pos = [split_pos(split, r, np.arange(Lr), L, rd) for r in range(rd)]
+    dQ, dK, dV = np.zeros(Q.shape), np.zeros(K.shape), np.zeros(V.shape)
+    for r in range(rd):
+        for u in range(ud):
+            for b in range(bs):
+                dq_r = np.zeros(Q[r, u, :, b].shape)
+                for t in range(rd):
+                    s = ring_source(r, t, rd)
+                    dk_s = np.zeros(K[s, u, :, b].shape)
+                    dv_s = np.zeros(V[s, u, :, b].shape)
+                    attn_block_bwd(Q[r, u, :, b], dO[r, u, :, b], pos[r], LSE[r, u, :, b], DD[r, u, :, b],
+                                   K[s, u, :, b], V[s, u, :, b], pos[s], scale, causal, dq_r, dk_s, dv_s)
+                    dK[s, u, :, b] += dk_s
+                    dV[s, u, :, b] += dv_s
+                dQ[r, u, :, b] = dq_r
+    dq = extract_inverse(a2a_inv(dQ, ud), L, rd, ud, split=split)
+    dk = extract_inverse(a2a_inv_sum(dK, ud, hkv), L, rd, ud, split=split)
+    dv = extract_inverse(a2a_inv_sum(dV, ud, hkv), L, rd, ud, split=split)
+    return dq, dk, dv
 
 
 def _to_f64(x):
