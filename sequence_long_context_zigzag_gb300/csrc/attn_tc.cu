@@ -44,10 +44,15 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;     // issues Q tile 0's MMAs; allocates and frees tensor memory
 constexpr int kMmaWarp1 = 10;   // issues Q tile 1's MMAs
 // Register split per warpgroup (setmaxnreg). The launch grants 384 threads x 168 registers = 64512;
-// the softmax warpgroups take 2 x 128 x 208 = 53248 and the control warpgroup keeps 128 x 88 = 11264:
-// 64512 in total, so the increase can always be granted.
-constexpr int kSoftmaxRegs = 208;
-constexpr int kControlRegs = 88;
+// the softmax warpgroups take 2 x 128 x kSoftmaxRegs and the control warpgroup keeps
+// 128 x kControlRegs: 64512 in total, so the increase can always be granted.
+#ifndef USP_SOFTMAX_REGS
+#define USP_SOFTMAX_REGS 208
+#endif
+constexpr int kSoftmaxRegs = USP_SOFTMAX_REGS;
+constexpr int kControlRegs = 504 - 2 * kSoftmaxRegs;
+static_assert(kSoftmaxRegs % 8 == 0 && kControlRegs >= 24 && 2 * kSoftmaxRegs + kControlRegs == 504,
+              "register split must use exactly the launch's 168 registers per thread");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8

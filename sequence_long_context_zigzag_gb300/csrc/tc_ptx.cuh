@@ -55,20 +55,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed, at most `limit_ns` nanoseconds.
-// Returns false on expiry after recording `code` in the status word, and also gives up at once when
-// another thread has already recorded a failure there.
+// Returns false on expiry after recording `code` in the status word, and also gives up when another
+// thread has already recorded a failure there. The timer and the status word (a global-memory read)
+// are checked only every kPollsPerCheck polls, so that a wait that ends soon reacts at the latency
+// of the barrier itself; each poll suspends in hardware until the phase completes or a short time
+// limit passes, so the bound still holds to within a few microseconds.
+constexpr uint32_t kPollsPerCheck = 32;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status, int code,
                                           uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*reinterpret_cast<volatile int *>(status) != 0) return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
-            atomicExch(status, code);
-            return false;
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (n % kPollsPerCheck == 0) {
+            if (*reinterpret_cast<volatile int *>(status) != 0) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                atomicExch(status, code);
+                return false;
+            }
         }
     }
-    return true;
 }
 
 // ---------------------------------------------------------------------------------------------
