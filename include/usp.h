@@ -118,7 +118,9 @@ USP_API int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, in
  * dir == +1: sequence-sharded -> head-sharded.  dir == -1: head-sharded -> sequence-sharded.
  * dir == +1 with H < ud and ud % H == 0 replicates (K/V under GQA/MQA): head-sharded is
  *   [rd][ud][1][bs][Lr][hd] and head-sharded[r][u'][0][b][u Lu + j] =
- *   sequence-sharded[r][u][b][j][h0 + u' / (ud / H)]. dir == -1 needs H % ud == 0.
+ *   sequence-sharded[r][u][b][j][h0 + u' / (ud / H)]. dir == -1 with H < ud is the adjoint of that:
+ *   each head receives the SUM of its ud / H replicas (fp32 sum, rounded once), which is what the
+ *   gradients of replicated K/V need.
  * Alignment and overlap rules as for usp_extract_local. An lse tensor is moved with hd = 1, USP_F32.
  */
 USP_API int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stream);
@@ -137,8 +139,9 @@ USP_API int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_strea
  *   src, dst  : HOST arrays of n DEVICE pointers. inverse == 0: src[k] natural (bs, L, H_total, hd),
  *               dst[k] head-sharded [rd][ud][H/ud][bs][Lr][hd] (or, when H < ud and ud % H == 0,
  *               [rd][ud][1][bs][Lr][hd] holding head u' / (ud / H) on rank u', as usp_a2a4d);
- *               inverse != 0: the other way round, H % ud == 0 (heads outside the window of the
- *               natural tensor are left untouched).
+ *               inverse != 0: the other way round (with H < ud, the sum of each head's replicas,
+ *               as usp_a2a4d dir = -1); heads outside the window of the natural tensor are left
+ *               untouched.
  *   d         : HOST array of n dims; bs, L, rd, ud, hd and dtype must agree (USP_ERR_SHAPE
  *               otherwise); H, H_total and h0 may differ (Q and K/V head counts under GQA).
  * Alignment and overlap rules as for usp_extract_local.
@@ -264,6 +267,61 @@ USP_API size_t usp_forward_workspace_size(usp_attn_desc d, int head_chunk, int h
  */
 USP_API int usp_forward_noalloc(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d,
                                 int head_chunk, usp_stream_t stream);
+
+/*
+ * usp_attn_bwd_delta -- D_i = <dout_i, out_i> for every row (the softmax backward's row term).
+ * Source: the gradient of softmax attention (UPipe page, attention formula; the backward needs the
+ * forward's inputs and output): with P = softmax(S), dS = P o (dP - D) and D_i = sum_j P_ij dP_ij,
+ * which equals <dout_i, out_i> because out_i = sum_j P_ij v_j and dP_ij = <dout_i, v_j>.
+ *   out, dout : rows x hd of `dtype`, row-major, any layout whose rows are contiguous (natural or
+ *               head-sharded);  delta : rows fp32 (same row order). fp32 accumulation.
+ * Pointers 16-byte aligned; hd * elem_size a multiple of 16.
+ */
+USP_API int usp_attn_bwd_delta(const void *out, const void *dout, float *delta, int64_t rows, int32_t hd,
+                               int32_t dtype, usp_stream_t stream);
+
+/*
+ * usp_attn_bwd -- backward of usp_attn_fwd (the whole ring, USP_MODE_FUSED) over all virtual ring
+ * ranks: the gradients of out with respect to q, k and v.
+ * Source: the YunChang page runs its hybrid zigzag test with the backward (--use_bwd); the
+ * Context-Parallel page pairs the forward's gather of K/V with a reduce-scatter of their gradients
+ * in the backward; the formulas are the chain rule through softmax (usp_attn_bwd_delta):
+ *   P_ij = exp(s_ij - lse_i), dP_ij = <dout_i, v_j>, dS_ij = P_ij (dP_ij - D_i),
+ *   dq_i = scale sum_j dS_ij k_j, dk_j = scale sum_i dS_ij q_i, dv_j = sum_i P_ij dout_i,
+ * over the same causal (query, key) pairs as the forward. In a multi-GPU ring, the dk/dv partials of
+ * a KV block travel with it and are home after rd steps; here each KV block's gradient is formed in
+ * place.
+ *   q, dout, dq : [rd][ud][hq/ud][bs][Lr][hd]   (head-sharded)
+ *   k, v, dk, dv: [rd][ud][Hkl][bs][Lr][hd]     (Hkl as for usp_attn_fwd; with replicated K/V each
+ *                 replica receives the gradient from its own rank's query heads only, and the
+ *                 replica sum happens in the inverse all-to-all, usp_a2a4d dir = -1)
+ *   lse, delta  : [rd][ud][hq/ud][bs][Lr] fp32: the forward's lse and usp_attn_bwd_delta's output
+ * d as for usp_attn_fwd with d.mode == USP_MODE_FUSED and d.ring_rank_only == 0. All pointers
+ * 16-byte aligned; outputs must not overlap inputs. Arithmetic in fp32; gradients written in the
+ * input dtype.
+ */
+USP_API int usp_attn_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse,
+                         const float *delta, void *dq, void *dk, void *dv, usp_attn_desc d, usp_stream_t stream);
+
+/*
+ * usp_backward -- the whole USP-Attention backward on device buffers, the counterpart of
+ * usp_forward: D from out and dout, then for every head group the split and AllToAll4D of q, k, v,
+ * dout, lse and D, the ring backward (usp_attn_bwd), and the inverse AllToAll4D (summing replicas of
+ * replicated K/V) and inverse split of dq, dk, dv back to natural order.
+ * Source: as usp_forward and usp_attn_bwd; the UPipe page's headwise chunks each take their own
+ * gradients, so the grouping does not change the result.
+ *   q, out, dout, dq : (bs, L, hq, hd) natural order;  k, v, dk, dv : (bs, L, hkv, hd)
+ *   lse              : (bs, L, hq) fp32, the forward's
+ *   d, head_chunk    : as for usp_forward
+ *   workspace        : DEVICE buffer, 256-byte aligned, at least usp_backward_workspace_size(d,
+ *                      head_chunk) bytes; owned by the caller, clobbered by the call
+ */
+USP_API int usp_backward(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                         const void *dout, void *dq, void *dk, void *dv, usp_attn_desc d, int head_chunk,
+                         void *workspace, size_t workspace_bytes, usp_stream_t stream);
+
+/* Bytes of workspace usp_backward needs; 0 if the arguments are invalid. */
+USP_API size_t usp_backward_workspace_size(usp_attn_desc d, int head_chunk);
 
 /* Synchronise `stream`, then report (and clear) the device status word of the current device:
  * USP_OK, USP_ERR_TIMEOUT, or USP_ERR_CUDA if the synchronisation itself failed. */

@@ -26,6 +26,7 @@ from ._abi import (USP_BF16, USP_F32, USP_MODE_ACCUM, USP_MODE_FUSED, USP_MODE_S
 __all__ = ["usp_extract_local", "usp_a2a4d", "usp_extract_a2a", "usp_attn_fwd", "usp_lse_merge", "usp_check", "usp_attention",
            "usp_attention_host", "usp_forward", "usp_forward_host", "usp_forward_workspace_size",
            "usp_forward_noalloc", "heads_per_rank",
+           "usp_attn_bwd_delta", "usp_attn_bwd", "usp_backward", "usp_backward_workspace_size", "UspAttentionFunction",
            "UspAttention", "UspError", "USP_MODE_FUSED", "USP_MODE_STEP", "USP_MODE_ACCUM", "lib_path"]
 
 lib_path = _abi.LIB_PATH
@@ -116,7 +117,8 @@ def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int =
     """AllToAll4D inside every Ulysses group: dir=+1 sequence-sharded [rd][ud][bs][Lu][H_total][hd]
     -> head-sharded [rd][ud][H/ud][bs][Lr][hd]; dir=-1 back. lse tensors drop the trailing hd axis.
     dir=+1 with H < ud (ud % H == 0, K/V under GQA/MQA) replicates: head-sharded is
-    [rd][ud][1][bs][Lr][hd], rank u' holding head u' // (ud // H)."""
+    [rd][ud][1][bs][Lr][hd], rank u' holding head u' // (ud // H); dir=-1 then sums each head's
+    replicas (the adjoint, for gradients)."""
     _dev(src, dst)
     seq, hs = (src, dst) if dir > 0 else (dst, src)
     _need(seq.dtype == hs.dtype, "dtype mismatch")
@@ -129,8 +131,8 @@ def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int =
     _need(rd_ == rd and ud_ == ud, "grid mismatch")
     H = Ht - h0 if H is None else H
     _need(0 <= h0 and h0 + H <= Ht, "head window out of range")
-    Hl = heads_per_rank(H, ud) if dir > 0 else (H // ud if H % ud == 0 else 0)
-    _need(Hl > 0, "heads must divide by ud (or, forward only, divide ud)")
+    Hl = heads_per_rank(H, ud)
+    _need(Hl > 0, "heads must divide by ud or divide ud")
     L = Lu * ud * rd
     _need(hs.numel() == rd * ud * Hl * bs * ud * Lu * hd, "head-sharded tensor has the wrong size")
     d = UspDims(bs, L, H, hd, _dtype_code(seq), rd, ud, Ht, h0, 0)
@@ -165,7 +167,7 @@ def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=Non
             bs, L, Ht, hd = nat.shape
         H = Ht - h0s[k] if Hs[k] is None else Hs[k]
         _need(0 <= h0s[k] and h0s[k] + H <= Ht, "head window out of range")
-        Hl = (H // ud if H % ud == 0 else 0) if inverse else heads_per_rank(H, ud)
+        Hl = heads_per_rank(H, ud)
         _need(L % (2 * rd) == 0 and (L // rd) % ud == 0 and Hl > 0, "shape not divisible")
         _need(hs.numel() == bs * L * Hl * ud * hd, "head-sharded tensor has the wrong size")
         dims.append(UspDims(bs, L, H, hd, _dtype_code(nat), rd, ud, Ht, h0s[k], _split_code(split)))
@@ -360,6 +362,97 @@ def usp_attention_host(q, k, v, ud: int, rd: int, causal: bool = True, scale: Op
     usp_forward_host(q, k, v, out, lse, ud, rd, causal=causal, scale=scale, head_chunk=head_chunk, device=device)
     torch.cuda.current_stream(device).synchronize()
     return out, lse
+
+
+def usp_attn_bwd_delta(out: torch.Tensor, dout: torch.Tensor, delta: torch.Tensor, stream=None) -> torch.Tensor:
+    """delta[row] = <dout[row], out[row]> (fp32) for every row of hd elements (any row-contiguous layout)."""
+    _dev(out, dout, delta)
+    _need(out.shape == dout.shape and out.dtype == dout.dtype, "out / dout differ")
+    hd = out.shape[-1]
+    rows = out.numel() // hd
+    _need(delta.numel() == rows and delta.dtype == torch.float32, "delta must hold one fp32 value per row")
+    _abi.check("usp_attn_bwd_delta", _abi.load().usp_attn_bwd_delta(_ptr(out), _ptr(dout), _ptr(delta), rows, hd,
+                                                                   _dtype_code(out), _stream(stream)))
+    return delta
+
+
+def usp_attn_bwd(q, k, v, dout, lse, delta, dq, dk, dv, causal: bool = True, scale: Optional[float] = None,
+                 split="zigzag", hkv: Optional[int] = None, stream=None):
+    """Backward of usp_attn_fwd (whole ring) on head-sharded buffers: q/dout/dq [rd][ud][hq/ud][bs][Lr][hd],
+    k/v/dk/dv [rd][ud][Hkl][bs][Lr][hd], lse/delta [rd][ud][hq/ud][bs][Lr] fp32 (delta from
+    usp_attn_bwd_delta). Replicated K/V (hkv < ud): each replica gets its own rank's share."""
+    _dev(q, k, v, dout, lse, delta, dq, dk, dv)
+    _need(q.dim() == 6 and k.dim() == 6, "q, k must be [rd][ud][H/ud][bs][Lr][hd]")
+    rd, ud, Hl, bs, Lr, hd = q.shape
+    Hkl = k.shape[2]
+    _need(k.shape == (rd, ud, Hkl, bs, Lr, hd) and v.shape == k.shape, "k/v shape mismatch")
+    _need(dout.shape == q.shape and dq.shape == q.shape and dk.shape == k.shape and dv.shape == k.shape,
+          "gradient shapes must match their inputs")
+    for t in (k, v, dout, dq, dk, dv):
+        _need(t.dtype == q.dtype, "dtype mismatch")
+    for t in (lse, delta):
+        _need(t.shape == (rd, ud, Hl, bs, Lr) and t.dtype == torch.float32, "lse/delta must be fp32 [rd][ud][Hl][bs][Lr]")
+    hkv = Hkl * ud if hkv is None else int(hkv)
+    _need(hkv > 0 and heads_per_rank(hkv, ud) == Hkl, "k/v heads per rank do not match hkv and ud")
+    d = UspAttnDesc(bs, Lr * rd, Hl * ud, hkv, hd, rd, ud, _dtype_code(q), int(bool(causal)),
+                    float(scale) if scale is not None else 0.0, USP_MODE_FUSED, 0, _split_code(split), 0)
+    _abi.check("usp_attn_bwd", _abi.load().usp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse),
+                                                       _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), d, _stream(stream)))
+    return dq, dk, dv
+
+
+def usp_backward_workspace_size(q, k, ud: int, rd: int, head_chunk: Optional[int] = None, causal: bool = True) -> int:
+    """Workspace bytes usp_backward needs for these shapes."""
+    d = _forward_desc(q, k, ud, rd, causal, None)
+    n = _abi.load().usp_backward_workspace_size(d, int(head_chunk or 0))
+    _need(n > 0, "invalid backward shapes")
+    return int(n)
+
+
+def usp_backward(q, k, v, out, lse, dout, dq, dk, dv, ud: int, rd: int, causal: bool = True,
+                 scale: Optional[float] = None, head_chunk: Optional[int] = None,
+                 workspace: Optional[torch.Tensor] = None, split="zigzag", stream=None):
+    """The whole backward on device buffers in one C call (natural order in and out): dq, dk, dv of
+    the forward's out for the upstream gradient dout, given the forward's out and lse."""
+    _dev(q, k, v, out, lse, dout, dq, dk, dv)
+    _check_natural(q, k, v, out, lse)
+    _need(dout.shape == q.shape and dq.shape == q.shape and dk.shape == k.shape and dv.shape == k.shape,
+          "gradient shapes must match their inputs")
+    for t in (dout, dq, dk, dv):
+        _need(t.dtype == q.dtype and t.is_contiguous(), "gradients must be contiguous and of q's dtype")
+    d = _forward_desc(q, k, ud, rd, causal, scale, split)
+    n = usp_backward_workspace_size(q, k, ud, rd, head_chunk, causal=causal)
+    if workspace is None:
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _need(workspace.numel() >= n and workspace.is_cuda, "workspace too small")
+    _abi.check("usp_backward", _abi.load().usp_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), d,
+        int(head_chunk or 0), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dq, dk, dv
+
+
+class UspAttentionFunction(torch.autograd.Function):
+    """usp_forward / usp_backward as one differentiable op: out = USP-Attention(q, k, v) in natural
+    order, with gradients for q, k and v (lse is saved for the backward, not differentiated)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, ud, rd, causal=True, scale=None, head_chunk=None, split="zigzag"):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
+        usp_forward(q, k, v, out, lse, ud, rd, causal=causal, scale=scale, head_chunk=head_chunk, split=split)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.cfg = (ud, rd, causal, scale, head_chunk, split)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        ud, rd, causal, scale, head_chunk, split = ctx.cfg
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        usp_backward(q, k, v, out, lse, dout.contiguous(), dq, dk, dv, ud, rd, causal=causal, scale=scale,
+                     head_chunk=head_chunk, split=split)
+        return dq, dk, dv, None, None, None, None, None, None
 
 
 class UspAttention:

@@ -81,6 +81,15 @@ def load():
     lib.usp_forward_workspace_size.restype = ctypes.c_size_t
     lib.usp_attn_fwd.argtypes = [vp, vp, vp, vp, vp, UspAttnDesc, vp]
     lib.usp_attn_fwd.restype = ctypes.c_int
+    lib.usp_attn_bwd_delta.argtypes = [vp, vp, vp, i64, i32, i32, vp]
+    lib.usp_attn_bwd_delta.restype = ctypes.c_int
+    lib.usp_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, UspAttnDesc, vp]
+    lib.usp_attn_bwd.restype = ctypes.c_int
+    lib.usp_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, UspAttnDesc, ctypes.c_int, vp, ctypes.c_size_t,
+                                 vp]
+    lib.usp_backward.restype = ctypes.c_int
+    lib.usp_backward_workspace_size.argtypes = [UspAttnDesc, ctypes.c_int]
+    lib.usp_backward_workspace_size.restype = ctypes.c_size_t
     lib.usp_lse_merge.argtypes = [vp, vp, vp, vp, i64, i32, i32, vp]
     lib.usp_lse_merge.restype = ctypes.c_int
     lib.usp_check.argtypes = [vp]

@@ -1,5 +1,6 @@
 // forward.cu -- the whole USP-Attention forward (steps a1-a5, plus the inverse split a7 back to
-// natural order) as one call, on device buffers or pipelined from pinned host buffers.
+// natural order) as one call, on device buffers or pipelined from pinned host buffers; and the whole
+// backward on device buffers.
 //
 // Per head group (UPipe-style head chunking): the composed zigzag split + AllToAll4D of Q, K, V, the
 // fused ring attention, and the composed inverse of out and lse. The host-buffer variant overlaps,
@@ -47,6 +48,13 @@ int fwd_shape(const usp_attn_desc &d, int head_chunk, FwdShape &s) {
 // workspace of the device-buffer forward: head-sharded q, k, v, out, lse of one group
 size_t ws_device(const FwdShape &s) {
     return align_up(s.q_grp) * 2 + align_up(s.kv_hs) * 2 + align_up(s.lse_grp);
+}
+
+// workspace of the backward: D of all rows (natural), then per group head-sharded q, dout, dq,
+// k, v, dk, dv, lse and D
+size_t ws_backward(const FwdShape &s) {
+    const size_t d_all = (size_t)s.bs * s.L * s.hq * 4;
+    return align_up(d_all) + align_up(s.q_grp) * 3 + align_up(s.kv_hs) * 4 + align_up(s.lse_grp) * 2;
 }
 
 // the host-buffer forward adds two slots of compact natural-order staging for q, k, v and out, and
@@ -243,6 +251,57 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
     chk(cudaEventRecord(hp.d2h_done, hp.d2h) == cudaSuccess);
     chk(cudaStreamWaitEvent(user, hp.d2h_done, 0) == cudaSuccess);
     return okc ? USP_OK : USP_ERR_CUDA;
+}
+
+size_t usp_backward_workspace_size(usp_attn_desc d, int head_chunk) {
+    FwdShape s{};
+    if (fwd_shape(d, head_chunk, s) != USP_OK) return 0;
+    return ws_backward(s);
+}
+
+int usp_backward(const void *q, const void *k, const void *v, const void *out, const float *lse, const void *dout,
+                 void *dq, void *dk, void *dv, usp_attn_desc d, int head_chunk, void *workspace,
+                 size_t workspace_bytes, usp_stream_t stream) {
+    FwdShape s{};
+    int rc = fwd_shape(d, head_chunk, s);
+    if (rc) return rc;
+    if (d.bs == 0 || d.L == 0) return USP_OK;
+    if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return USP_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_backward(s)) return USP_ERR_INVALID_ARG;
+    if (!aligned(workspace, kAlign)) return USP_ERR_ALIGN;
+    Carve cv{static_cast<char *>(workspace), workspace_bytes};
+    float *d_all = static_cast<float *>(cv.take((size_t)s.bs * s.L * s.hq * 4));
+    void *qh = cv.take(s.q_grp), *gh = cv.take(s.q_grp), *dqh = cv.take(s.q_grp);
+    void *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *dkh = cv.take(s.kv_hs), *dvh = cv.take(s.kv_hs);
+    float *lh = static_cast<float *>(cv.take(s.lse_grp)), *dh = static_cast<float *>(cv.take(s.lse_grp));
+    // D = <dout, out> for every (token, query head), natural layout
+    if ((rc = usp_attn_bwd_delta(out, dout, d_all, s.bs * s.L * s.hq, s.hd, d.dtype, stream))) return rc;
+    for (int g0 = 0; g0 < s.hq; g0 += s.hc) {
+        const int gk = g0 / s.G;
+        const void *srcs[4] = {q, k, v, dout};
+        void *dsts[4] = {qh, kh, vh, gh};
+        usp_dims dd[4] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype), dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype),
+                          dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype), dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype)};
+        if ((rc = usp_extract_a2a(4, srcs, dsts, dd, 0, stream))) return rc;
+        const void *ls[2] = {lse, d_all};
+        void *ld[2] = {lh, dh};
+        usp_dims ldims[2] = {dims_of(s, s.hc, s.hq, g0, 1, USP_F32), dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
+        if ((rc = usp_extract_a2a(2, ls, ld, ldims, 0, stream))) return rc;
+        usp_attn_desc ad = d;
+        ad.hq = s.hc;
+        ad.hkv = s.hkc;
+        if ((rc = usp_attn_bwd(qh, kh, vh, gh, lh, dh, dqh, dkh, dvh, ad, stream))) return rc;
+        const void *qs[1] = {dqh};
+        void *qd[1] = {dq};
+        usp_dims qdims[1] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype)};
+        if ((rc = usp_extract_a2a(1, qs, qd, qdims, 1, stream))) return rc;
+        // the KV gradients: inverse all-to-all (summing the replicas of replicated heads) and split
+        const void *ks[2] = {dkh, dvh};
+        void *kd[2] = {dk, dv};
+        usp_dims kdims[2] = {dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype), dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype)};
+        if ((rc = usp_extract_a2a(2, ks, kd, kdims, 1, stream))) return rc;
+    }
+    return USP_OK;
 }
 
 }  // extern "C"

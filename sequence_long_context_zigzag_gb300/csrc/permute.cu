@@ -18,6 +18,7 @@
 // load and store instruction covers contiguous row segments (a 256-byte row is one half-warp).
 // Loads are issued in groups of 8 before their stores to keep enough bytes in flight for HBM.
 // Up to four tensors (e.g. Q, K and V) share one launch; batches are numbered across them.
+#include "usp_device.cuh"
 #include "usp_internal.cuh"
 
 namespace usp {
@@ -145,12 +146,122 @@ __global__ void __launch_bounds__(kWarps * 32) permute_rows_kernel(const __grid_
     }
 }
 
+// ---- the adjoint of the replicating all-to-all: each head receives the sum of its replicas ----
+// Destination rows are enumerated as [rd][Lr][bs][H] (ring rank, ring-local row, batch, head); row
+// (r, p, b, h) is natural token split_pos(r, p) (fused inverse) or sequence-sharded slot
+// (r, p / Lu, b, p % Lu) (plain inverse), and sums head-sharded rows (r, u', 0, b, p) over the
+// replicas u' in [h rep, (h + 1) rep). One thread per 16-byte vector; fp32 sums, rounded once.
+struct RepSumK {
+    const char *src;
+    char *dst;
+    uint32_t nvec;  // destination rows x vectors per row
+    uint32_t Ht, h0, rep, bs, L, Lr, Lu, c, rd, ud, vpr;
+    int mode, split;
+    FastDiv f_H, f_bs, f_Lr, f_Lu, f_vpr;
+};
+
+__device__ __forceinline__ void add_vec(float (&acc)[8], uint4 w, bool bf16) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    if (bf16) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = bf16x2_to_float2(u[e]);
+            acc[2 * e] += f.x;
+            acc[2 * e + 1] += f.y;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += __uint_as_float(u[e]);
+    }
+}
+
+__global__ void __launch_bounds__(256) replica_sum_kernel(const __grid_constant__ RepSumK p, int bf16) {
+    for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < p.nvec; t += gridDim.x * blockDim.x) {
+        uint32_t row, vec, q, h, b, pp, r;
+        p.f_vpr.divmod(t, row, vec);
+        p.f_H.divmod(row, q, h);
+        p.f_bs.divmod(q, q, b);
+        p.f_Lr.divmod(q, r, pp);
+        int64_t drow;
+        if (p.mode == PERM_FUSED_INV) {
+            drow = ((int64_t)b * p.L + split_pos(p.split, r, pp, p.c, p.rd)) * p.Ht + p.h0 + h;
+        } else {
+            uint32_t u, j;
+            p.f_Lu.divmod(pp, u, j);
+            drow = ((((int64_t)r * p.ud + u) * p.bs + b) * p.Lu + j) * p.Ht + p.h0 + h;
+        }
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (uint32_t k = 0; k < p.rep; ++k) {
+            const int64_t srow = (((int64_t)r * p.ud + h * p.rep + k) * p.bs + b) * p.Lr + pp;
+            add_vec(acc, __ldg(reinterpret_cast<const uint4 *>(p.src) + srow * p.vpr + vec), bf16 != 0);
+        }
+        uint4 o;
+        if (bf16) {
+            o = make_uint4(float2_to_bf16x2(acc[0], acc[1]), float2_to_bf16x2(acc[2], acc[3]),
+                           float2_to_bf16x2(acc[4], acc[5]), float2_to_bf16x2(acc[6], acc[7]));
+        } else {
+            o = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                           __float_as_uint(acc[3]));
+        }
+        reinterpret_cast<uint4 *>(p.dst)[drow * p.vpr + vec] = o;
+    }
+}
+
+int launch_replica_sum(const PermArgs &a, const PermJob &j, int sms, cudaStream_t s) {
+    if (a.row_bytes % 16 != 0 || (a.dtype != USP_BF16 && a.dtype != USP_F32)) return USP_ERR_UNSUPPORTED;
+    RepSumK p{};
+    p.src = j.src;
+    p.dst = j.dst;
+    p.mode = a.mode;
+    p.split = a.split;
+    p.Ht = (uint32_t)j.H_total;
+    p.h0 = (uint32_t)j.h0;
+    p.rep = (uint32_t)(a.ud / j.H);
+    p.bs = (uint32_t)a.bs;
+    p.L = (uint32_t)a.L;
+    p.rd = (uint32_t)a.rd;
+    p.ud = (uint32_t)a.ud;
+    p.Lr = (uint32_t)(a.L / a.rd);
+    p.Lu = p.Lr / p.ud;
+    p.c = (uint32_t)(a.L / (2 * a.rd));
+    p.vpr = (uint32_t)(a.row_bytes / 16);
+    const int64_t nvec = (int64_t)a.rd * p.Lr * a.bs * j.H * p.vpr;
+    if (nvec == 0) return USP_OK;
+    if (nvec >= (int64_t(1) << 31)) return USP_ERR_UNSUPPORTED;
+    p.nvec = (uint32_t)nvec;
+    p.f_H = FastDiv((uint32_t)j.H);
+    p.f_bs = FastDiv(p.bs);
+    p.f_Lr = FastDiv(p.Lr);
+    p.f_Lu = FastDiv(p.Lu);
+    p.f_vpr = FastDiv(p.vpr);
+    int64_t blocks = (nvec + 255) / 256;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    replica_sum_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, a.dtype == USP_BF16 ? 1 : 0);
+    return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA;
+}
+
 }  // namespace
 
 int launch_permute(const PermArgs &a, cudaStream_t s) {
     const DeviceInfo *di = device_info();
     if (!di) return USP_ERR_CUDA;
     if (a.njobs < 1 || a.njobs > kMaxPermJobs) return USP_ERR_INVALID_ARG;
+    // inverse all-to-all of replicated heads (H < ud): the replica sum, one launch per such tensor;
+    // the other tensors go through the row gather below
+    if (a.mode == PERM_A2A_INV || a.mode == PERM_FUSED_INV) {
+        PermArgs rest = a;
+        rest.njobs = 0;
+        for (int k = 0; k < a.njobs; ++k) {
+            if (a.job[k].H > 0 && a.job[k].H < a.ud) {
+                const int rc = launch_replica_sum(a, a.job[k], di->sm_count, s);
+                if (rc) return rc;
+            } else {
+                rest.job[rest.njobs++] = a.job[k];
+            }
+        }
+        if (rest.njobs == 0) return USP_OK;
+        if (rest.njobs < a.njobs) return launch_permute(rest, s);
+    }
     PermK p{};
     p.mode = a.mode;
     p.split = a.split;

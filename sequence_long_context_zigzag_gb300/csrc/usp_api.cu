@@ -33,8 +33,8 @@ const DeviceInfo *device_info() {
 
 static bool overflow31(int64_t x) { return x < 0 || x >= (int64_t(1) << 31); }
 
-// shared checks of a permute's dims. need_head_split: 0 = none (split only), 1 = ud must divide H
-// (the inverse all-to-all), 2 = ud divides H or H divides ud (the forward all-to-all replicates)
+// shared checks of a permute's dims. need_head_split: 0 = none (split only), 1 = ud must divide H,
+// 2 = ud divides H or H divides ud (the all-to-all replicates heads, its inverse sums the replicas)
 static int check_dims(const usp_dims &d, int need_head_split) {
     if (d.bs < 0 || d.L < 0 || d.H < 0 || d.hd <= 0 || d.rd <= 0 || d.ud <= 0 || d.h0 < 0 ||
         d.H_total < 0)
@@ -96,6 +96,7 @@ int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, int invers
                        d.h0};
     a.mode = inverse ? PERM_EXTRACT_INV : PERM_EXTRACT;
     a.split = d.split;
+    a.dtype = d.dtype;
     a.bs = d.bs; a.L = d.L;
     a.rd = d.rd; a.ud = d.ud; a.row_bytes = row_bytes;
     a.r_fixed = vr >= 0 ? vr / d.ud : -1;
@@ -105,7 +106,7 @@ int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, int invers
 
 int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stream) {
     if (dir != 1 && dir != -1) return USP_ERR_INVALID_ARG;
-    int rc = check_dims(d, dir > 0 ? 2 : 1);
+    int rc = check_dims(d, 2);  // fewer heads than ranks: replicate (dir +1) or sum replicas (dir -1)
     if (rc) return rc;
     if (d.bs == 0 || d.L == 0 || d.H == 0) return USP_OK;
     if (!src || !dst) return USP_ERR_INVALID_ARG;
@@ -116,6 +117,7 @@ int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stre
     a.job[0] = PermJob{static_cast<const char *>(src), static_cast<char *>(dst), d.H, d.H_total ? d.H_total : d.H,
                        d.h0};
     a.mode = dir > 0 ? PERM_A2A_FWD : PERM_A2A_INV;
+    a.dtype = d.dtype;
     a.bs = d.bs; a.L = d.L;
     a.rd = d.rd; a.ud = d.ud; a.row_bytes = row_bytes;
     a.r_fixed = -1; a.u_fixed = -1;
@@ -133,7 +135,7 @@ int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_d
     int64_t work = 0;
     for (int k = 0; k < n; ++k) {
         const usp_dims &dk = d[k];
-        int rc = check_dims(dk, inverse ? 1 : 2);
+        int rc = check_dims(dk, 2);
         if (rc) return rc;
         if (dk.bs != d[0].bs || dk.L != d[0].L || dk.rd != d[0].rd || dk.ud != d[0].ud || dk.hd != d[0].hd ||
             dk.dtype != d[0].dtype || dk.split != d[0].split)
@@ -151,13 +153,14 @@ int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_d
         if (rc) return rc;
     }
     a.split = d[0].split;
+    a.dtype = d[0].dtype;
     a.bs = d[0].bs; a.L = d[0].L;
     a.rd = d[0].rd; a.ud = d[0].ud; a.row_bytes = row_bytes;
     return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d,
-                 usp_stream_t stream) {
+// checks shared by the forward and backward attention entry points; fills the kernel arguments
+static int check_attn_desc(const usp_attn_desc &d) {
     if (d.bs < 0 || d.L < 0 || d.hq <= 0 || d.hkv <= 0 || d.rd <= 0 || d.ud <= 0)
         return USP_ERR_INVALID_ARG;
     if (d.mode < USP_MODE_FUSED || d.mode > USP_MODE_ACCUM) return USP_ERR_INVALID_ARG;
@@ -170,16 +173,61 @@ int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *
     if (d.hd != 64 && d.hd != 128) return USP_ERR_UNSUPPORTED;
     if (overflow31(d.bs * d.L * (int64_t)d.hq) || overflow31(d.L)) return USP_ERR_UNSUPPORTED;
     if (!(d.scale == d.scale) || isinf(d.scale)) return USP_ERR_INVALID_ARG;
-    if (d.bs == 0 || d.L == 0) return USP_OK;
-    if (!q || !k || !v || !out || !lse) return USP_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 16))
-        return USP_ERR_ALIGN;
+    return USP_OK;
+}
+
+static AttnArgs attn_args(const usp_attn_desc &d) {
     AttnArgs a{};
-    a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
     a.bs = d.bs; a.L = d.L; a.hq = d.hq; a.hkv = d.hkv; a.hd = d.hd; a.rd = d.rd; a.ud = d.ud;
     a.dtype = d.dtype; a.causal = d.causal ? 1 : 0; a.mode = d.mode; a.step = d.step;
     a.split = d.split; a.ring_rank_only = d.ring_rank_only;
     a.scale = d.scale > 0.f ? d.scale : 1.0f / sqrtf((float)d.hd);
+    return a;
+}
+
+int usp_attn_bwd_delta(const void *out, const void *dout, float *delta, int64_t rows, int32_t hd, int32_t dtype,
+                       usp_stream_t stream) {
+    if (rows < 0 || hd <= 0) return USP_ERR_INVALID_ARG;
+    const int es = elem_size(dtype);
+    if (es == 0) return USP_ERR_DTYPE;
+    if (((int64_t)hd * es) % 16 != 0) return USP_ERR_UNSUPPORTED;
+    if (overflow31(rows) || overflow31(rows * hd)) return USP_ERR_UNSUPPORTED;
+    if (rows == 0) return USP_OK;
+    if (!out || !dout || !delta) return USP_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(dout, 16) || !aligned(delta, 16)) return USP_ERR_ALIGN;
+    return launch_row_dot(out, dout, delta, rows, hd, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_attn_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse, const float *delta,
+                 void *dq, void *dk, void *dv, usp_attn_desc d, usp_stream_t stream) {
+    int rc = check_attn_desc(d);
+    if (rc) return rc;
+    if (d.mode != USP_MODE_FUSED || d.ring_rank_only != 0) return USP_ERR_INVALID_ARG;
+    if (d.bs == 0 || d.L == 0) return USP_OK;
+    const void *ptrs[] = {q, k, v, dout, lse, delta, dq, dk, dv};
+    for (const void *x : ptrs) {
+        if (!x) return USP_ERR_INVALID_ARG;
+        if (!aligned(x, 16)) return USP_ERR_ALIGN;
+    }
+    BwdArgs a{};
+    a.f = attn_args(d);
+    a.f.q = q; a.f.k = k; a.f.v = v;
+    a.f.lse = const_cast<float *>(lse);
+    a.dout = dout; a.delta = delta;
+    a.dq = dq; a.dk = dk; a.dv = dv;
+    return launch_attn_bwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d,
+                 usp_stream_t stream) {
+    int rc = check_attn_desc(d);
+    if (rc) return rc;
+    if (d.bs == 0 || d.L == 0) return USP_OK;
+    if (!q || !k || !v || !out || !lse) return USP_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 16))
+        return USP_ERR_ALIGN;
+    AttnArgs a = attn_args(d);
+    a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (d.dtype == USP_BF16) return launch_attn_tc(a, s);
     return launch_attn_simt(a, s);

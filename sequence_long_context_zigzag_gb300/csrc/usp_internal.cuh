@@ -118,6 +118,7 @@ struct PermArgs {
     int32_t rd, ud;
     int32_t r_fixed, u_fixed;  // >= 0 when only one virtual rank takes part (extract only)
     int64_t row_bytes;
+    int32_t dtype;             // element type (the replica sum of an inverse all-to-all adds values)
 };
 int launch_permute(const PermArgs &a, cudaStream_t s);
 
@@ -134,5 +135,15 @@ struct AttnArgs {
 };
 int launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 int launch_attn_tc(const AttnArgs &a, cudaStream_t s);
+
+// backward: the forward's arguments plus dout, delta and the three gradients
+struct BwdArgs {
+    AttnArgs f;
+    const void *dout;
+    const float *delta;
+    void *dq, *dk, *dv;
+};
+int launch_attn_bwd_simt(const BwdArgs &a, cudaStream_t s);
+int launch_row_dot(const void *x, const void *y, float *out, int64_t rows, int hd, int dtype, cudaStream_t s);
 
 }  // namespace usp

@@ -64,9 +64,10 @@ def test_a2a_rejects(d, code):
 
 def test_a2a_rejects_direction_and_alignment():
     lib = _abi.load()
-    # replication (H < ud, ud % H == 0) exists in the forward direction only
+    # fewer heads than ranks (ud % H == 0): replication forward, replica sum backward; both accepted
     assert lib.usp_a2a4d(BAD, BAD, dims(H=1, ud=4), 1, None) == _abi.USP_ERR_ALIGN
-    assert lib.usp_a2a4d(BAD, BAD, dims(H=1, ud=4), -1, None) == _abi.USP_ERR_SHAPE
+    assert lib.usp_a2a4d(BAD, BAD, dims(H=1, ud=4), -1, None) == _abi.USP_ERR_ALIGN
+    assert lib.usp_a2a4d(BAD, BAD, dims(H=3, ud=4), -1, None) == _abi.USP_ERR_SHAPE
     assert lib.usp_a2a4d(BAD, BAD, dims(), 0, None) == _abi.USP_ERR_INVALID_ARG
     assert lib.usp_a2a4d(BAD, BAD, dims(), 1, None) == _abi.USP_ERR_ALIGN
     assert lib.usp_a2a4d(None, BAD, dims(), 1, None) == _abi.USP_ERR_INVALID_ARG
@@ -177,3 +178,32 @@ def test_forward_noalloc_rejects_before_launch():
     # invalid shapes report the same status as usp_forward
     assert lib.usp_forward_noalloc(BAD, BAD, BAD, BAD, BAD, desc(L=250), 0, None) == _abi.USP_ERR_SHAPE
     assert lib.usp_forward_noalloc(None, None, None, None, None, desc(L=0), 0, None) == _abi.USP_OK
+
+
+def test_backward_rejects_before_launch():
+    lib = _abi.load()
+    nine = [BAD] * 9
+    assert lib.usp_attn_bwd(*nine, desc(mode=1), None) == _abi.USP_ERR_INVALID_ARG       # whole ring only
+    assert lib.usp_attn_bwd(*nine, desc(ring_rank_only=1), None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_attn_bwd(*nine, desc(hd=96), None) == _abi.USP_ERR_UNSUPPORTED
+    assert lib.usp_attn_bwd(*nine, desc(hq=6, hkv=3), None) == _abi.USP_ERR_SHAPE
+    assert lib.usp_attn_bwd(*nine, desc(), None) == _abi.USP_ERR_ALIGN
+    assert lib.usp_attn_bwd(None, *nine[1:], desc(), None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_attn_bwd(None, *nine[1:], desc(L=0), None) == _abi.USP_OK
+    assert lib.usp_attn_bwd_delta(BAD, BAD, BAD, 10, 4, _abi.USP_BF16, None) == _abi.USP_ERR_UNSUPPORTED
+    assert lib.usp_attn_bwd_delta(BAD, BAD, BAD, 10, 128, 9, None) == _abi.USP_ERR_DTYPE
+    assert lib.usp_attn_bwd_delta(BAD, BAD, BAD, 10, 128, _abi.USP_BF16, None) == _abi.USP_ERR_ALIGN
+    assert lib.usp_attn_bwd_delta(None, None, None, 0, 128, _abi.USP_BF16, None) == _abi.USP_OK
+
+
+def test_backward_workspace_size():
+    lib = _abi.load()
+    d = desc(L=1024, hq=8, hkv=2, ud=2, rd=2)
+    # D of all rows (1024*8*4 = 32 KiB), q/dout/dq groups (2 MiB each), k/v/dk/dv (512 KiB each),
+    # lse and D groups (32 KiB each)
+    assert lib.usp_backward_workspace_size(d, 0) == 2 ** 15 + 3 * 2 ** 21 + 4 * 2 ** 19 + 2 * 2 ** 15
+    assert lib.usp_backward_workspace_size(desc(mode=1), 0) == 0
+    ws = BAD - 1
+    n = lib.usp_backward_workspace_size(d, 0)
+    assert lib.usp_backward(*([BAD] * 9), d, 0, ws, n - 1, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_backward(*([BAD] * 9), d, 0, BAD, n, None) == _abi.USP_ERR_ALIGN
