@@ -216,6 +216,41 @@ class Step:
                 self.perm_events.append((e0, e1, e2, e3))
 
 
+def time_backward(usp, w, step, reps=5):
+    """The ring attention backward (usp_attn_bwd: the dk/dv and dq kernels) of the last head group,
+    on the step's head-sharded buffers and a seeded upstream gradient, median of ``reps`` launches.
+    Algorithmic FLOPs: 2.5x the forward's (five matrix products per causal pair instead of two)."""
+    if w.dtype != "bf16":
+        return None
+    g = torch.Generator(device="cuda").manual_seed(7)
+    dout = torch.randn(step.oh.shape, device="cuda", generator=g).to(step.oh.dtype)
+    delta = torch.empty_like(step.lh)
+    dq, dk, dv = torch.empty_like(step.qh), torch.empty_like(step.kh), torch.empty_like(step.vh)
+    usp.usp_attn_fwd(step.qh, step.kh, step.vh, step.oh, step.lh, causal=w.causal, hkv=step.hkc)
+    usp.usp_attn_bwd_delta(step.oh, dout, delta)
+
+    def once():
+        usp.usp_attn_bwd(step.qh, step.kh, step.vh, dout, step.lh, delta, dq, dk, dv, causal=w.causal, hkv=step.hkc)
+
+    once()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        once()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    usp.usp_check()
+    t = statistics.median(ts)
+    flops = 2.5 * w.causal_flops / len(step.groups)
+    peaks, _ = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    return {"kernel": "usp_attn_bwd (dk/dv and dq tensor-core kernels)", "ms": t * 1e3,
+            "tflops": flops / t / 1e12, "frac_of_peak": flops / t / 1e12 / peak,
+            "algorithmic_flops": flops, "note": f"one head group ({step.hc} query heads), median of {reps}"}
+
+
 def rank_balance(usp, w, q, k, v, reps=5):
     """Per-ring-rank attention time under each sequence split (each rank's query rows computed alone,
     median of ``reps`` launches): the load imbalance a multi-GPU ring would see, measured on the device.
@@ -436,6 +471,9 @@ def main():
     # ---- per-ring-rank work under the three splits (outside the timed region) ----------------
     balance = rank_balance(usp, w, q, k, v) if w.rd > 1 else None
 
+    # ---- the backward of one head group's ring attention (outside the timed region) ----------
+    backward = time_backward(usp, w, step, reps=max(3, args.steps // 2))
+
     # ---- CPU baseline (the oracle on the host cores), rank 0 at N = 1 -----------------------
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -475,6 +513,7 @@ def main():
                     "api": f"usp_forward_host (pinned host buffers, head_chunk={chunk}, wall clock)"},
             "gpu_launches": step.launches_per_step * args.steps,
             "rank_balance": balance,
+            "backward": backward,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

@@ -29,6 +29,7 @@
 // word, drains what it has in flight and returns.
 #include <cuda.h>
 
+#include "tc_common.cuh"
 #include "tc_ptx.cuh"
 #include "usp_device.cuh"
 #include "usp_internal.cuh"
@@ -118,28 +119,6 @@ struct TileIter {
     uint32_t kt, nkt, s;
     uint32_t nhi[2], nlo[2];
 };
-
-// global position of ring-local row p on ring rank r (chunk length c = Lr / 2) under the split:
-// zigzag keeps chunks r and 2 rd - 1 - r, basic the contiguous block r, stripe every rd-th token
-__device__ __forceinline__ uint32_t pos32(int split, uint32_t r, uint32_t p, uint32_t c, uint32_t rd) {
-    if (split == USP_SPLIT_BASIC) return r * 2 * c + p;
-    if (split == USP_SPLIT_STRIPE) return p * rd + r;
-    return p < c ? r * c + p : (2 * rd - 1 - r) * c + (p - c);
-}
-
-// number of ring-local rows of rank s whose global position is <= qpos (a prefix: every split's
-// position map is increasing in the row)
-__device__ __forceinline__ uint32_t vis32(int split, uint32_t qpos, uint32_t s, uint32_t c, uint32_t rd) {
-    if (split == USP_SPLIT_BASIC) {
-        const uint32_t a0 = s * 2 * c;
-        return qpos < a0 ? 0u : min(qpos - a0 + 1, 2 * c);
-    }
-    if (split == USP_SPLIT_STRIPE) return qpos < s ? 0u : min((qpos - s) / rd + 1, 2 * c);
-    const uint32_t a0 = s * c, a1 = (2 * rd - 1 - s) * c;
-    const uint32_t c0 = qpos < a0 ? 0u : min(qpos - a0 + 1, c);
-    const uint32_t c1 = qpos < a1 ? 0u : min(qpos - a1 + 1, c);
-    return c0 + c1;
-}
 
 __device__ __forceinline__ Work decode_work(const TcParams &p) {
     Work w;
@@ -654,38 +633,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 // ------------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
-    return fn;
-}
-
-// 2-D view (rows x hd) of a bf16 tensor, 128-row x 64-column boxes, 128-byte swizzle, zero fill
-bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, int hd) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)hd * 2};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int HD>
 int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
     using C = Cfg<HD>;
@@ -716,8 +663,8 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     const uint64_t q_rows = (uint64_t)a.hq * a.bs * a.L;
     // K/V rows in the head-sharded layout [rd][ud][Hkl][bs][Lr]: Hkl * ud heads of bs * L tokens
     const uint64_t kv_rows = (uint64_t)heads_per_rank(a.hkv, a.ud) * a.ud * a.bs * a.L;
-    if (!make_tmap(&p.tq, a.q, q_rows, a.hd) || !make_tmap(&p.tk, a.k, kv_rows, a.hd) ||
-        !make_tmap(&p.tv, a.v, kv_rows, a.hd))
+    if (!make_tmap(&p.tq, a.q, q_rows, a.hd, 128) || !make_tmap(&p.tk, a.k, kv_rows, a.hd, 128) ||
+        !make_tmap(&p.tv, a.v, kv_rows, a.hd, 128))
         return USP_ERR_CUDA;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.lse = a.lse;

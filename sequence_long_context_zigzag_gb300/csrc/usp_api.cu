@@ -215,7 +215,9 @@ int usp_attn_bwd(const void *q, const void *k, const void *v, const void *dout, 
     a.f.lse = const_cast<float *>(lse);
     a.dout = dout; a.delta = delta;
     a.dq = dq; a.dk = dk; a.dv = dv;
-    return launch_attn_bwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d.dtype == USP_BF16) return launch_attn_bwd_tc(a, s);
+    return launch_attn_bwd_simt(a, s);
 }
 
 int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d,

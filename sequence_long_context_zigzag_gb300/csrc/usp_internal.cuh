@@ -144,6 +144,7 @@ struct BwdArgs {
     void *dq, *dk, *dv;
 };
 int launch_attn_bwd_simt(const BwdArgs &a, cudaStream_t s);
+int launch_attn_bwd_tc(const BwdArgs &a, cudaStream_t s);
 int launch_row_dot(const void *x, const void *y, float *out, int64_t rows, int hd, int dtype, cudaStream_t s);
 
 }  // namespace usp

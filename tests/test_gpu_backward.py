@@ -123,6 +123,33 @@ def test_head_sharded_backward_matches_mapped_oracle():
     assert rel_err(dq, hs(rq)) <= 2e-4 and rel_err(dk, hs(rk)) <= 2e-4 and rel_err(dv, hs(rv)) <= 2e-4
 
 
+def test_head_sharded_backward_bf16_replicated():
+    """Tensor-core backward on head-sharded buffers with replicated K/V (MQA, ud = 4): each replica
+    carries its own rank's share; summing the replicas (the inverse all-to-all) gives the oracle's."""
+    L, hq, hkv, hd, ud, rd = 1024, 8, 1, 128, 4, 2
+    q, k, v, g = _inputs(L, hq, hkv, hd, "bf16", seed=33)
+    Lr = L // rd
+    qh = torch.empty(rd, ud, hq // ud, 1, Lr, hd, device="cuda", dtype=torch.bfloat16)
+    gh = torch.empty_like(qh)
+    kh = torch.empty(rd, ud, 1, 1, Lr, hd, device="cuda", dtype=torch.bfloat16)
+    vh = torch.empty_like(kh)
+    usp.usp_extract_a2a([q.cuda(), k.cuda(), v.cuda(), g.cuda()], [qh, kh, vh, gh], rd, ud)
+    oh = torch.empty_like(qh)
+    lh = torch.empty(qh.shape[:5], device="cuda")
+    usp.usp_attn_fwd(qh, kh, vh, oh, lh, hkv=hkv)
+    dh = torch.empty_like(lh)
+    usp.usp_attn_bwd_delta(oh, gh, dh)
+    dq, dk, dv = torch.empty_like(qh), torch.empty_like(kh), torch.empty_like(vh)
+    usp.usp_attn_bwd(qh, kh, vh, gh, lh, dh, dq, dk, dv, hkv=hkv)
+    dk_n = torch.empty(1, L, hkv, hd, device="cuda", dtype=torch.bfloat16)
+    dv_n = torch.empty_like(dk_n)
+    usp.usp_extract_a2a([dk, dv], [dk_n, dv_n], rd, ud, inverse=True)
+    usp.usp_check()
+    rq, rk, rv = oracle.attn_direct_bwd(q, k, v, g)
+    hs = lambda x: oracle.a2a_fwd(oracle.extract_local(x, rd, ud), ud)  # noqa: E731
+    assert rel_err(dq, hs(rq)) <= 2e-2 and rel_err(dk_n, rk) <= 2e-2 and rel_err(dv_n, rv) <= 2e-2
+
+
 def test_autograd_function():
     L, hq, hkv, hd, ud, rd = 512, 4, 2, 128, 2, 2
     q, k, v, g = _inputs(L, hq, hkv, hd, "bf16", seed=41)
@@ -134,3 +161,67 @@ def test_autograd_function():
     assert max(rel_err(qd.grad, rq), rel_err(kd.grad, rk), rel_err(vd.grad, rv)) <= 2e-2
     o_ref, _ = oracle.attn_direct(q, k, v)
     assert np.abs(out.detach().float().cpu().numpy() - o_ref).max() <= 2e-2
+
+
+@pytest.mark.parametrize("L,hq,hkv,hd,ud,rd", [(4096, 8, 2, 128, 2, 4), (2000, 4, 4, 64, 1, 5), (3072, 8, 1, 128, 4, 3)])
+def test_backward_many_tiles(L, hq, hkv, hd, ud, rd):
+    """Several 128-key CTAs and 64-row tiles per block, ragged block ends (Lr = 400 at L = 2000),
+    and the dk/dv kernel's walk over every ring rank's visible query tiles."""
+    q, k, v, g = _inputs(L, hq, hkv, hd, "bf16", seed=L + rd)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    out = torch.empty_like(qd)
+    lse = torch.empty(1, L, hq, device="cuda")
+    usp.usp_forward(qd, kd, vd, out, lse, ud, rd)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    usp.usp_backward(qd, kd, vd, out, lse, gd, dq, dk, dv, ud, rd)
+    usp.usp_check()
+    rq, rk, rv = oracle.attn_direct_bwd(q, k, v, g)
+    errs = [rel_err(dq, rq), rel_err(dk, rk), rel_err(dv, rv)]
+    print(f"L={L} hq={hq} hkv={hkv} hd={hd} ud={ud} rd={rd}: rel err dq {errs[0]:.2e} dk {errs[1]:.2e} dv {errs[2]:.2e}")
+    assert max(errs) <= 2e-2
+
+
+def test_backward_noncausal():
+    L, hq, hkv, hd, ud, rd = 1024, 4, 2, 128, 2, 2
+    q, k, v, g = _inputs(L, hq, hkv, hd, "bf16", seed=12)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    out = torch.empty_like(qd)
+    lse = torch.empty(1, L, hq, device="cuda")
+    usp.usp_forward(qd, kd, vd, out, lse, ud, rd, causal=False)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    usp.usp_backward(qd, kd, vd, out, lse, gd, dq, dk, dv, ud, rd, causal=False)
+    usp.usp_check()
+    rq, rk, rv = oracle.attn_direct_bwd(q, k, v, g, causal=False)
+    assert max(rel_err(dq, rq), rel_err(dk, rk), rel_err(dv, rv)) <= 2e-2
+
+
+@pytest.mark.parametrize("wi", [1, 2])
+def test_backward_full_size_sampled(wi):
+    """At the workloads' full sizes: dq on seeded sampled rows (plus chunk-boundary rows) and dk, dv
+    on the last 256 keys (seen only by the last queries, so the oracle stays cheap); and the
+    invariants that hold at any size, sum_j dk_j = 0 and sum_j dv_j = sum of dout over the group."""
+    from seeded_inputs import WORKLOADS, default_seed, make_rows, make_workload_qkv
+    w = WORKLOADS[wi]
+    seed = default_seed(wi)
+    q, k, v = make_workload_qkv(w, seed)
+    g, _, _ = make_qkv(w.bs, w.L, w.hq, w.hkv, w.hd, w.dtype, seed=seed + 500)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    out = torch.empty_like(qd)
+    lse = torch.empty(w.bs, w.L, w.hq, device="cuda")
+    usp.usp_forward(qd, kd, vd, out, lse, w.ud, w.rd, head_chunk=w.head_chunk)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    usp.usp_backward(qd, kd, vd, out, lse, gd, dq, dk, dv, w.ud, w.rd, head_chunk=w.head_chunk)
+    usp.usp_check()
+    rows = np.array(make_rows(w.L, w.c, 128, seed))
+    j0 = w.L - 256
+    rq, rk, rv = oracle.attn_direct_bwd(q, k, v, g, q_rows=rows, kv_from=j0)
+    e_q = rel_err(dq[:, torch.as_tensor(rows, device="cuda")], rq)
+    e_k, e_v = rel_err(dk[:, j0:], rk), rel_err(dv[:, j0:], rv)
+    print(f"{w.name}: dq rows {len(rows)} rel {e_q:.2e}; dk/dv tail rel {e_k:.2e} / {e_v:.2e}")
+    assert max(e_q, e_k, e_v) <= 2e-2
+    G = w.hq // w.hkv
+    dk_sum = dk.double().sum(dim=1)
+    assert dk_sum.abs().max().item() <= 2e-2 * max(dk.double().abs().sum(dim=1).max().item(), 1.0)
+    dv_sum = dv.double().sum(dim=1)
+    g_sum = gd.double().reshape(w.bs, w.L, w.hkv, G, w.hd).sum(dim=(1, 3))
+    assert (dv_sum - g_sum).abs().max().item() <= 2e-2 * max(g_sum.abs().max().item(), 1.0) + 1e-2 * w.L ** 0.5
