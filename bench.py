@@ -34,7 +34,9 @@ DEFAULT_WORKLOAD = 1
 L2_BYTES = 129 * 10 ** 6
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_tc_kernel_mha_L8192.md")
-ATTN_SRC = os.path.join(ROOT, "sequence_long_context_zigzag_gb300", "csrc", "attn_tc.cu")
+# the forward attention kernel's sources: the traffic figure is valid only for this exact code
+ATTN_SRCS = [os.path.join(ROOT, "sequence_long_context_zigzag_gb300", "csrc", f)
+             for f in ("attn_tc.cu", "tc_ptx.cuh", "tc_common.cuh")]
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -286,6 +288,15 @@ def rank_balance(usp, w, q, k, v, reps=5):
     return res
 
 
+def attn_src_hash():
+    """First 16 hex digits of the SHA-256 of the forward kernel's sources, concatenated in order."""
+    hs = hashlib.sha256()
+    for fn in ATTN_SRCS:
+        with open(fn, "rb") as f:
+            hs.update(f.read())
+    return hs.hexdigest()[:16]
+
+
 def traffic_for_current_kernel(workload_index):
     """DRAM bytes per attention launch (read + write) from the committed ncu summary, if it was taken
     on this workload and on the attention kernel source as it is now (else None)."""
@@ -298,8 +309,7 @@ def traffic_for_current_kernel(workload_index):
                 k, sep, v = line.partition(":")
                 if sep:
                     rec[k.strip()] = v.strip()
-        with open(ATTN_SRC, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        h = attn_src_hash()
     except OSError:
         return None
     if rec.get("attn_src_sha256_16") != h or "dram_bytes_per_launch" not in rec:
