@@ -144,7 +144,7 @@ __device__ __forceinline__ void store_zero32(__nv_bfloat16 *dst) {
 // ================================================================================================
 template <int HD> struct KvCfg : Lay<HD> {
     using Y = Lay<HD>;
-    static constexpr int kStages = HD == 128 ? 3 : 4;
+    static constexpr int kStages = HD == 128 ? 4 : 6;
     static constexpr int kK = 0;
     static constexpr int kV = Y::kBigTile;
     static constexpr int kQ = 2 * Y::kBigTile;              // stage s: Q at kQ + s * kStage, dout + kSmallTile
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkv_kernel(const __grid_
 // ================================================================================================
 template <int HD> struct QCfg : Lay<HD> {
     using Y = Lay<HD>;
-    static constexpr int kStages = HD == 128 ? 4 : 6;
+    static constexpr int kStages = HD == 128 ? 5 : 8;
     static constexpr int kQ = 0;
     static constexpr int kDo = Y::kBigTile;
     static constexpr int kKV = 2 * Y::kBigTile;             // stage s: K at kKV + s * kStage, V + kSmallTile
