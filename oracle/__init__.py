@@ -58,6 +58,11 @@ def _load():
     i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
     lib.oracle_attn_direct.argtypes = [vp, vp, vp, i32, i64, i64, i32, i32, i32, dbl, i32, vp, i64, vp, vp]
     lib.oracle_attn_direct.restype = i32
+    lib.oracle_attn_direct_seg.argtypes = [vp, vp, vp, i32, i64, i64, i32, i32, i32, dbl, i32, vp, vp, vp, i64, vp,
+                                           vp]
+    lib.oracle_attn_direct_seg.restype = i32
+    lib.oracle_attn_block_seg.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, i64, i32, i32, i32, dbl, i32, vp, vp]
+    lib.oracle_attn_block_seg.restype = i32
     lib.oracle_attn_block.argtypes = [vp, vp, i64, vp, vp, vp, i64, i32, i32, i32, dbl, i32, vp, vp]
     lib.oracle_attn_block.restype = i32
     lib.oracle_attn_bwd_direct.argtypes = [vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, dbl, i32, vp, i64, vp,
@@ -108,12 +113,24 @@ def _p(a):
 # ----------------------------------------------------------------------------------------------
 # attention (C core)
 # ----------------------------------------------------------------------------------------------
-def attn_direct(q, k, v, scale=None, causal=True, rows=None):
+def seg_bounds(cu_seqlens, L):
+    """Packed sequences: for every position, the first and one-past-last position of its sample and
+    the sample's index. cu_seqlens = [0, l_0, l_0 + l_1, ..., L] (the samples' cumulative lengths)."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    if cu.ndim != 1 or len(cu) < 2 or cu[0] != 0 or cu[-1] != L or np.any(np.diff(cu) <= 0):
+        raise ValueError("cu_seqlens must rise strictly from 0 to L")
+    ids = np.repeat(np.arange(len(cu) - 1), np.diff(cu))
+    return cu[ids], cu[ids + 1], ids
+
+
+def attn_direct(q, k, v, scale=None, causal=True, rows=None, cu_seqlens=None):
     """Direct softmax attention with row LSE for selected query rows, natural token order.
 
     q: (bs, L, hq, hd), k/v: (bs, L, hkv, hd); fp32, bf16 or fp64 (torch tensors or numpy).
     Returns out (bs, nrows, hq, hd) fp64 and lse (bs, nrows, hq) fp64 (natural log).
     Context-Parallel page, section 先弄清楚 (partial output and log-sum-exp); causal mask j <= i.
+    cu_seqlens: packed samples (every batch element packed alike); a query sees only keys of its own
+    sample (the sequence packing of the Context-Parallel page's ByteScale section).
     """
     qa, dt = _raw(q)
     ka, dk = _raw(k)
@@ -127,14 +144,21 @@ def attn_direct(q, k, v, scale=None, causal=True, rows=None):
     rows = np.arange(L, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     out = np.empty((bs, len(rows), hq, hd), dtype=np.float64)
     lse = np.empty((bs, len(rows), hq), dtype=np.float64)
-    rc = _load().oracle_attn_direct(_p(qa), _p(ka), _p(va), dt, bs, L, hq, hkv, hd, float(scale),
-                                    int(bool(causal)), _p(rows), len(rows), _p(out), _p(lse))
+    if cu_seqlens is None:
+        rc = _load().oracle_attn_direct(_p(qa), _p(ka), _p(va), dt, bs, L, hq, hkv, hd, float(scale),
+                                        int(bool(causal)), _p(rows), len(rows), _p(out), _p(lse))
+    else:
+        st, en, _ = seg_bounds(cu_seqlens, L)
+        st, en = np.ascontiguousarray(st), np.ascontiguousarray(en)
+        rc = _load().oracle_attn_direct_seg(_p(qa), _p(ka), _p(va), dt, bs, L, hq, hkv, hd, float(scale),
+                                            int(bool(causal)), _p(st), _p(en), _p(rows), len(rows), _p(out),
+                                            _p(lse))
     if rc != 0:
         raise ValueError("oracle_attn_direct: bad arguments")
     return out, lse
 
 
-def attn_block(q, qpos, k, v, kpos, scale, causal=True):
+def attn_block(q, qpos, k, v, kpos, scale, causal=True, qseg=None, kseg=None):
     """Attention of query rows against one block of keys, masked on explicit global positions.
 
     q: (hq, nq, hd) fp64, k/v: (hkv, nk, hd) fp64. Returns (o (hq, nq, hd), lse (hq, nq)); rows that
@@ -149,8 +173,14 @@ def attn_block(q, qpos, k, v, kpos, scale, causal=True):
     hkv, nk, _ = k.shape
     o = np.empty((hq, nq, hd), dtype=np.float64)
     lse = np.empty((hq, nq), dtype=np.float64)
-    rc = _load().oracle_attn_block(_p(q), _p(qpos), nq, _p(k), _p(v), _p(kpos), nk, hq, hkv, hd,
-                                   float(scale), int(bool(causal)), _p(o), _p(lse))
+    if qseg is None:
+        rc = _load().oracle_attn_block(_p(q), _p(qpos), nq, _p(k), _p(v), _p(kpos), nk, hq, hkv, hd,
+                                       float(scale), int(bool(causal)), _p(o), _p(lse))
+    else:
+        qseg = np.ascontiguousarray(qseg, dtype=np.int64)
+        kseg = np.ascontiguousarray(kseg, dtype=np.int64)
+        rc = _load().oracle_attn_block_seg(_p(q), _p(qpos), _p(qseg), nq, _p(k), _p(v), _p(kpos), _p(kseg), nk,
+                                           hq, hkv, hd, float(scale), int(bool(causal)), _p(o), _p(lse))
     if rc != 0:
         raise ValueError("oracle_attn_block: bad arguments")
     return o, lse
@@ -405,7 +435,7 @@ def ring_schedule(cp):
     return [[ring_source(r, t, cp) for r in range(cp)] for t in range(cp)]
 
 
-def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True, split="zigzag"):
+def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True, split="zigzag", cu_seqlens=None):
     """USP-Attention forward, run rank by rank over the virtual ud x rd grid, in fp64.
 
     Algorithm 2 split (a1), AllToAll4D on Q, K, V (a2), for every ring rank the ring loop in Fig. 1
@@ -413,6 +443,8 @@ def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True, split="zigzag"):
     AllToAll4D on O and on lse (a5) and the inverse split (a7).
     q: (bs, L, hq, hd), k/v: (bs, L, hkv, hd) numpy or torch (any float dtype; widened to fp64).
     Returns out (bs, L, hq, hd) and lse (bs, L, hq) in natural order.
+    cu_seqlens: packed samples; the split is applied to the packed sequence as to one sequence, and
+    every block keeps a key only for queries of the same sample.
     """
     q, k, v = (np.asarray(_to_f64(x)) for x in (q, k, v))
     bs, L, hq, hd = q.shape
@@ -426,6 +458,8 @@ def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True, split="zigzag"):
     K = a2a_fwd(extract_local(k, rd, ud, split=split), ud)          # [rd][ud][max(hkv/ud,1)][bs][Lr][hd]
     V = a2a_fwd(extract_local(v, rd, ud, split=split), ud)
     pos = [split_pos(split, r, np.arange(Lr), L, rd) for r in range(rd)]
+    seg = None if cu_seqlens is None else seg_bounds(cu_seqlens, L)[2]
+    sg = (lambda r: None) if seg is None else (lambda r: seg[pos[r]])  # noqa: E731
     O = np.zeros_like(Q)
     LSE = np.full(Q.shape[:5], -np.inf)
     for r in range(rd):
@@ -436,7 +470,7 @@ def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True, split="zigzag"):
                 for t in range(rd):
                     s = ring_source(r, t, rd)
                     o_t, l_t = attn_block(Q[r, u, :, b], pos[r], K[s, u, :, b], V[s, u, :, b], pos[s],
-                                          scale, causal)
+                                          scale, causal, sg(r), sg(s))
                     o_acc, l_acc = lse_merge(o_acc, l_acc, o_t, l_t)
                 O[r, u, :, b] = o_acc
                 LSE[r, u, :, b] = l_acc

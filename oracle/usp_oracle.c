@@ -56,9 +56,30 @@ int oracle_num_threads(void)
  * causal != 0 keeps keys j <= i; otherwise all L keys.
  * Returns 0, or -1 on a bad argument / allocation failure.
  */
+int oracle_attn_direct_seg(const void *q, const void *k, const void *v, int dtype,
+                           int64_t bs, int64_t L, int hq, int hkv, int hd, double scale, int causal,
+                           const int64_t *seg_start, const int64_t *seg_end,
+                           const int64_t *rows, int64_t nrows, double *out, double *lse);
+
 int oracle_attn_direct(const void *q, const void *k, const void *v, int dtype,
                        int64_t bs, int64_t L, int hq, int hkv, int hd, double scale, int causal,
                        const int64_t *rows, int64_t nrows, double *out, double *lse)
+{
+    return oracle_attn_direct_seg(q, k, v, dtype, bs, L, hq, hkv, hd, scale, causal, NULL, NULL, rows, nrows,
+                                  out, lse);
+}
+
+/*
+ * Packed sequences (sequence packing: several samples concatenated into one sequence, each attending
+ * only within itself -- the ByteScale motivation on the Context-Parallel page): seg_start[i] and
+ * seg_end[i] are the first and one-past-last positions of the sample that position i belongs to.
+ * Key j is visible to query i iff seg_start[i] <= j < seg_end[i] and, when causal, j <= i.
+ * NULL seg arrays mean one sample spanning the sequence.
+ */
+int oracle_attn_direct_seg(const void *q, const void *k, const void *v, int dtype,
+                           int64_t bs, int64_t L, int hq, int hkv, int hd, double scale, int causal,
+                           const int64_t *seg_start, const int64_t *seg_end,
+                           const int64_t *rows, int64_t nrows, double *out, double *lse)
 {
     if (bs <= 0 || L <= 0 || hq <= 0 || hkv <= 0 || hd <= 0 || hq % hkv != 0 || nrows < 0)
         return -1;
@@ -84,11 +105,12 @@ int oracle_attn_direct(const void *q, const void *k, const void *v, int dtype,
                 const int64_t b = t / ((int64_t)hq * nrows);
                 const int64_t i = rows[ri];
                 const int kh = h / G;
-                const int64_t nk = causal ? i + 1 : L;
+                const int64_t j0 = seg_start ? seg_start[i] : 0;
+                const int64_t nk = causal ? i + 1 : (seg_end ? seg_end[i] : L);
                 for (int d = 0; d < hd; ++d)
                     qi[d] = widen(q, ((b * L + i) * hq + h) * hd + d, dtype);
                 double m = -INFINITY;
-                for (int64_t j = 0; j < nk; ++j) {
+                for (int64_t j = j0; j < nk; ++j) {
                     const int64_t kb = ((b * L + j) * hkv + kh) * hd;
                     double dot = 0.0;
                     for (int d = 0; d < hd; ++d) dot += qi[d] * widen(k, kb + d, dtype);
@@ -96,10 +118,10 @@ int oracle_attn_direct(const void *q, const void *k, const void *v, int dtype,
                     if (s[j] > m) m = s[j];
                 }
                 double sum = 0.0;
-                for (int64_t j = 0; j < nk; ++j) sum += exp(s[j] - m);
+                for (int64_t j = j0; j < nk; ++j) sum += exp(s[j] - m);
                 const double l = m + log(sum);
                 for (int d = 0; d < hd; ++d) acc[d] = 0.0;
-                for (int64_t j = 0; j < nk; ++j) {
+                for (int64_t j = j0; j < nk; ++j) {
                     const double p = exp(s[j] - l);
                     const int64_t vb = ((b * L + j) * hkv + kh) * hd;
                     for (int d = 0; d < hd; ++d) acc[d] += p * widen(v, vb + d, dtype);
@@ -123,9 +145,22 @@ int oracle_attn_direct(const void *q, const void *k, const void *v, int dtype,
  * causal != 0 keeps key j for query i iff kpos[j] <= qpos[i]. Rows with no kept key get
  * o = 0, lse = -inf.
  */
+int oracle_attn_block_seg(const double *q, const int64_t *qpos, const int64_t *qseg, int64_t nq,
+                          const double *k, const double *v, const int64_t *kpos, const int64_t *kseg, int64_t nk,
+                          int hq, int hkv, int hd, double scale, int causal, double *out, double *lse);
+
 int oracle_attn_block(const double *q, const int64_t *qpos, int64_t nq,
                       const double *k, const double *v, const int64_t *kpos, int64_t nk,
                       int hq, int hkv, int hd, double scale, int causal, double *out, double *lse)
+{
+    return oracle_attn_block_seg(q, qpos, NULL, nq, k, v, kpos, NULL, nk, hq, hkv, hd, scale, causal, out, lse);
+}
+
+/* The same with the sample index of every query and key (packed sequences): key j is kept for query
+ * i only if qseg[i] == kseg[j] (and kpos[j] <= qpos[i] when causal); NULL arrays mean one sample. */
+int oracle_attn_block_seg(const double *q, const int64_t *qpos, const int64_t *qseg, int64_t nq,
+                          const double *k, const double *v, const int64_t *kpos, const int64_t *kseg, int64_t nk,
+                          int hq, int hkv, int hd, double scale, int causal, double *out, double *lse)
 {
     if (nq < 0 || nk < 0 || hq <= 0 || hkv <= 0 || hd <= 0 || hq % hkv != 0) return -1;
     const int G = hq / hkv;
@@ -148,7 +183,7 @@ int oracle_attn_block(const double *q, const int64_t *qpos, int64_t nq,
                 double m = -INFINITY;
                 int64_t nkeep = 0;
                 for (int64_t j = 0; j < nk; ++j) {
-                    keep[j] = (char)(!causal || kpos[j] <= qpos[i]);
+                    keep[j] = (char)((!causal || kpos[j] <= qpos[i]) && (!qseg || qseg[i] == kseg[j]));
                     if (!keep[j]) continue;
                     ++nkeep;
                     const double *kj = k + ((int64_t)kh * nk + j) * hd;
