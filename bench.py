@@ -253,6 +253,34 @@ def time_backward(usp, w, step, reps=5):
             "algorithmic_flops": flops, "note": f"one head group ({step.hc} query heads), median of {reps}"}
 
 
+def packing(usp, w, step, reps=5):
+    """The pages' packing case (ByteScale): the same total length packed as 1, 2 and L/1024 samples,
+    each sample attending only within itself. The ring attention of the last head group is timed for
+    each packing (median of ``reps``); FLOPs count each sample's causal pairs, 4 hq hd len^2 / 2."""
+    if w.dtype != "bf16" or not w.causal:
+        return None
+    res = {}
+    for n in (1, 2, max(2, w.L // 1024)):
+        if w.L % n:
+            continue
+        cu = torch.arange(0, w.L + 1, w.L // n, dtype=torch.int32, device="cuda")
+        kw = {} if n == 1 else {"cu_seqlens": cu}
+        ts = []
+        for r in range(reps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            usp.usp_attn_fwd(step.qh, step.kh, step.vh, step.oh, step.lh, causal=True, hkv=step.hkc, **kw)
+            e1.record()
+            torch.cuda.synchronize()
+            if r:
+                ts.append(e0.elapsed_time(e1) / 1e3)
+        t = statistics.median(ts)
+        fl = 4.0 * step.hc * w.hd * n * (w.L // n) ** 2 / 2 * w.bs
+        res[f"{n}x{w.L // n}"] = {"ms": round(t * 1e3, 4), "tflops": round(fl / t / 1e12, 1)}
+    usp.usp_check()
+    return res
+
+
 def rank_balance(usp, w, q, k, v, reps=5):
     """Per-ring-rank attention time under each sequence split (each rank's query rows computed alone,
     median of ``reps`` launches): the load imbalance a multi-GPU ring would see, measured on the device.
@@ -483,6 +511,7 @@ def main():
 
     # ---- the backward of one head group's ring attention (outside the timed region) ----------
     backward = time_backward(usp, w, step, reps=max(3, args.steps // 2))
+    packed = packing(usp, w, step)
 
     # ---- CPU baseline (the oracle on the host cores), rank 0 at N = 1 -----------------------
     cpu = None
@@ -524,6 +553,7 @@ def main():
             "gpu_launches": step.launches_per_step * args.steps,
             "rank_balance": balance,
             "backward": backward,
+            "packing": packed,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

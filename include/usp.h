@@ -173,6 +173,11 @@ typedef struct {
     int32_t split;  /* usp_split of q / k / v (must match the split the permutes used) */
     int32_t ring_rank_only; /* 0: every ring rank; k > 0: only ring rank k - 1's query rows are
                                computed and written (its share of the work, e.g. to time one rank) */
+    int32_t nseq;   /* packed samples: 0 (or 1) = one sequence; n > 1 = n samples concatenated */
+    const int32_t *cu_seqlens; /* DEVICE array of nseq + 1 cumulative sample lengths, 0 = cu[0] <
+                               cu[1] < ... < cu[nseq] = L (the same packing for every batch element);
+                               a query sees only keys of its own sample. Read by the kernels only;
+                               values that break these rules give meaningless masks, not faults. */
 } usp_attn_desc;
 
 /*
@@ -186,7 +191,9 @@ typedef struct {
  *            Ulysses rank holds the replica of KV head u' / (ud / hkv), as usp_a2a4d writes it)
  *   lse    : [rd][ud][hq/ud][bs][Lr] fp32, natural log of the row's softmax normaliser.
  * Row p of ring rank r is the token at global position zig(r, p); the causal mask compares global
- * positions. Scores are scale * <q, k>; inputs bf16 (tensor cores, fp32 accumulation, bf16 out) or
+ * positions. Packed samples (d.nseq > 1; the sequence packing of the Context-Parallel page's
+ * ByteScale section): the split is that of the packed sequence, and a query sees only keys of its
+ * own sample, so tiles across sample boundaries are skipped. Scores are scale * <q, k>; inputs bf16 (tensor cores, fp32 accumulation, bf16 out) or
  * fp32 (fp32 arithmetic, fp32 out). All pointers 16-byte aligned. out/lse must not overlap inputs.
  * In USP_MODE_ACCUM, out and lse are read and rewritten in place.
  */

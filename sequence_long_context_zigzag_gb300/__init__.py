@@ -181,8 +181,10 @@ def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=Non
 
 def usp_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
                  causal: bool = True, scale: Optional[float] = None, mode: int = USP_MODE_FUSED, step: int = 0,
-                 split="zigzag", ring_rank: Optional[int] = None, hkv: Optional[int] = None, stream=None):
+                 split="zigzag", ring_rank: Optional[int] = None, hkv: Optional[int] = None, cu_seqlens=None,
+                 stream=None):
     """Ring attention over all virtual ring ranks (or only ring rank ``ring_rank``'s query rows).
+    cu_seqlens: packed samples' cumulative lengths (int32, device; a query sees only its own sample).
     q/out [rd][ud][hq/ud][bs][Lr][hd], k/v [rd][ud][hkv/ud][bs][Lr][hd], lse [rd][ud][hq/ud][bs][Lr] fp32.
     Replicated K/V (hkv < ud): k/v [rd][ud][1][bs][Lr][hd] and ``hkv`` gives the global KV head count
     (default: k's heads per rank times ud)."""
@@ -197,9 +199,10 @@ def usp_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.T
     L = Lr * rd
     hkv = Hkl * ud if hkv is None else int(hkv)
     _need(hkv > 0 and heads_per_rank(hkv, ud) == Hkl, "k/v heads per rank do not match hkv and ud")
+    nseq, cu = _packed(cu_seqlens, L, q.device)
     d = UspAttnDesc(bs, L, Hl * ud, hkv, hd, rd, ud, _dtype_code(q), int(bool(causal)),
                     float(scale) if scale is not None else 0.0, int(mode), int(step), _split_code(split),
-                    0 if ring_rank is None else int(ring_rank) + 1)
+                    0 if ring_rank is None else int(ring_rank) + 1, nseq, cu)
     _abi.check("usp_attn_fwd", _abi.load().usp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d,
                                                        _stream(stream)))
     return out, lse
@@ -226,7 +229,7 @@ def usp_check(stream=None) -> None:
 
 def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd: int, causal: bool = True,
                   scale: Optional[float] = None, head_chunk: Optional[int] = None, natural_output: bool = True,
-                  split="zigzag", stream=None):
+                  split="zigzag", cu_seqlens=None, stream=None):
     """USP-Attention forward (Algorithm 1 of the USP review) over a virtual ud x rd grid on one GPU.
 
     q: (bs, L, hq, hd), k/v: (bs, L, hkv, hd) CUDA tensors in natural token order. For every head group
@@ -253,7 +256,7 @@ def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd
         out = torch.empty(bs, L, hq, hd, device=dev, dtype=dt)
         lse = torch.empty(bs, L, hq, device=dev, dtype=torch.float32)
         usp_forward(q, k, v, out, lse, ud, rd, causal=causal, scale=scale, head_chunk=head_chunk, split=split,
-                    stream=stream)
+                    cu_seqlens=cu_seqlens, stream=stream)
         return out, lse
     out = torch.empty(rd, ud, bs, Lu, hq, hd, device=dev, dtype=dt)
     lse = torch.empty(rd, ud, bs, Lu, hq, device=dev, dtype=torch.float32)
@@ -269,18 +272,33 @@ def usp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ud: int, rd
         usp_extract_a2a([q, k, v], [qh, kh, vh], rd, ud, h0s=[g0, gk, gk], Hs=[hc, hkc, hkc], split=split,
                         stream=stream)
         # a3 + a4: the ring with the fused LSE merge
-        usp_attn_fwd(qh, kh, vh, oh, lh, causal=causal, scale=scale, split=split, hkv=hkc, stream=stream)
+        usp_attn_fwd(qh, kh, vh, oh, lh, causal=causal, scale=scale, split=split, hkv=hkc, cu_seqlens=cu_seqlens,
+                     stream=stream)
         # a5 on out and lse: back to the sequence-sharded layout a model keeps
         usp_a2a4d(oh, out, rd, ud, -1, h0=g0, H=hc, stream=stream)
         usp_a2a4d(lh, lse, rd, ud, -1, h0=g0, H=hc, stream=stream)
     return out, lse
 
 
-def _forward_desc(q, k, ud, rd, causal, scale, split="zigzag"):
+def _packed(cu_seqlens, L, device):
+    """(nseq, device pointer) of packed samples' cumulative lengths (int32 on the tensors' device)."""
+    if cu_seqlens is None:
+        return 0, None
+    _need(isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.dtype == torch.int32 and cu_seqlens.dim() == 1
+          and cu_seqlens.is_contiguous() and cu_seqlens.device == device,
+          "cu_seqlens must be a contiguous 1-D int32 tensor on the tensors' device")
+    n = cu_seqlens.numel() - 1
+    _need(n >= 1 and n <= L, "cu_seqlens needs 2 to L + 1 entries")
+    return n, cu_seqlens.data_ptr()
+
+
+def _forward_desc(q, k, ud, rd, causal, scale, split="zigzag", cu_seqlens=None):
     bs, L, hq, hd = q.shape
     hkv = k.shape[2]
+    nseq, cu = _packed(cu_seqlens, L, q.device)
     return UspAttnDesc(bs, L, hq, hkv, hd, rd, ud, _dtype_code(q), int(bool(causal)),
-                       float(scale) if scale is not None else 0.0, USP_MODE_FUSED, 0, _split_code(split), 0)
+                       float(scale) if scale is not None else 0.0, USP_MODE_FUSED, 0, _split_code(split), 0,
+                       nseq, cu)
 
 
 def usp_forward_workspace_size(q, k, ud: int, rd: int, head_chunk: Optional[int] = None, host: bool = False,
@@ -303,11 +321,12 @@ def _check_natural(q, k, v, out, lse):
 
 def usp_forward(q, k, v, out, lse, ud: int, rd: int, causal: bool = True, scale: Optional[float] = None,
                 head_chunk: Optional[int] = None, workspace: Optional[torch.Tensor] = None, split="zigzag",
-                stream=None):
-    """The whole forward on device buffers in one C call (natural-order in and out)."""
+                cu_seqlens=None, stream=None):
+    """The whole forward on device buffers in one C call (natural-order in and out). cu_seqlens:
+    packed samples' cumulative lengths (int32 on the device), each sample attending only within itself."""
     _dev(q, k, v, out, lse)
     _check_natural(q, k, v, out, lse)
-    d = _forward_desc(q, k, ud, rd, causal, scale, split)
+    d = _forward_desc(q, k, ud, rd, causal, scale, split, cu_seqlens)
     n = usp_forward_workspace_size(q, k, ud, rd, head_chunk, host=False, causal=causal)
     if workspace is None:
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device)

@@ -41,7 +41,8 @@ class UspAttnDesc(ctypes.Structure):
     _fields_ = [("bs", ctypes.c_int64), ("L", ctypes.c_int64), ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32),
                 ("hd", ctypes.c_int32), ("rd", ctypes.c_int32), ("ud", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("causal", ctypes.c_int32), ("scale", ctypes.c_float), ("mode", ctypes.c_int32),
-                ("step", ctypes.c_int32), ("split", ctypes.c_int32), ("ring_rank_only", ctypes.c_int32)]
+                ("step", ctypes.c_int32), ("split", ctypes.c_int32), ("ring_rank_only", ctypes.c_int32),
+                ("nseq", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p)]
 
 
 class UspError(RuntimeError):

@@ -21,6 +21,8 @@ struct AttnK {
     uint32_t nrows, bs, Lr, c, rd, ud, Hl, Hkl, G;
     int causal, mode, step, split, ring_rank_only;
     float scale_log2;  // softmax scale * log2(e)
+    const int32_t *cu;  // packed samples, or nullptr
+    uint32_t nseq;
     FastDiv f_Lr, f_bs, f_Hl, f_ud;
 };
 
@@ -70,6 +72,9 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnK p) {
     if (p.ring_rank_only > 0 && r != (uint32_t)(p.ring_rank_only - 1)) return;
     const int64_t qpos = split_pos(p.split, r, pq, p.c, p.rd);
     const uint32_t kh = h / p.G;
+    // packed samples: the keys of the query's own sample [sa, se) only
+    uint32_t sa = 0, se = p.Lr * p.rd;
+    if (p.cu) sample_bounds(p.cu, p.nseq, (uint32_t)qpos, p.Lr * p.rd, sa, se);
 
     float qv[EPL], acc[EPL];
     Lane<T, EPL>::load(static_cast<const T *>(p.q) + (size_t)row * HD + lane * EPL, qv);
@@ -84,11 +89,14 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnK p) {
     const int t_end = p.mode == USP_MODE_FUSED ? (int)p.rd : p.step + 1;
     for (int t = t_begin; t < t_end; ++t) {
         const uint32_t s = (r + p.rd - (uint32_t)t) % p.rd;
-        const int64_t nvis = p.causal ? split_visible(p.split, qpos, s, p.c, p.rd) : (int64_t)p.Lr;
+        // visible keys of rank s's block: a range of rows (every split's position map increases)
+        const int64_t j0 = sa > 0 ? split_visible(p.split, (int64_t)sa - 1, s, p.c, p.rd) : 0;
+        const int64_t nvis = p.causal ? split_visible(p.split, qpos, s, p.c, p.rd)
+                                      : split_visible(p.split, (int64_t)se - 1, s, p.c, p.rd);
         const size_t kv_row0 = ((((size_t)s * p.ud + u) * p.Hkl + kh) * p.bs + b) * p.Lr;
         const T *kp = static_cast<const T *>(p.k) + kv_row0 * HD + lane * EPL;
         const T *vp = static_cast<const T *>(p.v) + kv_row0 * HD + lane * EPL;
-        for (int64_t j = 0; j < nvis; ++j) {
+        for (int64_t j = j0; j < nvis; ++j) {
             float kv[EPL], vv[EPL];
             Lane<T, EPL>::load(kp + j * HD, kv);
             Lane<T, EPL>::load(vp + j * HD, vv);
@@ -164,6 +172,8 @@ int launch_attn_simt(const AttnArgs &a, cudaStream_t s) {
     k.split = a.split;
     k.ring_rank_only = a.ring_rank_only;
     k.scale_log2 = a.scale * 1.4426950408889634f;
+    k.cu = a.cu;
+    k.nseq = (uint32_t)a.nseq;
     k.f_Lr = FastDiv(k.Lr);
     k.f_bs = FastDiv(k.bs);
     k.f_Hl = FastDiv(k.Hl);

@@ -106,6 +106,8 @@ struct TcParams {
     uint32_t bs, Lr, c, rd, ud, Hl, Hkl, G, npairs;
     int causal, mode, step, lpt, split, ring_rank_only;
     float scale_log2;
+    const int32_t *cu;  // packed samples' cumulative lengths, or nullptr
+    uint32_t nseq, L;
 };
 
 // The work of one CTA and the walk over its KV tiles (identical in every role). Positions and row
@@ -116,6 +118,8 @@ struct Work {
     uint32_t q0[2];       // first local row of each Q tile
     bool valid[2];
     uint32_t qpos_min[2], qpos_max[2];
+    uint32_t sa_first[2], sa_last[2];  // sample start of the tile's first / last row (0 unless packed)
+    uint32_t se_first[2], se_last[2];  // sample end (one past) of the first / last row (L unless packed)
     int t_begin, t_end;
 };
 
@@ -126,12 +130,18 @@ struct Tile {
     bool full[2];     // every key of the tile is visible to every row of the Q tile
 };
 
+// Per ring step, the keys of rank s's block visible to a row form a range of its rows [lo, hi)
+// (every split's position map increases with the row; packed samples cut the range at the row's
+// sample start). Over the rows of a Q tile both ends are non-decreasing, so the tile's first and last
+// rows bound them: lomin / lomax are the first / last row's lo, nlo / nhi their hi.
 struct TileIter {
     int t;
     uint32_t kt, nkt, s;
     uint32_t nhi[2], nlo[2];
+    uint32_t lomin[2], lomax[2];
 };
 
+template <bool PK>
 __device__ __forceinline__ Work decode_work(const TcParams &p) {
     Work w;
     uint32_t x = blockIdx.x;
@@ -173,49 +183,82 @@ __device__ __forceinline__ Work decode_work(const TcParams &p) {
         const uint32_t last = min(w.q0[i] + 127, p.Lr - 1);
         w.qpos_min[i] = pos32(p.split, w.r, min(w.q0[i], p.Lr - 1), p.c, p.rd);
         w.qpos_max[i] = pos32(p.split, w.r, last, p.c, p.rd);
+        w.sa_first[i] = w.sa_last[i] = 0;
+        w.se_first[i] = w.se_last[i] = p.L;
+        if constexpr (PK) {
+            sample_bounds(p.cu, p.nseq, w.qpos_min[i], p.L, w.sa_first[i], w.se_first[i]);
+            sample_bounds(p.cu, p.nseq, w.qpos_max[i], p.L, w.sa_last[i], w.se_last[i]);
+        }
     }
     w.t_begin = p.mode == USP_MODE_FUSED ? 0 : p.step;
     w.t_end = p.mode == USP_MODE_FUSED ? (int)p.rd : p.step + 1;
     return w;
 }
 
+template <bool PK>
 __device__ __forceinline__ void iter_setup(const TcParams &p, const Work &w, TileIter &it) {
     it.s = (w.r + p.rd - (uint32_t)it.t) % p.rd;
-    uint32_t mx = 0;
+    uint32_t mx = 0, mn = 0xffffffffu;
     for (int i = 0; i < 2; ++i) {
         if (!w.valid[i]) {
             it.nhi[i] = 0;
             it.nlo[i] = 0;
-        } else if (p.causal) {
+            it.lomin[i] = 0;
+            it.lomax[i] = 0;
+            continue;
+        }
+        if (p.causal) {
             it.nhi[i] = vis32(p.split, w.qpos_max[i], it.s, p.c, p.rd);
             it.nlo[i] = vis32(p.split, w.qpos_min[i], it.s, p.c, p.rd);
         } else {
-            it.nhi[i] = p.Lr;
-            it.nlo[i] = p.Lr;
+            it.nhi[i] = PK ? before32(p.split, w.se_last[i], it.s, p.c, p.rd) : p.Lr;
+            it.nlo[i] = PK ? before32(p.split, w.se_first[i], it.s, p.c, p.rd) : p.Lr;
         }
-        mx = max(mx, it.nhi[i]);
+        it.lomin[i] = PK ? before32(p.split, w.sa_first[i], it.s, p.c, p.rd) : 0u;
+        it.lomax[i] = PK ? before32(p.split, w.sa_last[i], it.s, p.c, p.rd) : 0u;
+        if (it.nhi[i] > it.lomin[i]) {
+            mx = max(mx, it.nhi[i]);
+            mn = min(mn, it.lomin[i]);
+        }
     }
     it.nkt = (uint32_t)((mx + kN - 1) / kN);
-    it.kt = 0;
+    it.kt = mn == 0xffffffffu ? it.nkt : mn / kN;
 }
 
+template <bool PK>
 __device__ __forceinline__ void iter_init(const TcParams &p, const Work &w, TileIter &it) {
     it.t = w.t_begin;
-    iter_setup(p, w, it);
+    iter_setup<PK>(p, w, it);
 }
 
+// the next KV tile that at least one Q tile of the CTA needs (packed samples can leave gaps between
+// the two Q tiles' key ranges; every role skips the same tiles)
+template <bool PK>
 __device__ __forceinline__ bool iter_next(const TcParams &p, const Work &w, TileIter &it, Tile &tl) {
-    while (it.kt >= it.nkt) {
-        if (++it.t >= w.t_end) return false;
-        iter_setup(p, w, it);
+    for (;;) {
+        while (it.kt >= it.nkt) {
+            if (++it.t >= w.t_end) return false;
+            iter_setup<PK>(p, w, it);
+        }
+        if constexpr (PK) {
+            for (int i = 0; i < 2; ++i) {
+                tl.act[i] = it.kt * kN < it.nhi[i] && (it.kt + 1) * kN > it.lomin[i];
+                tl.full[i] = (it.kt + 1) * kN <= it.nlo[i] && it.kt * kN >= it.lomax[i];
+            }
+            if (tl.act[0] || tl.act[1]) break;
+            ++it.kt;
+        } else {
+            // one sample: the key ranges start at row 0 and the Q tile with the larger range is active
+            for (int i = 0; i < 2; ++i) {
+                tl.act[i] = it.kt * kN < it.nhi[i];
+                tl.full[i] = (it.kt + 1) * kN <= it.nlo[i];
+            }
+            break;
+        }
     }
     tl.s = it.s;
     tl.kt = it.kt;
     tl.kv_row = (((it.s * p.ud + w.u) * p.Hkl + w.kh) * p.bs + w.b) * p.Lr + it.kt * kN;
-    for (int i = 0; i < 2; ++i) {
-        tl.act[i] = it.kt * kN < it.nhi[i];
-        tl.full[i] = (it.kt + 1) * kN <= it.nlo[i];
-    }
     ++it.kt;
     return true;
 }
@@ -225,7 +268,7 @@ __device__ __forceinline__ bool iter_next(const TcParams &p, const Work &w, Tile
 // ------------------------------------------------------------------------------------------------
 // One thread issues every copy: Q0 and Q1 once, then for each KV tile K into a K stage and V into a
 // V stage, each waiting only for its own stage to be released.
-template <int HD>
+template <int HD, bool PK>
 __device__ void producer_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0) {
     using C = Cfg<HD>;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
@@ -240,10 +283,10 @@ __device__ void producer_role(const TcParams &p, const Work &w, uint32_t sbase, 
                             (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
     uint32_t kfills = 0, vfills = 0;  // stage fills issued
     TileIter it;
-    iter_init(p, w, it);
+    iter_init<PK>(p, w, it);
     Tile tl;
     bool ok = true;
-    while (ok && iter_next(p, w, it, tl)) {
+    while (ok && iter_next<PK>(p, w, it, tl)) {
         const uint32_t st = kfills % C::kStages;
         const uint32_t ph = ((kfills / C::kStages) & 1u) ^ 1u;
         if (!(ok = wait(C::K_EMPTY + st, ph))) break;
@@ -305,7 +348,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 // them, and when the softmax sees S_i(j+1) complete, PV_i(j) is complete too (which makes its
 // in-place rescale of O_i safe). The tcgen05 fence follows only the wait on the softmax threads' P
 // (TMA completion is ordered by the mbarrier).
-template <int HD>
+template <int HD, bool PK>
 __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0, uint32_t tmem, int i) {
     using C = Cfg<HD>;
     auto BAR = [&](int k) { return bar0 + 8u * k; };
@@ -328,9 +371,9 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
     auto take_turn = [&]() { return wait(my_turn, (turns++) & 1u); };
     bool ok = wait(C::Q_FULL, 0);
     TileIter it;
-    iter_init(p, w, it);
+    iter_init<PK>(p, w, it);
     Tile cur, nxt;
-    bool have = ok && iter_next(p, w, it, cur);
+    bool have = ok && iter_next<PK>(p, w, it, cur);
     uint32_t pc = 0, started = 0;
     uint32_t j = 0;
     if (have) {
@@ -346,7 +389,7 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
         }
     }
     while (ok && have) {
-        const bool have_n = iter_next(p, w, it, nxt);
+        const bool have_n = iter_next<PK>(p, w, it, nxt);
         const uint32_t st = j % C::kStages, ph = (j / C::kStages) & 1u;
         const uint32_t stn = (j + 1) % C::kStages, phn = ((j + 1) / C::kStages) & 1u;
         const bool act = i ? cur.act[1] : cur.act[0];
@@ -391,6 +434,13 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&r)[32], int col0, int lim_
 #pragma unroll
     for (int e = 0; e < 32; ++e)
         if (col0 + e >= lim_local) r[e] = __float_as_uint(-INFINITY);
+}
+
+// packed samples: columns outside the row's visible range [lo_local, lim_local) get score -inf
+__device__ __forceinline__ void mask_chunk2(uint32_t (&r)[32], int col0, int lo_local, int lim_local) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        if (col0 + e >= lim_local || col0 + e < lo_local) r[e] = __float_as_uint(-INFINITY);
 }
 
 __device__ __forceinline__ float chunk_max(const uint32_t (&r)[32]) {
@@ -462,7 +512,7 @@ __device__ __forceinline__ bool pair_sync_and(int i, bool v) {
 // A failed (timed-out) wait in any warp is passed on through the same exchange (a barrier that ANDs
 // the threads' results), so every warp of the tile leaves the loop at the same KV tile and none is
 // left waiting at the barrier.
-template <int HD>
+template <int HD, bool PK>
 __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem, int i, int hf,
                              float *xch) {
     using C = Cfg<HD>;
@@ -481,6 +531,8 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     const uint32_t row_local = q0 + row;
     const bool row_ok = valid && row_local < p.Lr;
     const uint32_t qpos_row = pos32(p.split, w.r, min(row_local, p.Lr - 1), p.c, p.rd);
+    uint32_t sa_row = 0, se_row = p.L;  // the row's sample (packed sequences)
+    if constexpr (PK) sample_bounds(p.cu, p.nseq, qpos_row, p.L, sa_row, se_row);
     const float sl2 = p.scale_log2;
     const uint64_t sl22 = tc::pack2(sl2, sl2);
     // exchange slots of this tile: maxima [parity][warpgroup][row], then row sums [warpgroup][row]
@@ -490,17 +542,19 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     uint32_t n_act = 0;
     bool ok = true;
     TileIter it;
-    iter_init(p, w, it);
+    iter_init<PK>(p, w, it);
     Tile tl;
     uint32_t s_cur = 0xffffffffu;
-    uint32_t lim = 0;
-    while (iter_next(p, w, it, tl)) {
+    uint32_t lim = 0, lim_lo = 0;
+    while (iter_next<PK>(p, w, it, tl)) {
         const bool act = i ? tl.act[1] : tl.act[0];
         if (!act) continue;
         const bool full = i ? tl.full[1] : tl.full[0];
         if (tl.s != s_cur) {
             s_cur = tl.s;
-            lim = p.causal ? vis32(p.split, qpos_row, s_cur, p.c, p.rd) : p.Lr;
+            lim = p.causal ? vis32(p.split, qpos_row, s_cur, p.c, p.rd)
+                           : (PK ? before32(p.split, se_row, s_cur, p.c, p.rd) : p.Lr);
+            if constexpr (PK) lim_lo = before32(p.split, sa_row, s_cur, p.c, p.rd);
         }
         ok = tc::mbar_wait(barS, n_act & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
@@ -514,8 +568,14 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
             if (!full) {
                 const int ll = (int)lim - (int)(tl.kt * kN);
                 const int lim_local = ll < 0 ? 0 : (ll > kN ? kN : ll);
+                if constexpr (PK) {
+                    const int lo_local = (int)lim_lo - (int)(tl.kt * kN);
 #pragma unroll
-                for (int cc = 0; cc < kCh; ++cc) mask_chunk(sr[cc], (hf * kCh + cc) * 32, lim_local);
+                    for (int cc = 0; cc < kCh; ++cc) mask_chunk2(sr[cc], (hf * kCh + cc) * 32, lo_local, lim_local);
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < kCh; ++cc) mask_chunk(sr[cc], (hf * kCh + cc) * 32, lim_local);
+                }
             }
 #pragma unroll
             for (int cc = 0; cc < kCh; ++cc) mx = fmaxf(mx, chunk_max(sr[cc]));
@@ -635,7 +695,7 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     if (row_ok && hf == 0) p.lse[grow] = lse_out;
 }
 
-template <int HD>
+template <int HD, bool PK>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -683,24 +743,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const bool skip = *skip_flag != 0;
-    const Work w = decode_work(p);
+    const Work w = decode_work<PK>(p);
 
     if (warp >= kSoftmaxWarps) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
         if (!skip) {
             if (warp == kProducerWarp && lane == 0)
-                producer_role<HD>(p, w, sbase, bar0);
+                producer_role<HD, PK>(p, w, sbase, bar0);
             else if (warp == kMmaWarp && lane == 0)
-                mma_role<HD>(p, w, sbase, bar0, tmem, 0);
+                mma_role<HD, PK>(p, w, sbase, bar0, tmem, 0);
             else if (warp == kMmaWarp1 && lane == 0)
-                mma_role<HD>(p, w, sbase, bar0, tmem, 1);
+                mma_role<HD, PK>(p, w, sbase, bar0, tmem, 1);
             __syncwarp();
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         // warpgroup g: Q tile g / kSplit, column share g % kSplit
         const int g = warp >> 2;
-        if (!skip) softmax_role<HD>(p, w, bar0, tmem, g / kSplit, g % kSplit, reinterpret_cast<float *>(smem + C::kXch));
+        if (!skip) softmax_role<HD, PK>(p, w, bar0, tmem, g / kSplit, g % kSplit, reinterpret_cast<float *>(smem + C::kXch));
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -713,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 // ------------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------------
-template <int HD>
+template <int HD, bool PK>
 int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
     using C = Cfg<HD>;
     static bool attr_set[64] = {};
@@ -723,15 +783,15 @@ int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
         // setmaxnreg.inc can only be granted from registers the launch already holds: never launch a
         // build whose register count would make the warpgroup split wait forever
         cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, attn_tc_kernel<HD>) != cudaSuccess) return USP_ERR_CUDA;
+        if (cudaFuncGetAttributes(&fa, attn_tc_kernel<HD, PK>) != cudaSuccess) return USP_ERR_CUDA;
         if ((long)fa.numRegs * kThreads < 2L * kSplit * 128 * kSoftmaxRegs + 128L * kControlRegs)
             return USP_ERR_UNSUPPORTED;
-        if (cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        if (cudaFuncSetAttribute(attn_tc_kernel<HD, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
             cudaSuccess)
             return USP_ERR_CUDA;
         attr_set[dev] = true;
     }
-    attn_tc_kernel<HD><<<grid, kThreads, C::kSmemBytes, s>>>(prm);
+    attn_tc_kernel<HD, PK><<<grid, kThreads, C::kSmemBytes, s>>>(prm);
     return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA;
 }
 
@@ -766,11 +826,17 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     p.ring_rank_only = a.ring_rank_only;
     p.lpt = (p.split == USP_SPLIT_ZIGZAG && p.c % 256 == 0) ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.cu = a.cu;
+    p.nseq = (uint32_t)a.nseq;
+    p.L = (uint32_t)a.L;
     const uint64_t ranks = a.ring_rank_only > 0 ? 1 : (uint64_t)p.rd;
     const uint64_t grid = ranks * p.ud * p.Hl * p.bs * p.npairs;
     if (grid == 0) return USP_OK;
     if (grid >= (1ull << 31)) return USP_ERR_UNSUPPORTED;
-    return a.hd == 128 ? launch_typed<128>(p, (uint32_t)grid, s) : launch_typed<64>(p, (uint32_t)grid, s);
+    // packed samples run a separate instantiation, so the one-sample kernel carries none of their code
+    if (p.cu)
+        return a.hd == 128 ? launch_typed<128, true>(p, (uint32_t)grid, s) : launch_typed<64, true>(p, (uint32_t)grid, s);
+    return a.hd == 128 ? launch_typed<128, false>(p, (uint32_t)grid, s) : launch_typed<64, false>(p, (uint32_t)grid, s);
 }
 
 }  // namespace usp

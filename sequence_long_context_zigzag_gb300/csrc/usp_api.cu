@@ -173,6 +173,8 @@ static int check_attn_desc(const usp_attn_desc &d) {
     if (d.hd != 64 && d.hd != 128) return USP_ERR_UNSUPPORTED;
     if (overflow31(d.bs * d.L * (int64_t)d.hq) || overflow31(d.L)) return USP_ERR_UNSUPPORTED;
     if (!(d.scale == d.scale) || isinf(d.scale)) return USP_ERR_INVALID_ARG;
+    if (d.nseq < 0 || (d.nseq > 1 && (!d.cu_seqlens || !aligned(d.cu_seqlens, 4)))) return USP_ERR_INVALID_ARG;
+    if (d.nseq > d.L) return USP_ERR_SHAPE;
     return USP_OK;
 }
 
@@ -182,6 +184,8 @@ static AttnArgs attn_args(const usp_attn_desc &d) {
     a.dtype = d.dtype; a.causal = d.causal ? 1 : 0; a.mode = d.mode; a.step = d.step;
     a.split = d.split; a.ring_rank_only = d.ring_rank_only;
     a.scale = d.scale > 0.f ? d.scale : 1.0f / sqrtf((float)d.hd);
+    a.cu = d.nseq > 1 ? d.cu_seqlens : nullptr;
+    a.nseq = d.nseq > 1 ? d.nseq : 0;
     return a;
 }
 
@@ -203,6 +207,7 @@ int usp_attn_bwd(const void *q, const void *k, const void *v, const void *dout, 
     int rc = check_attn_desc(d);
     if (rc) return rc;
     if (d.mode != USP_MODE_FUSED || d.ring_rank_only != 0) return USP_ERR_INVALID_ARG;
+    if (d.nseq > 1) return USP_ERR_UNSUPPORTED;  // the backward of packed samples is not built yet
     if (d.bs == 0 || d.L == 0) return USP_OK;
     const void *ptrs[] = {q, k, v, dout, lse, delta, dq, dk, dv};
     for (const void *x : ptrs) {

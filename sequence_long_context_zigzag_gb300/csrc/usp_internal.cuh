@@ -68,6 +68,22 @@ __host__ __device__ __forceinline__ int64_t split_visible(int split, int64_t qpo
     return c0 + c1;
 }
 
+// Packed samples: the first and one-past-last global position [a, e) of the sample holding position
+// g, by binary search in the cumulative lengths cu[0..nseq] (read-only, in bounds for any values);
+// the result is clamped to a <= g < e <= L, so malformed lengths give odd masks but never a fault.
+__device__ __forceinline__ void sample_bounds(const int32_t *cu, uint32_t nseq, uint32_t g, uint32_t L, uint32_t &a,
+                                              uint32_t &e) {
+    uint32_t lo = 0, hi = nseq;  // the sample index lies in [lo, hi)
+    while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (__ldg(cu + mid) <= (int32_t)g) lo = mid;
+        else hi = mid;
+    }
+    const int32_t a0 = __ldg(cu + lo), e0 = __ldg(cu + lo + 1);
+    a = (a0 < 0 || (uint32_t)a0 > g) ? (a0 < 0 ? 0u : g) : (uint32_t)a0;
+    e = (e0 <= (int32_t)g) ? g + 1 : ((uint32_t)e0 > L ? L : (uint32_t)e0);
+}
+
 // per-device cached properties and the device status word address
 struct DeviceInfo {
     int sm_count;
@@ -132,6 +148,8 @@ struct AttnArgs {
     int64_t bs, L;
     int32_t hq, hkv, hd, rd, ud, dtype, causal, mode, step, split, ring_rank_only;
     float scale;
+    const int32_t *cu;  // packed samples' cumulative lengths (nseq + 1 entries), or nullptr
+    int32_t nseq;       // > 1 when packed
 };
 int launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 int launch_attn_tc(const AttnArgs &a, cudaStream_t s);

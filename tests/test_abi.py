@@ -88,7 +88,7 @@ def test_extract_rejects():
 
 def desc(**kw):
     base = dict(bs=1, L=256, hq=4, hkv=2, hd=128, rd=2, ud=2, dtype=_abi.USP_BF16, causal=1, scale=0.0,
-                mode=0, step=0, split=0, ring_rank_only=0)
+                mode=0, step=0, split=0, ring_rank_only=0, nseq=0, cu_seqlens=None)
     base.update(kw)
     return _abi.UspAttnDesc(*[base[f] for f, _ in _abi.UspAttnDesc._fields_])
 
@@ -207,3 +207,15 @@ def test_backward_workspace_size():
     n = lib.usp_backward_workspace_size(d, 0)
     assert lib.usp_backward(*([BAD] * 9), d, 0, ws, n - 1, None) == _abi.USP_ERR_INVALID_ARG
     assert lib.usp_backward(*([BAD] * 9), d, 0, BAD, n, None) == _abi.USP_ERR_ALIGN
+
+
+def test_packed_samples_rejects():
+    lib = _abi.load()
+    assert lib.usp_attn_fwd(BAD, BAD, BAD, BAD, BAD, desc(nseq=3, cu_seqlens=None), None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_attn_fwd(BAD, BAD, BAD, BAD, BAD, desc(nseq=-1), None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_attn_fwd(BAD, BAD, BAD, BAD, BAD, desc(nseq=3, cu_seqlens=0x1002), None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_attn_fwd(BAD, BAD, BAD, BAD, BAD, desc(L=256, nseq=300, cu_seqlens=0x1000), None) == \
+        _abi.USP_ERR_SHAPE
+    assert lib.usp_attn_fwd(BAD, BAD, BAD, BAD, BAD, desc(nseq=3, cu_seqlens=0x1000), None) == _abi.USP_ERR_ALIGN
+    # the backward of packed samples is not built: refused before anything runs
+    assert lib.usp_attn_bwd(*([BAD] * 9), desc(nseq=3, cu_seqlens=0x1000), None) == _abi.USP_ERR_UNSUPPORTED
