@@ -71,6 +71,12 @@ def _load():
     lib.oracle_attn_block_bwd.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, vp, i64, i32, i32, i32, dbl, i32, vp,
                                           vp, vp]
     lib.oracle_attn_block_bwd.restype = i32
+    lib.oracle_attn_bwd_direct_seg.argtypes = [vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, dbl, i32, vp, vp, vp,
+                                               i64, vp, i64, vp, vp]
+    lib.oracle_attn_bwd_direct_seg.restype = i32
+    lib.oracle_attn_block_bwd_seg.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, i64, i32, i32, i32, dbl,
+                                              i32, vp, vp, vp]
+    lib.oracle_attn_block_bwd_seg.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     _lib = lib
@@ -186,14 +192,14 @@ def attn_block(q, qpos, k, v, kpos, scale, causal=True, qseg=None, kseg=None):
     return o, lse
 
 
-def attn_direct_bwd(q, k, v, dout, scale=None, causal=True, q_rows=None, kv_from=0):
+def attn_direct_bwd(q, k, v, dout, scale=None, causal=True, q_rows=None, kv_from=0, cu_seqlens=None):
     """Gradients of direct attention's output with respect to q, k, v for an upstream gradient dout
     (the chain rule through softmax, written out in usp_oracle.c), natural token order, fp64.
 
     q, dout: (bs, L, hq, hd), k/v: (bs, L, hkv, hd), one dtype (fp32, bf16 or fp64).
     q_rows: query rows whose dq is returned (default all); kv_from: dk, dv are returned for key rows
     [kv_from, L) (default all; L for none). Returns dq (bs, len(q_rows), hq, hd),
-    dk, dv (bs, L - kv_from, hkv, hd).
+    dk, dv (bs, L - kv_from, hkv, hd). cu_seqlens: packed samples (as attn_direct).
     """
     qa, dt = _raw(q)
     ka, dk_ = _raw(k)
@@ -212,15 +218,22 @@ def attn_direct_bwd(q, k, v, dout, scale=None, causal=True, q_rows=None, kv_from
     dq = np.zeros((bs, len(rows), hq, hd), dtype=np.float64)
     dk = np.zeros((bs, nkv, hkv, hd), dtype=np.float64)
     dv = np.zeros((bs, nkv, hkv, hd), dtype=np.float64)
-    rc = _load().oracle_attn_bwd_direct(_p(qa), _p(ka), _p(va), _p(ga), dt, bs, L, hq, hkv, hd, float(scale),
-                                        int(bool(causal)), _p(rows), len(rows), _p(dq), int(kv_from), _p(dk),
-                                        _p(dv))
+    if cu_seqlens is None:
+        rc = _load().oracle_attn_bwd_direct(_p(qa), _p(ka), _p(va), _p(ga), dt, bs, L, hq, hkv, hd, float(scale),
+                                            int(bool(causal)), _p(rows), len(rows), _p(dq), int(kv_from), _p(dk),
+                                            _p(dv))
+    else:
+        st, en, _ = seg_bounds(cu_seqlens, L)
+        st, en = np.ascontiguousarray(st), np.ascontiguousarray(en)
+        rc = _load().oracle_attn_bwd_direct_seg(_p(qa), _p(ka), _p(va), _p(ga), dt, bs, L, hq, hkv, hd,
+                                                float(scale), int(bool(causal)), _p(st), _p(en), _p(rows),
+                                                len(rows), _p(dq), int(kv_from), _p(dk), _p(dv))
     if rc != 0:
         raise ValueError("oracle_attn_bwd_direct: bad arguments")
     return dq, dk, dv
 
 
-def attn_block_bwd(q, dout, qpos, lse, D, k, v, kpos, scale, causal, dq_acc, dk_acc, dv_acc):
+def attn_block_bwd(q, dout, qpos, lse, D, k, v, kpos, scale, causal, dq_acc, dk_acc, dv_acc, qseg=None, kseg=None):
     """One ring step's share of the backward, accumulated in place: dq_acc (hq, nq, hd) += the keys'
     contribution, dk_acc / dv_acc (hkv, nk, hd) += the queries' contribution, using the rows' final
     lse and D = <dout, out> (all fp64, head-sharded block layout as attn_block)."""
@@ -232,9 +245,16 @@ def attn_block_bwd(q, dout, qpos, lse, D, k, v, kpos, scale, causal, dq_acc, dk_
         assert a.dtype == np.float64 and a.flags.c_contiguous
     hq, nq, hd = q.shape
     hkv, nk, _ = k.shape
-    rc = _load().oracle_attn_block_bwd(_p(q), _p(dout), _p(qpos), _p(lse), _p(D), nq, _p(k), _p(v), _p(kpos), nk,
-                                       hq, hkv, hd, float(scale), int(bool(causal)), _p(dq_acc), _p(dk_acc),
-                                       _p(dv_acc))
+    if qseg is None:
+        rc = _load().oracle_attn_block_bwd(_p(q), _p(dout), _p(qpos), _p(lse), _p(D), nq, _p(k), _p(v), _p(kpos),
+                                           nk, hq, hkv, hd, float(scale), int(bool(causal)), _p(dq_acc), _p(dk_acc),
+                                           _p(dv_acc))
+    else:
+        qseg = np.ascontiguousarray(qseg, dtype=np.int64)
+        kseg = np.ascontiguousarray(kseg, dtype=np.int64)
+        rc = _load().oracle_attn_block_bwd_seg(_p(q), _p(dout), _p(qpos), _p(qseg), _p(lse), _p(D), nq, _p(k), _p(v),
+                                               _p(kpos), _p(kseg), nk, hq, hkv, hd, float(scale), int(bool(causal)),
+                                               _p(dq_acc), _p(dk_acc), _p(dv_acc))
     if rc != 0:
         raise ValueError("oracle_attn_block_bwd: bad arguments")
 
@@ -479,7 +499,7 @@ def literal_pipeline(q, k, v, rd, ud, scale=None, causal=True, split="zigzag", c
     return out, lse
 
 
-def literal_pipeline_bwd(q, k, v, dout, rd, ud, scale=None, causal=True, split="zigzag"):
+def literal_pipeline_bwd(q, k, v, dout, rd, ud, scale=None, causal=True, split="zigzag", cu_seqlens=None):
     """USP-Attention backward, run rank by rank over the virtual ud x rd grid, in fp64.
 
     The forward's layout changes are applied to q, k, v, the upstream gradient dout, and the
@@ -497,12 +517,14 @@ def literal_pipeline_bwd(q, k, v, dout, rd, ud, scale=None, causal=True, split="
     c, Lr, _ = _dims(L, rd, ud)
     if hq % ud or hq % hkv or (hkv % ud and ud % hkv):
         raise ValueError("hq must divide by ud and by hkv; hkv must divide by ud or divide ud")
-    o_nat, l_nat = attn_direct(q, k, v, scale=scale, causal=causal)
+    o_nat, l_nat = attn_direct(q, k, v, scale=scale, causal=causal, cu_seqlens=cu_seqlens)
     D_nat = np.einsum("blhd,blhd->blh", dout, o_nat)
     hs = lambda x: a2a_fwd(extract_local(x, rd, ud, split=split), ud)  # noqa: E731
     Q, K, V, dO = hs(q), hs(k), hs(v), hs(dout)
     LSE, DD = hs(l_nat[..., None])[..., 0], hs(D_nat[..., None])[..., 0]
     pos = [split_pos(split, r, np.arange(Lr), L, rd) for r in range(rd)]
+    seg = None if cu_seqlens is None else seg_bounds(cu_seqlens, L)[2]
+    sg = (lambda r: None) if seg is None else (lambda r: seg[pos[r]])  # noqa: E731
     dQ, dK, dV = np.zeros(Q.shape), np.zeros(K.shape), np.zeros(V.shape)
     for r in range(rd):
         for u in range(ud):
@@ -513,7 +535,8 @@ def literal_pipeline_bwd(q, k, v, dout, rd, ud, scale=None, causal=True, split="
                     dk_s = np.zeros(K[s, u, :, b].shape)
                     dv_s = np.zeros(V[s, u, :, b].shape)
                     attn_block_bwd(Q[r, u, :, b], dO[r, u, :, b], pos[r], LSE[r, u, :, b], DD[r, u, :, b],
-                                   K[s, u, :, b], V[s, u, :, b], pos[s], scale, causal, dq_r, dk_s, dv_s)
+                                   K[s, u, :, b], V[s, u, :, b], pos[s], scale, causal, dq_r, dk_s, dv_s,
+                                   sg(r), sg(s))
                     dK[s, u, :, b] += dk_s
                     dV[s, u, :, b] += dv_s
                 dQ[r, u, :, b] = dq_r

@@ -236,9 +236,25 @@ int oracle_attn_block_seg(const double *q, const int64_t *qpos, const int64_t *q
  *   mask every row does.
  * Returns 0, or -1 on a bad argument / allocation failure.
  */
+int oracle_attn_bwd_direct_seg(const void *q, const void *k, const void *v, const void *dout, int dtype,
+                               int64_t bs, int64_t L, int hq, int hkv, int hd, double scale, int causal,
+                               const int64_t *seg_start, const int64_t *seg_end, const int64_t *qrows, int64_t nq,
+                               double *dq, int64_t j0, double *dk, double *dv);
+
 int oracle_attn_bwd_direct(const void *q, const void *k, const void *v, const void *dout, int dtype,
                            int64_t bs, int64_t L, int hq, int hkv, int hd, double scale, int causal,
                            const int64_t *qrows, int64_t nq, double *dq, int64_t j0, double *dk, double *dv)
+{
+    return oracle_attn_bwd_direct_seg(q, k, v, dout, dtype, bs, L, hq, hkv, hd, scale, causal, NULL, NULL, qrows, nq,
+                                      dq, j0, dk, dv);
+}
+
+/* The same for packed samples (seg_start / seg_end of every position, as oracle_attn_direct_seg):
+ * query i and key j interact only inside one sample. */
+int oracle_attn_bwd_direct_seg(const void *q, const void *k, const void *v, const void *dout, int dtype,
+                               int64_t bs, int64_t L, int hq, int hkv, int hd, double scale, int causal,
+                               const int64_t *seg_start, const int64_t *seg_end, const int64_t *qrows, int64_t nq,
+                               double *dq, int64_t j0, double *dk, double *dv)
 {
     if (bs <= 0 || L <= 0 || hq <= 0 || hkv <= 0 || hd <= 0 || hq % hkv != 0 || nq < 0 || j0 < 0 || j0 > L)
         return -1;
@@ -276,10 +292,11 @@ int oracle_attn_bwd_direct(const void *q, const void *k, const void *v, const vo
                 const int64_t b = t / (L * hq);
                 if (!need[i]) continue;
                 const int kh = h / G;
-                const int64_t nk = causal ? i + 1 : L;
+                const int64_t ka = seg_start ? seg_start[i] : 0;
+                const int64_t nk = causal ? i + 1 : (seg_end ? seg_end[i] : L);
                 for (int d = 0; d < hd; ++d) qi[d] = widen(q, ((b * L + i) * hq + h) * hd + d, dtype);
                 double m = -INFINITY;
-                for (int64_t j = 0; j < nk; ++j) {
+                for (int64_t j = ka; j < nk; ++j) {
                     const int64_t kb = ((b * L + j) * hkv + kh) * hd;
                     double dot = 0.0;
                     for (int d = 0; d < hd; ++d) dot += qi[d] * widen(k, kb + d, dtype);
@@ -287,10 +304,10 @@ int oracle_attn_bwd_direct(const void *q, const void *k, const void *v, const vo
                     if (s[j] > m) m = s[j];
                 }
                 double sum = 0.0;
-                for (int64_t j = 0; j < nk; ++j) sum += exp(s[j] - m);
+                for (int64_t j = ka; j < nk; ++j) sum += exp(s[j] - m);
                 const double l = m + log(sum);
                 for (int d = 0; d < hd; ++d) o[d] = 0.0;
-                for (int64_t j = 0; j < nk; ++j) {
+                for (int64_t j = ka; j < nk; ++j) {
                     const double p = exp(s[j] - l);
                     const int64_t vb = ((b * L + j) * hkv + kh) * hd;
                     for (int d = 0; d < hd; ++d) o[d] += p * widen(v, vb + d, dtype);
@@ -322,14 +339,15 @@ int oracle_attn_bwd_direct(const void *q, const void *k, const void *v, const vo
                     const int64_t b = t / ((int64_t)hq * nq);
                     const int64_t i = qrows[ri];
                     const int kh = h / G;
-                    const int64_t nk = causal ? i + 1 : L;
+                    const int64_t ka = seg_start ? seg_start[i] : 0;
+                    const int64_t nk = causal ? i + 1 : (seg_end ? seg_end[i] : L);
                     const double l = lse[(b * hq + h) * L + i], di = D[(b * hq + h) * L + i];
                     for (int d = 0; d < hd; ++d) {
                         qi[d] = widen(q, ((b * L + i) * hq + h) * hd + d, dtype);
                         gi[d] = widen(dout, ((b * L + i) * hq + h) * hd + d, dtype);
                         acc[d] = 0.0;
                     }
-                    for (int64_t j = 0; j < nk; ++j) {
+                    for (int64_t j = ka; j < nk; ++j) {
                         const int64_t kb = ((b * L + j) * hkv + kh) * hd;
                         double dot = 0.0, dp = 0.0;
                         for (int d = 0; d < hd; ++d) {
@@ -374,7 +392,9 @@ int oracle_attn_bwd_direct(const void *q, const void *k, const void *v, const vo
                         av[d] = 0.0;
                     }
                     for (int h = kh * G; h < (kh + 1) * G; ++h) {
-                        for (int64_t i = causal ? j : 0; i < L; ++i) {
+                        const int64_t ib = causal ? j : (seg_start ? seg_start[j] : 0);
+                        const int64_t ie = seg_end ? seg_end[j] : L;
+                        for (int64_t i = ib; i < ie; ++i) {
                             const int64_t qb = ((b * L + i) * hq + h) * hd;
                             double dot = 0.0, dp = 0.0;
                             for (int d = 0; d < hd; ++d) {
@@ -414,10 +434,25 @@ int oracle_attn_bwd_direct(const void *q, const void *k, const void *v, const vo
  *   k, v: (hkv, nk, hd) fp64, kpos[nk]
  *   dq_acc (hq, nq, hd) += ...;  dk_acc, dv_acc (hkv, nk, hd) += ...
  */
+int oracle_attn_block_bwd_seg(const double *q, const double *dout, const int64_t *qpos, const int64_t *qseg,
+                              const double *lse, const double *D, int64_t nq, const double *k, const double *v,
+                              const int64_t *kpos, const int64_t *kseg, int64_t nk, int hq, int hkv, int hd,
+                              double scale, int causal, double *dq_acc, double *dk_acc, double *dv_acc);
+
 int oracle_attn_block_bwd(const double *q, const double *dout, const int64_t *qpos, const double *lse,
                           const double *D, int64_t nq, const double *k, const double *v, const int64_t *kpos,
                           int64_t nk, int hq, int hkv, int hd, double scale, int causal, double *dq_acc,
                           double *dk_acc, double *dv_acc)
+{
+    return oracle_attn_block_bwd_seg(q, dout, qpos, NULL, lse, D, nq, k, v, kpos, NULL, nk, hq, hkv, hd, scale, causal,
+                                     dq_acc, dk_acc, dv_acc);
+}
+
+/* ... with the sample index of every query and key: pairs from different samples do not interact. */
+int oracle_attn_block_bwd_seg(const double *q, const double *dout, const int64_t *qpos, const int64_t *qseg,
+                              const double *lse, const double *D, int64_t nq, const double *k, const double *v,
+                              const int64_t *kpos, const int64_t *kseg, int64_t nk, int hq, int hkv, int hd,
+                              double scale, int causal, double *dq_acc, double *dk_acc, double *dv_acc)
 {
     if (nq < 0 || nk < 0 || hq <= 0 || hkv <= 0 || hd <= 0 || hq % hkv != 0) return -1;
     const int G = hq / hkv;
@@ -431,6 +466,7 @@ int oracle_attn_block_bwd(const double *q, const double *dout, const int64_t *qp
         double *acc = dq_acc + ((int64_t)h * nq + i) * hd;
         for (int64_t j = 0; j < nk; ++j) {
             if (causal && kpos[j] > qpos[i]) continue;
+            if (qseg && qseg[i] != kseg[j]) continue;
             const double *kj = k + ((int64_t)kh * nk + j) * hd;
             const double *vj = v + ((int64_t)kh * nk + j) * hd;
             double dot = 0.0, dp = 0.0;
@@ -454,6 +490,7 @@ int oracle_attn_block_bwd(const double *q, const double *dout, const int64_t *qp
         for (int h = kh * G; h < (kh + 1) * G; ++h) {
             for (int64_t i = 0; i < nq; ++i) {
                 if (causal && kpos[j] > qpos[i]) continue;
+                if (qseg && qseg[i] != kseg[j]) continue;
                 const double *qi = q + ((int64_t)h * nq + i) * hd;
                 const double *gi = dout + ((int64_t)h * nq + i) * hd;
                 double dot = 0.0, dp = 0.0;

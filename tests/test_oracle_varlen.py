@@ -57,3 +57,31 @@ def test_bad_cu_seqlens(cu):
     q, k, v = make_qkv(1, 48, 2, 2, 4, "f32", seed=1)
     with pytest.raises(ValueError):
         oracle.attn_direct(q, k, v, cu_seqlens=cu)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("cu", [[0, 10, 30, 48], [0, 1, 2, 47, 48], [0, 48]])
+def test_packed_grads_equal_samples_one_by_one(causal, cu):
+    q, k, v = make_qkv(1, 48, 4, 2, 4, "f32", seed=11 + len(cu))
+    g, _, _ = make_qkv(1, 48, 4, 2, 4, "f32", seed=99)
+    dq, dk, dv = oracle.attn_direct_bwd(q, k, v, g, scale=0.5, causal=causal, cu_seqlens=cu)
+    parts = [oracle.attn_direct_bwd(q[:, a:b], k[:, a:b], v[:, a:b], g[:, a:b], scale=0.5, causal=causal)
+             for a, b in zip(cu[:-1], cu[1:])]
+    for got, i in ((dq, 0), (dk, 1), (dv, 2)):
+        np.testing.assert_allclose(got, np.concatenate([p[i] for p in parts], 1), atol=1e-13)
+    # restricted rows agree with the full call
+    rows = np.array([0, 9, 10, 47])
+    dq_r, dk_t, _ = oracle.attn_direct_bwd(q, k, v, g, scale=0.5, causal=causal, cu_seqlens=cu, q_rows=rows,
+                                           kv_from=40)
+    assert np.array_equal(dq_r, dq[:, rows]) and np.array_equal(dk_t, dk[:, 40:])
+
+
+@pytest.mark.parametrize("split", ["zigzag", "basic", "stripe"])
+@pytest.mark.parametrize("L,rd,ud,hkv,cu", [(48, 3, 2, 2, [0, 7, 20, 21, 48]), (32, 2, 4, 1, [0, 3, 30, 32])])
+def test_literal_ring_bwd_packed_equals_direct(split, L, rd, ud, hkv, cu):
+    q, k, v = make_qkv(1, L, 4, hkv, 4, "f32", seed=L + rd)
+    g, _, _ = make_qkv(1, L, 4, hkv, 4, "f32", seed=L + rd + 500)
+    dq, dk, dv = oracle.attn_direct_bwd(q, k, v, g, cu_seqlens=cu)
+    lq, lk, lv = oracle.literal_pipeline_bwd(q, k, v, g, rd, ud, split=split, cu_seqlens=cu)
+    for a, b in ((lq, dq), (lk, dk), (lv, dv)):
+        np.testing.assert_allclose(a, b, atol=1e-12)
