@@ -396,7 +396,7 @@ def usp_attn_bwd_delta(out: torch.Tensor, dout: torch.Tensor, delta: torch.Tenso
 
 
 def usp_attn_bwd(q, k, v, dout, lse, delta, dq, dk, dv, causal: bool = True, scale: Optional[float] = None,
-                 split="zigzag", hkv: Optional[int] = None, stream=None):
+                 split="zigzag", hkv: Optional[int] = None, cu_seqlens=None, stream=None):
     """Backward of usp_attn_fwd (whole ring) on head-sharded buffers: q/dout/dq [rd][ud][hq/ud][bs][Lr][hd],
     k/v/dk/dv [rd][ud][Hkl][bs][Lr][hd], lse/delta [rd][ud][hq/ud][bs][Lr] fp32 (delta from
     usp_attn_bwd_delta). Replicated K/V (hkv < ud): each replica gets its own rank's share."""
@@ -413,8 +413,9 @@ def usp_attn_bwd(q, k, v, dout, lse, delta, dq, dk, dv, causal: bool = True, sca
         _need(t.shape == (rd, ud, Hl, bs, Lr) and t.dtype == torch.float32, "lse/delta must be fp32 [rd][ud][Hl][bs][Lr]")
     hkv = Hkl * ud if hkv is None else int(hkv)
     _need(hkv > 0 and heads_per_rank(hkv, ud) == Hkl, "k/v heads per rank do not match hkv and ud")
+    nseq, cu = _packed(cu_seqlens, Lr * rd, q.device)
     d = UspAttnDesc(bs, Lr * rd, Hl * ud, hkv, hd, rd, ud, _dtype_code(q), int(bool(causal)),
-                    float(scale) if scale is not None else 0.0, USP_MODE_FUSED, 0, _split_code(split), 0)
+                    float(scale) if scale is not None else 0.0, USP_MODE_FUSED, 0, _split_code(split), 0, nseq, cu)
     _abi.check("usp_attn_bwd", _abi.load().usp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse),
                                                        _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), d, _stream(stream)))
     return dq, dk, dv
@@ -430,7 +431,7 @@ def usp_backward_workspace_size(q, k, ud: int, rd: int, head_chunk: Optional[int
 
 def usp_backward(q, k, v, out, lse, dout, dq, dk, dv, ud: int, rd: int, causal: bool = True,
                  scale: Optional[float] = None, head_chunk: Optional[int] = None,
-                 workspace: Optional[torch.Tensor] = None, split="zigzag", stream=None):
+                 workspace: Optional[torch.Tensor] = None, split="zigzag", cu_seqlens=None, stream=None):
     """The whole backward on device buffers in one C call (natural order in and out): dq, dk, dv of
     the forward's out for the upstream gradient dout, given the forward's out and lse."""
     _dev(q, k, v, out, lse, dout, dq, dk, dv)
@@ -439,7 +440,7 @@ def usp_backward(q, k, v, out, lse, dout, dq, dk, dv, ud: int, rd: int, causal: 
           "gradient shapes must match their inputs")
     for t in (dout, dq, dk, dv):
         _need(t.dtype == q.dtype and t.is_contiguous(), "gradients must be contiguous and of q's dtype")
-    d = _forward_desc(q, k, ud, rd, causal, scale, split)
+    d = _forward_desc(q, k, ud, rd, causal, scale, split, cu_seqlens)
     n = usp_backward_workspace_size(q, k, ud, rd, head_chunk, causal=causal)
     if workspace is None:
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
@@ -455,23 +456,24 @@ class UspAttentionFunction(torch.autograd.Function):
     order, with gradients for q, k and v (lse is saved for the backward, not differentiated)."""
 
     @staticmethod
-    def forward(ctx, q, k, v, ud, rd, causal=True, scale=None, head_chunk=None, split="zigzag"):
+    def forward(ctx, q, k, v, ud, rd, causal=True, scale=None, head_chunk=None, split="zigzag", cu_seqlens=None):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
         out = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
-        usp_forward(q, k, v, out, lse, ud, rd, causal=causal, scale=scale, head_chunk=head_chunk, split=split)
+        usp_forward(q, k, v, out, lse, ud, rd, causal=causal, scale=scale, head_chunk=head_chunk, split=split,
+                    cu_seqlens=cu_seqlens)
         ctx.save_for_backward(q, k, v, out, lse)
-        ctx.cfg = (ud, rd, causal, scale, head_chunk, split)
+        ctx.cfg = (ud, rd, causal, scale, head_chunk, split, cu_seqlens)
         return out
 
     @staticmethod
     def backward(ctx, dout):
         q, k, v, out, lse = ctx.saved_tensors
-        ud, rd, causal, scale, head_chunk, split = ctx.cfg
+        ud, rd, causal, scale, head_chunk, split, cu_seqlens = ctx.cfg
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         usp_backward(q, k, v, out, lse, dout.contiguous(), dq, dk, dv, ud, rd, causal=causal, scale=scale,
-                     head_chunk=head_chunk, split=split)
-        return dq, dk, dv, None, None, None, None, None, None
+                     head_chunk=head_chunk, split=split, cu_seqlens=cu_seqlens)
+        return dq, dk, dv, None, None, None, None, None, None, None
 
 
 class UspAttention:

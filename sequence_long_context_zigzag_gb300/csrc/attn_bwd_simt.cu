@@ -6,10 +6,12 @@
 //   dq_i = scale sum_j dS_ij k_j,   dk_j = scale sum_i dS_ij q_i,   dv_j = sum_i P_ij dout_i,
 // over the forward's causal (query, key) pairs. Two kernels, one warp per output row each:
 //   * dq: a query row of ring rank r walks the ring in the Context-Parallel page's Fig. 1 order
-//     (step t: KV block of rank (r - t) mod rd), visible keys being a prefix of each block;
+//     (step t: KV block of rank (r - t) mod rd), its visible keys being a range of each block's rows
+//     (a prefix of it unless samples are packed);
 //   * dk/dv: a key row of rank s meets the queries of every ring rank once; those that see it are a
-//     suffix of each rank's block (every split's position map increases with the row), and the
-//     query heads of its group (or, for a replicated KV head, all of the rank's query heads) add up.
+//     range of each rank's rows (every split's position map increases with the row; a suffix unless
+//     samples are packed), and the query heads of its group (or, for a replicated KV head, all of the
+//     rank's query heads) add up.
 // In a multi-GPU ring the dk/dv partials would travel with the KV block and be home after rd steps;
 // here each key row's warp forms its whole sum.
 #include <math.h>
@@ -27,8 +29,15 @@ struct BwdK {
     uint32_t nq_rows, nkv_rows, bs, Lr, c, rd, ud, Hl, Hkl, G;
     int causal, split;
     float scale, scale_log2;
+    const int32_t *cu;  // packed samples, or nullptr
+    uint32_t nseq;
     FastDiv f_Lr, f_bs, f_Hl, f_Hkl, f_ud;
 };
+
+// number of rank-s rows whose global position is below x (a prefix of the block)
+__device__ __forceinline__ int64_t rows_before(int split, int64_t x, int64_t s, int64_t c, int64_t rd) {
+    return x > 0 ? split_visible(split, x - 1, s, c, rd) : 0;
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -77,6 +86,8 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdK p) {
     p.f_ud.divmod(t0, r, u);
     const int64_t qpos = split_pos(p.split, r, pq, p.c, p.rd);
     const uint32_t kh = h / p.G;
+    uint32_t sa = 0, se = p.Lr * p.rd;  // the row's sample (packed sequences)
+    if (p.cu) sample_bounds(p.cu, p.nseq, (uint32_t)qpos, p.Lr * p.rd, sa, se);
     float qv[EPL], gv[EPL], acc[EPL];
     Row<T, EPL>::load(static_cast<const T *>(p.q) + (size_t)row * HD + lane * EPL, qv);
     Row<T, EPL>::load(static_cast<const T *>(p.dout) + (size_t)row * HD + lane * EPL, gv);
@@ -85,11 +96,13 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdK p) {
     const float lse2 = p.lse[row] * kLog2e, Di = p.delta[row];
     for (uint32_t t = 0; t < p.rd; ++t) {
         const uint32_t s = (r + p.rd - t) % p.rd;
-        const int64_t nvis = p.causal ? split_visible(p.split, qpos, s, p.c, p.rd) : (int64_t)p.Lr;
+        const int64_t j0 = rows_before(p.split, sa, s, p.c, p.rd);
+        const int64_t nvis = p.causal ? split_visible(p.split, qpos, s, p.c, p.rd)
+                                      : rows_before(p.split, se, s, p.c, p.rd);
         const size_t kv_row0 = ((((size_t)s * p.ud + u) * p.Hkl + kh) * p.bs + b) * p.Lr;
         const T *kp = static_cast<const T *>(p.k) + kv_row0 * HD + lane * EPL;
         const T *vp = static_cast<const T *>(p.v) + kv_row0 * HD + lane * EPL;
-        for (int64_t j = 0; j < nvis; ++j) {
+        for (int64_t j = j0; j < nvis; ++j) {
             float kv[EPL], vv[EPL];
             Row<T, EPL>::load(kp + j * HD, kv);
             Row<T, EPL>::load(vp + j * HD, vv);
@@ -123,6 +136,8 @@ __global__ void __launch_bounds__(256) bwd_dkv_kernel(const BwdK p) {
     p.f_Hkl.divmod(t0, t0, kh);
     p.f_ud.divmod(t0, s, u);
     const int64_t kpos = split_pos(p.split, s, pk, p.c, p.rd);
+    uint32_t sa = 0, se = p.Lr * p.rd;  // the key's sample (packed sequences)
+    if (p.cu) sample_bounds(p.cu, p.nseq, (uint32_t)kpos, p.Lr * p.rd, sa, se);
     float kv[EPL], vv[EPL], ak[EPL], av[EPL];
     Row<T, EPL>::load(static_cast<const T *>(p.k) + (size_t)row * HD + lane * EPL, kv);
     Row<T, EPL>::load(static_cast<const T *>(p.v) + (size_t)row * HD + lane * EPL, vv);
@@ -134,13 +149,15 @@ __global__ void __launch_bounds__(256) bwd_dkv_kernel(const BwdK p) {
     // the rank's query heads that read this KV head: [kh G, kh G + G), clipped to the rank's Hl
     const uint32_t h_end = min(kh * p.G + p.G, p.Hl);
     for (uint32_t r = 0; r < p.rd; ++r) {
-        // queries of rank r that see key position kpos: those with position >= kpos, a suffix
-        const int64_t i0 = !p.causal ? 0 : (kpos > 0 ? split_visible(p.split, kpos - 1, r, p.c, p.rd) : 0);
+        // queries of rank r that see key position kpos: positions in [kpos, se) (causal) or [sa, se)
+        // of the key's sample -- a range of rows
+        const int64_t i0 = rows_before(p.split, p.causal ? kpos : (int64_t)sa, r, p.c, p.rd);
+        const int64_t i1 = rows_before(p.split, se, r, p.c, p.rd);
         for (uint32_t h = kh * p.G; h < h_end; ++h) {
             const size_t q_row0 = ((((size_t)r * p.ud + u) * p.Hl + h) * p.bs + b) * p.Lr;
             const T *qp = static_cast<const T *>(p.q) + q_row0 * HD + lane * EPL;
             const T *gp = static_cast<const T *>(p.dout) + q_row0 * HD + lane * EPL;
-            for (int64_t i = i0; i < (int64_t)p.Lr; ++i) {
+            for (int64_t i = i0; i < i1; ++i) {
                 float qv[EPL], gv[EPL];
                 Row<T, EPL>::load(qp + i * HD, qv);
                 Row<T, EPL>::load(gp + i * HD, gv);
@@ -219,6 +236,8 @@ int launch_attn_bwd_simt(const BwdArgs &a, cudaStream_t s) {
     k.split = f.split;
     k.scale = f.scale;
     k.scale_log2 = f.scale * kLog2e;
+    k.cu = f.cu;
+    k.nseq = (uint32_t)f.nseq;
     k.f_Lr = FastDiv(k.Lr);
     k.f_bs = FastDiv(k.bs);
     k.f_Hl = FastDiv(k.Hl);

@@ -57,6 +57,8 @@ struct BwdTcParams {
     uint32_t bs, Lr, c, rd, ud, Hl, Hkl, G, ntiles;  // ntiles: 128-row tiles per ring-local block
     int causal, split, lpt;
     float scale, scale_log2;
+    const int32_t *cu;  // packed samples' cumulative lengths, or nullptr
+    uint32_t nseq, L;
 };
 
 template <int HD> struct Lay {
@@ -170,6 +172,7 @@ struct KvWork {
     uint32_t kv_row0;            // row of local key 0 of (s, u, kh, b) in k / v / dk / dv
     uint32_t kpos_min, kpos_max;
     uint32_t hbeg, hend;         // the rank's query heads that read this KV head
+    uint32_t sa_first, se_last;  // sample start of the first key, sample end of the last (packed)
 };
 
 __device__ __forceinline__ KvWork kv_decode(const BwdTcParams &p) {
@@ -199,21 +202,35 @@ __device__ __forceinline__ KvWork kv_decode(const BwdTcParams &p) {
     w.kpos_max = pos32(p.split, w.s, min(w.k0 + 127, p.Lr - 1), p.c, p.rd);
     w.hbeg = w.kh * p.G;
     w.hend = min(w.hbeg + p.G, p.Hl);
+    w.sa_first = 0;
+    w.se_last = p.L;
+    if (p.cu) {
+        uint32_t a, e;
+        sample_bounds(p.cu, p.nseq, w.kpos_min, p.L, w.sa_first, e);
+        sample_bounds(p.cu, p.nseq, w.kpos_max, p.L, a, w.se_last);
+    }
     return w;
 }
 
-// the Q tiles that see the CTA's keys: ring ranks r, query heads h of the group, 64-row tiles n from
-// the first row that sees the earliest key to the end of the block
+// the Q tiles that see the CTA's keys: ring ranks r, query heads h of the group, 64-row tiles n over
+// the rows of rank r that see at least one of the keys -- from the first row that sees the earliest
+// key (the first row of its sample without the causal mask) to the end of the last key's sample
+// (the end of the block unless samples are packed)
 struct QIter {
-    uint32_t r, h, n, nlo, nhi, ifull;
+    uint32_t r, h, n, nlo, nhi;
     bool done;
 };
 
+__device__ __forceinline__ void kv_query_range(const BwdTcParams &p, const KvWork &w, uint32_t r, uint32_t &nlo,
+                                               uint32_t &nhi) {
+    const uint32_t ilo = before32(p.split, p.causal ? w.kpos_min : w.sa_first, r, p.c, p.rd);
+    const uint32_t ihi = before32(p.split, w.se_last, r, p.c, p.rd);
+    nlo = ilo / kT;
+    nhi = ihi > ilo ? (ihi + kT - 1) / kT : nlo;
+}
+
 __device__ __forceinline__ void qiter_rank(const BwdTcParams &p, const KvWork &w, QIter &it) {
-    const uint32_t ilo = p.causal ? before32(p.split, w.kpos_min, it.r, p.c, p.rd) : 0u;
-    it.ifull = p.causal ? before32(p.split, w.kpos_max, it.r, p.c, p.rd) : 0u;
-    it.nlo = ilo / kT;
-    it.nhi = (p.Lr + kT - 1) / kT;
+    kv_query_range(p, w, it.r, it.nlo, it.nhi);
     it.h = w.hbeg;
     it.n = it.nlo;
 }
@@ -244,8 +261,8 @@ __device__ __forceinline__ void qiter_advance(const BwdTcParams &p, const KvWork
 __device__ __forceinline__ uint32_t kv_count_tiles(const BwdTcParams &p, const KvWork &w) {
     uint32_t n = 0;
     for (uint32_t r = 0; r < p.rd; ++r) {
-        const uint32_t ilo = p.causal ? before32(p.split, w.kpos_min, r, p.c, p.rd) : 0u;
-        const uint32_t nlo = ilo / kT, nhi = (p.Lr + kT - 1) / kT;
+        uint32_t nlo, nhi;
+        kv_query_range(p, w, r, nlo, nhi);
         if (nhi > nlo) n += (nhi - nlo) * (w.hend - w.hbeg);
     }
     return n;
@@ -357,17 +374,21 @@ __device__ void kv_softmax(const BwdTcParams &p, const KvWork &w, uint32_t bar0,
     const uint32_t j = w.k0 + row;
     const bool row_ok = j < p.Lr;
     const uint32_t kpos = pos32(p.split, w.s, min(j, p.Lr - 1), p.c, p.rd);
+    uint32_t sa = 0, se = p.L;  // the key's sample (packed sequences)
+    if (p.cu) sample_bounds(p.cu, p.nseq, kpos, p.L, sa, se);
     const float sl2 = p.scale_log2;
     const uint32_t n = kv_count_tiles(p, w);
     QIter it;
     qiter_init(p, w, it);
-    uint32_t r_cur = 0xffffffffu, i0 = 0;
+    uint32_t r_cur = 0xffffffffu, i0 = 0, i1 = 0;
     bool ok = true;
     for (uint32_t t = 0; t < n && !it.done; ++t) {
         const uint32_t st = t % C::kStages, b = t & 1u;
         if (it.r != r_cur) {
+            // the query rows of rank r that see this key: [i0, i1)
             r_cur = it.r;
-            i0 = p.causal ? before32(p.split, kpos, r_cur, p.c, p.rd) : 0u;
+            i0 = before32(p.split, p.causal ? kpos : sa, r_cur, p.c, p.rd);
+            i1 = before32(p.split, se, r_cur, p.c, p.rd);
         }
         ok = tc::mbar_wait(BAR(C::SP_FULL + b), (t >> 1) & 1u, p.status, USP_ERR_TIMEOUT, kWaitNs) &&
              tc::mbar_wait(BAR(C::QD_FULL + st), (t / C::kStages) & 1u, p.status, USP_ERR_TIMEOUT, kWaitNs);
@@ -388,10 +409,10 @@ __device__ void kv_softmax(const BwdTcParams &p, const KvWork &w, uint32_t bar0,
             l2[4 * q] = a.x; l2[4 * q + 1] = a.y; l2[4 * q + 2] = a.z; l2[4 * q + 3] = a.w;
             dd[4 * q] = d.x; dd[4 * q + 1] = d.y; dd[4 * q + 2] = d.z; dd[4 * q + 3] = d.w;
         }
-        // query row it.n * 64 + 32 half + e sees key j iff it is at or after row i0 and inside the block
+        // query row it.n * 64 + 32 half + e sees key j iff it lies in [i0, i1)
         const int c0 = (int)(it.n * kT) + 32 * half;
         const int lo = (int)i0 - c0;
-        const int hi = row_ok ? (int)p.Lr - c0 : 0;
+        const int hi = row_ok ? (int)i1 - c0 : 0;
         tc::tmem_ld_wait();
         uint32_t pk[16], dk[16];
         p_ds_half(sv, dpv, l2, dd, sl2, lo, hi, pk, dk);
@@ -517,6 +538,7 @@ struct QWork {
     uint32_t r, u, h, b, kh, q0;
     uint32_t q_row0;  // row of local query 0 of (r, u, h, b) in q / dout / dq / lse / delta
     uint32_t qpos_min, qpos_max;
+    uint32_t sa_first, se_last;  // sample start of the first row, sample end of the last (packed)
 };
 
 __device__ __forceinline__ QWork q_decode(const BwdTcParams &p) {
@@ -547,28 +569,41 @@ __device__ __forceinline__ QWork q_decode(const BwdTcParams &p) {
     w.q_row0 = (((w.r * p.ud + w.u) * p.Hl + w.h) * p.bs + w.b) * p.Lr;
     w.qpos_min = pos32(p.split, w.r, w.q0, p.c, p.rd);
     w.qpos_max = pos32(p.split, w.r, min(w.q0 + 127, p.Lr - 1), p.c, p.rd);
+    w.sa_first = 0;
+    w.se_last = p.L;
+    if (p.cu) {
+        uint32_t a, e;
+        sample_bounds(p.cu, p.nseq, w.qpos_min, p.L, w.sa_first, e);
+        sample_bounds(p.cu, p.nseq, w.qpos_max, p.L, a, w.se_last);
+    }
     return w;
 }
 
-// KV tiles of 64 keys over the ring steps (Fig. 1 order), visible prefixes only
+// KV tiles of 64 keys over the ring steps (Fig. 1 order), over the rows of rank s that some query
+// of the tile sees: from the first row's sample start to the last row's visible limit
 struct KIter {
-    uint32_t t, s, kt, nkt, nlo;
+    uint32_t t, s, kt, nkt;
     bool done;
 };
 
+__device__ __forceinline__ void q_key_range(const BwdTcParams &p, const QWork &w, uint32_t s, uint32_t &kt0,
+                                            uint32_t &kt1) {
+    const uint32_t lo = before32(p.split, w.sa_first, s, p.c, p.rd);
+    const uint32_t hi = p.causal ? vis32(p.split, w.qpos_max, s, p.c, p.rd) : before32(p.split, w.se_last, s, p.c, p.rd);
+    kt0 = lo / kT;
+    kt1 = hi > lo ? (hi + kT - 1) / kT : kt0;
+}
+
 __device__ __forceinline__ void kiter_step(const BwdTcParams &p, const QWork &w, KIter &it) {
     it.s = (w.r + p.rd - it.t) % p.rd;
-    const uint32_t nhi = p.causal ? vis32(p.split, w.qpos_max, it.s, p.c, p.rd) : p.Lr;
-    it.nlo = p.causal ? vis32(p.split, w.qpos_min, it.s, p.c, p.rd) : p.Lr;
-    it.nkt = (nhi + kT - 1) / kT;
-    it.kt = 0;
+    q_key_range(p, w, it.s, it.kt, it.nkt);
 }
 
 __device__ __forceinline__ void kiter_init(const BwdTcParams &p, const QWork &w, KIter &it) {
     it.t = 0;
     it.done = false;
     kiter_step(p, w, it);
-    while (it.nkt == 0) {
+    while (it.kt >= it.nkt) {
         if (++it.t >= p.rd) {
             it.done = true;
             return;
@@ -585,15 +620,15 @@ __device__ __forceinline__ void kiter_advance(const BwdTcParams &p, const QWork 
             return;
         }
         kiter_step(p, w, it);
-    } while (it.nkt == 0);
+    } while (it.kt >= it.nkt);
 }
 
 __device__ __forceinline__ uint32_t q_count_tiles(const BwdTcParams &p, const QWork &w) {
     uint32_t n = 0;
     for (uint32_t t = 0; t < p.rd; ++t) {
-        const uint32_t s = (w.r + p.rd - t) % p.rd;
-        const uint32_t nhi = p.causal ? vis32(p.split, w.qpos_max, s, p.c, p.rd) : p.Lr;
-        n += (nhi + kT - 1) / kT;
+        uint32_t kt0, kt1;
+        q_key_range(p, w, (w.r + p.rd - t) % p.rd, kt0, kt1);
+        n += kt1 - kt0;
     }
     return n;
 }
@@ -685,6 +720,8 @@ __device__ void q_softmax(const BwdTcParams &p, const QWork &w, uint32_t bar0, u
     const uint32_t i = w.q0 + row;
     const bool row_ok = i < p.Lr;
     const uint32_t qpos = pos32(p.split, w.r, min(i, p.Lr - 1), p.c, p.rd);
+    uint32_t sa = 0, se = p.L;  // the row's sample (packed sequences)
+    if (p.cu) sample_bounds(p.cu, p.nseq, qpos, p.L, sa, se);
     const float lse2 = row_ok ? p.lse[w.q_row0 + i] * kLog2e : 0.f;
     const float di = row_ok ? p.delta[w.q_row0 + i] : 0.f;
     float l2[32], dd[32];
@@ -697,13 +734,15 @@ __device__ void q_softmax(const BwdTcParams &p, const QWork &w, uint32_t bar0, u
     const uint32_t n = q_count_tiles(p, w);
     KIter it;
     kiter_init(p, w, it);
-    uint32_t s_cur = 0xffffffffu, nvis = 0;
+    uint32_t s_cur = 0xffffffffu, nvis = 0, klo = 0;
     bool ok = true;
     for (uint32_t t = 0; t < n && !it.done; ++t) {
         const uint32_t b = t & 1u;
         if (it.s != s_cur) {
+            // the rows of rank s this query sees: [klo, nvis)
             s_cur = it.s;
-            nvis = p.causal ? vis32(p.split, qpos, s_cur, p.c, p.rd) : p.Lr;
+            nvis = p.causal ? vis32(p.split, qpos, s_cur, p.c, p.rd) : before32(p.split, se, s_cur, p.c, p.rd);
+            klo = before32(p.split, sa, s_cur, p.c, p.rd);
         }
         ok = tc::mbar_wait(BAR(C::SP_FULL + b), (t >> 1) & 1u, p.status, USP_ERR_TIMEOUT, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
@@ -714,11 +753,13 @@ __device__ void q_softmax(const BwdTcParams &p, const QWork &w, uint32_t bar0, u
         uint32_t sv[32], dpv[32];
         tc::tmem_ld32(tS, sv);
         tc::tmem_ld32(tP, dpv);
-        // key it.kt * 64 + 32 half + e is visible iff it lies in the row's visible prefix
-        const int hi = row_ok ? (int)nvis - (int)(it.kt * kT) - 32 * half : 0;
+        // key it.kt * 64 + 32 half + e is visible iff it lies in the row's range [klo, nvis)
+        const int c0 = (int)(it.kt * kT) + 32 * half;
+        const int lo = (int)klo - c0;
+        const int hi = row_ok ? (int)nvis - c0 : 0;
         tc::tmem_ld_wait();
         uint32_t pk[16], dk[16];
-        p_ds_half(sv, dpv, l2, dd, sl2, 0, hi, pk, dk);
+        p_ds_half(sv, dpv, l2, dd, sl2, lo, hi, pk, dk);
         tc::tmem_st16(tP, dk);
         tc::tmem_st_wait();
         tc::fence_before_sync();
@@ -858,6 +899,9 @@ int launch_attn_bwd_tc(const BwdArgs &a, cudaStream_t s) {
     base.lpt = (f.split == USP_SPLIT_ZIGZAG && base.c % 128 == 0) ? 1 : 0;
     base.scale = f.scale;
     base.scale_log2 = f.scale * kLog2e;
+    base.cu = f.cu;
+    base.nseq = (uint32_t)f.nseq;
+    base.L = (uint32_t)f.L;
     const uint64_t q_rows = (uint64_t)f.hq * f.bs * f.L;
     const uint64_t kv_rows = (uint64_t)base.Hkl * f.ud * f.bs * f.L;
     BwdTcParams kv = base, q = base;

@@ -265,7 +265,6 @@ int usp_backward(const void *q, const void *k, const void *v, const void *out, c
     FwdShape s{};
     int rc = fwd_shape(d, head_chunk, s);
     if (rc) return rc;
-    if (d.nseq > 1) return USP_ERR_UNSUPPORTED;  // the backward of packed samples is not built yet
     if (d.bs == 0 || d.L == 0) return USP_OK;
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return USP_ERR_INVALID_ARG;
     if (workspace_bytes < ws_backward(s)) return USP_ERR_INVALID_ARG;

@@ -207,7 +207,6 @@ int usp_attn_bwd(const void *q, const void *k, const void *v, const void *dout, 
     int rc = check_attn_desc(d);
     if (rc) return rc;
     if (d.mode != USP_MODE_FUSED || d.ring_rank_only != 0) return USP_ERR_INVALID_ARG;
-    if (d.nseq > 1) return USP_ERR_UNSUPPORTED;  // the backward of packed samples is not built yet
     if (d.bs == 0 || d.L == 0) return USP_OK;
     const void *ptrs[] = {q, k, v, dout, lse, delta, dq, dk, dv};
     for (const void *x : ptrs) {

@@ -217,5 +217,5 @@ def test_packed_samples_rejects():
     assert lib.usp_attn_fwd(BAD, BAD, BAD, BAD, BAD, desc(L=256, nseq=300, cu_seqlens=0x1000), None) == \
         _abi.USP_ERR_SHAPE
     assert lib.usp_attn_fwd(BAD, BAD, BAD, BAD, BAD, desc(nseq=3, cu_seqlens=0x1000), None) == _abi.USP_ERR_ALIGN
-    # the backward of packed samples is not built: refused before anything runs
-    assert lib.usp_attn_bwd(*([BAD] * 9), desc(nseq=3, cu_seqlens=0x1000), None) == _abi.USP_ERR_UNSUPPORTED
+    assert lib.usp_attn_bwd(*([BAD] * 9), desc(nseq=3, cu_seqlens=None), None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_attn_bwd(*([BAD] * 9), desc(nseq=3, cu_seqlens=0x1000), None) == _abi.USP_ERR_ALIGN
