@@ -512,27 +512,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkv_kernel(const __grid_
 // ================================================================================================
 // dq kernel
 // ================================================================================================
+// The dq kernel streams 128-key tiles (N = 128 products run at the full rate, N = 64 ones do not).
+constexpr int kKT = 128;
+
 template <int HD> struct QCfg : Lay<HD> {
     using Y = Lay<HD>;
-    static constexpr int kStages = HD == 128 ? 5 : 8;
+    static constexpr int kKS = HD == 128 ? 3 : 4;           // K stages: K(t) for S(t) and dQ(t), K(t+2) for S(t+2)
+    static constexpr int kVS = HD == 128 ? 2 : 3;           // V stages: V(t+1) for dP(t+1)
     static constexpr int kQ = 0;
     static constexpr int kDo = Y::kBigTile;
-    static constexpr int kKV = 2 * Y::kBigTile;             // stage s: K at kKV + s * kStage, V + kSmallTile
-    static constexpr int kStage = 2 * Y::kSmallTile;
-    static constexpr int kBar = kKV + kStages * kStage;
+    static constexpr int kK = 2 * Y::kBigTile;              // K stage s at kK + s * kBigTile
+    static constexpr int kV = kK + kKS * Y::kBigTile;       // V stage s at kV + s * kBigTile
+    static constexpr int kBar = kV + kVS * Y::kBigTile;
     static constexpr int QO_FULL = 0;
-    static constexpr int KV_FULL = 1;                        // [stages]
-    static constexpr int KV_EMPTY = KV_FULL + kStages;       // [stages]
-    static constexpr int SP_FULL = KV_EMPTY + kStages;       // [2]
-    static constexpr int P_FULL = SP_FULL + 2;               // [2], 8 arrivals
-    static constexpr int ACC_FULL = P_FULL + 2;
+    static constexpr int K_FULL = 1;                         // [kKS]
+    static constexpr int K_EMPTY = K_FULL + kKS;             // [kKS]
+    static constexpr int V_FULL = K_EMPTY + kKS;             // [kVS]
+    static constexpr int V_EMPTY = V_FULL + kVS;             // [kVS]
+    static constexpr int S_FULL = V_EMPTY + kVS;             // [2]: S_b complete
+    static constexpr int DP_FULL = S_FULL + 2;               // dP complete
+    static constexpr int DP_FREE = DP_FULL + 1;              // dP loaded by the softmax (8 warps)
+    static constexpr int DS_FULL = DP_FREE + 1;              // [2]: dS written over S_b (8 warps)
+    static constexpr int ACC_FULL = DS_FULL + 2;
     static constexpr int DONE = ACC_FULL + 1;
     static constexpr int kNumBars = DONE + 1;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kSmemBytes = kTmemSlot + 16 + 1024;
+    // TMEM: dQ [0, hd), S_0 [hd, hd + 128), S_1 [hd + 128, hd + 256), dP [hd + 256, hd + 384)
     __device__ static constexpr uint32_t colS(int b) { return (uint32_t)HD + 128u * (uint32_t)b; }
-    __device__ static constexpr uint32_t colP(int b) { return (uint32_t)HD + 128u * (uint32_t)b + 64u; }
+    __device__ static constexpr uint32_t colP() { return (uint32_t)HD + 256u; }
 };
+static_assert(QCfg<128>::kSmemBytes <= 232448, "dq kernel shared memory");
+
+// register split of the dq kernel (setmaxnreg): a softmax thread holds 64 S and 64 dP values
+constexpr int kQSoftmaxRegs = 208, kQControlRegs = 88;
+static_assert(2 * kQSoftmaxRegs + kQControlRegs == 504, "the launch's 168 registers per thread");
 
 struct QWork {
     uint32_t r, u, h, b, kh, q0;
@@ -579,7 +593,7 @@ __device__ __forceinline__ QWork q_decode(const BwdTcParams &p) {
     return w;
 }
 
-// KV tiles of 64 keys over the ring steps (Fig. 1 order), over the rows of rank s that some query
+// KV tiles of 128 keys over the ring steps (Fig. 1 order), over the rows of rank s that some query
 // of the tile sees: from the first row's sample start to the last row's visible limit
 struct KIter {
     uint32_t t, s, kt, nkt;
@@ -590,8 +604,8 @@ __device__ __forceinline__ void q_key_range(const BwdTcParams &p, const QWork &w
                                             uint32_t &kt1) {
     const uint32_t lo = before32(p.split, w.sa_first, s, p.c, p.rd);
     const uint32_t hi = p.causal ? vis32(p.split, w.qpos_max, s, p.c, p.rd) : before32(p.split, w.se_last, s, p.c, p.rd);
-    kt0 = lo / kT;
-    kt1 = hi > lo ? (hi + kT - 1) / kT : kt0;
+    kt0 = lo / kKT;
+    kt1 = hi > lo ? (hi + kKT - 1) / kKT : kt0;
 }
 
 __device__ __forceinline__ void kiter_step(const BwdTcParams &p, const QWork &w, KIter &it) {
@@ -633,6 +647,8 @@ __device__ __forceinline__ uint32_t q_count_tiles(const BwdTcParams &p, const QW
     return n;
 }
 
+// Q and dout once; then per KV tile K into a K stage and V into a V stage, each waiting only for its
+// own stage to be released (K after dQ(t), V after dP(t))
 template <int HD>
 __device__ void q_producer(const BwdTcParams &p, const QWork &w, uint32_t sbase, uint32_t bar0) {
     using C = QCfg<HD>;
@@ -649,29 +665,38 @@ __device__ void q_producer(const BwdTcParams &p, const QWork &w, uint32_t sbase,
     }
     KIter it;
     kiter_init(p, w, it);
-    uint32_t t = 0;
+    uint32_t t = 0, kf = 0, vf = 0;
     bool ok = true;
     while (!it.done) {
-        const uint32_t st = t % C::kStages;
-        if (!(ok = wait(C::KV_EMPTY + st, ((t / C::kStages) & 1u) ^ 1u))) break;
-        const uint32_t kv_row = (((it.s * p.ud + w.u) * p.Hkl + w.kh) * p.bs + w.b) * p.Lr + it.kt * kT;
-        const uint32_t sk = sbase + C::kKV + st * C::kStage;
-        tc::mbar_arrive_expect_tx(BAR(C::KV_FULL + st), 2 * C::kSmallTile);
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-            tc::tma_load_2d(sk + bx * C::kSmallBox, &p.t_small0, bx * 64, (int32_t)kv_row, BAR(C::KV_FULL + st));
-            tc::tma_load_2d(sk + C::kSmallTile + bx * C::kSmallBox, &p.t_small1, bx * 64, (int32_t)kv_row,
-                            BAR(C::KV_FULL + st));
-        }
+        const uint32_t kv_row = (((it.s * p.ud + w.u) * p.Hkl + w.kh) * p.bs + w.b) * p.Lr + it.kt * kKT;
+        const uint32_t ks = t % C::kKS, vs = t % C::kVS;
+        if (!(ok = wait(C::K_EMPTY + ks, ((t / C::kKS) & 1u) ^ 1u))) break;
+        tc::mbar_arrive_expect_tx(BAR(C::K_FULL + ks), C::kBigTile);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+            tc::tma_load_2d(sbase + C::kK + ks * C::kBigTile + bx * C::kBigBox, &p.t_small0, bx * 64, (int32_t)kv_row,
+                            BAR(C::K_FULL + ks));
+        ++kf;
+        if (!(ok = wait(C::V_EMPTY + vs, ((t / C::kVS) & 1u) ^ 1u))) break;
+        tc::mbar_arrive_expect_tx(BAR(C::V_FULL + vs), C::kBigTile);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+            tc::tma_load_2d(sbase + C::kV + vs * C::kBigTile + bx * C::kBigBox, &p.t_small1, bx * 64, (int32_t)kv_row,
+                            BAR(C::V_FULL + vs));
+        ++vf;
         ++t;
         kiter_advance(p, w, it);
     }
     if (!ok) {
+        // drain the copies this thread issued before the CTA exits
         wait(C::QO_FULL, 0);
-        for (uint32_t f = t > C::kStages ? t - C::kStages : 0; f < t; ++f)
-            wait(C::KV_FULL + f % C::kStages, (f / C::kStages) & 1u);
+        for (uint32_t f = kf > C::kKS ? kf - C::kKS : 0; f < kf; ++f) wait(C::K_FULL + f % C::kKS, (f / C::kKS) & 1u);
+        for (uint32_t f = vf > C::kVS ? vf - C::kVS : 0; f < vf; ++f) wait(C::V_FULL + f % C::kVS, (f / C::kVS) & 1u);
     }
 }
 
+// S_b(t) = Q K(t)^T into one of two S buffers, dP(t) = dout V(t)^T into the one dP buffer as soon
+// as the softmax has loaded dP(t-1), dQ += dS(t) K(t) (A = dS, written as bf16 over S_b) once the
+// softmax has written it, then S(t+2) over the same S buffer (issued after dQ(t), so it cannot
+// overwrite dS(t) before dQ(t) has read it).
 template <int HD>
 __device__ void q_mma(const BwdTcParams &p, const QWork &w, uint32_t sbase, uint32_t bar0, uint32_t tmem) {
     using C = QCfg<HD>;
@@ -682,33 +707,62 @@ __device__ void q_mma(const BwdTcParams &p, const QWork &w, uint32_t sbase, uint
     const uint32_t n = q_count_tiles(p, w);
     const uint64_t qdesc = tc::sw128_desc(sbase + C::kQ, 16, 1024);
     const uint64_t odesc = tc::sw128_desc(sbase + C::kDo, 16, 1024);
-    const uint64_t kk0 = tc::sw128_desc(sbase + C::kKV, 16, 1024);             // K-major view of K / V
-    const uint64_t km0 = tc::sw128_desc(sbase + C::kKV, C::kSmallBox, 1024);   // MN-major view of K
-    auto soff = [](uint32_t st) { return (uint64_t)((st * C::kStage) >> 4); };
-    constexpr uint64_t kVo = (uint64_t)(C::kSmallTile >> 4);
-    auto sp = [&](uint32_t t) {
-        const uint32_t st = t % C::kStages, b = t & 1u;
-        if (!wait(C::KV_FULL + st, (t / C::kStages) & 1u)) return false;
-        issue_sp<HD>(tmem + C::colS(b), tmem + C::colP(b), qdesc, kk0 + soff(st), odesc, kk0 + soff(st) + kVo);
-        tc::mma_commit(BAR(C::SP_FULL + b));
+    const uint64_t kdesc = tc::sw128_desc(sbase + C::kK, 16, 1024);              // K-major view of K
+    const uint64_t kmdesc = tc::sw128_desc(sbase + C::kK, C::kBigBox, 1024);     // MN-major view of K
+    const uint64_t vdesc = tc::sw128_desc(sbase + C::kV, 16, 1024);
+    constexpr uint32_t idS = tc::idesc_bf16_f32(128, kKT, 0, 0);
+    constexpr uint32_t idQ = tc::idesc_bf16_f32(128, HD, 0, 1);
+    auto toff = [](uint32_t st) { return (uint64_t)((st * C::kBigTile) >> 4); };
+    auto kofs = [](int kk) { return (uint64_t)(((kk / 4) * C::kBigBox + (kk % 4) * 32) >> 4); };
+    auto issue_s = [&](uint32_t t) {
+        const uint32_t ks = t % C::kKS;
+        if (!wait(C::K_FULL + ks, (t / C::kKS) & 1u)) return false;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+            tc::mma_ss(tmem + C::colS(t & 1u), qdesc + kofs(kk), kdesc + toff(ks) + kofs(kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit(BAR(C::S_FULL + (t & 1u)));
+        return true;
+    };
+    auto issue_dp = [&](uint32_t t) {
+        const uint32_t vs = t % C::kVS;
+        if (!wait(C::V_FULL + vs, (t / C::kVS) & 1u)) return false;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+            tc::mma_ss(tmem + C::colP(), odesc + kofs(kk), vdesc + toff(vs) + kofs(kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit(BAR(C::DP_FULL));
+        tc::mma_commit(BAR(C::V_EMPTY + vs));
         return true;
     };
     bool ok = wait(C::QO_FULL, 0);
-    if (ok && n > 0) ok = sp(0);
-    if (ok && n > 1) ok = sp(1);
+    if (ok && n > 0) ok = issue_s(0) && issue_dp(0);
+    if (ok && n > 1) ok = issue_s(1);
     for (uint32_t t = 0; ok && t < n; ++t) {
-        const uint32_t st = t % C::kStages, b = t & 1u;
-        if (!(ok = wait(C::P_FULL + b, (t >> 1) & 1u))) break;
+        const uint32_t b = t & 1u, ks = t % C::kKS;
+        // the softmax of tile t has loaded dP(t): compute dP(t+1) while it works
+        if (t + 1 < n) {
+            if (!(ok = wait(C::DP_FREE, t & 1u))) break;
+            tc::fence_after_sync();
+            if (!(ok = issue_dp(t + 1))) break;
+        }
+        if (!(ok = wait(C::DS_FULL + b, (t >> 1) & 1u))) break;
         tc::fence_after_sync();
-        issue_acc<HD>(tmem + 0, tmem + C::colP(b), km0 + soff(st), t > 0);  // dQ += dS K
-        tc::mma_commit(BAR(C::KV_EMPTY + st));
-        if (t + 2 < n) ok = sp(t + 2);
+        // dQ += dS(t) K(t): k-step kk reads keys [16 kk, 16 kk + 16), packed by the softmax at TMEM
+        // column 64 (kk / 4) + 8 (kk % 4) of S_b; K viewed MN-major (N = hd), 16 keys = 2048 bytes
+#pragma unroll
+        for (int kk = 0; kk < kKT / 16; ++kk)
+            tc::mma_ts(tmem, tmem + C::colS(b) + 64u * (kk / 4) + 8u * (kk % 4),
+                       kmdesc + toff(ks) + (uint64_t)((kk * 2048) >> 4), idQ, (t > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(BAR(C::K_EMPTY + ks));
+        if (t + 2 < n) ok = issue_s(t + 2);
     }
     tc::mma_commit(BAR(C::ACC_FULL));
     tc::mma_commit(BAR(C::DONE));
     wait(C::DONE, 0);
 }
 
+// two warpgroups, each owning keys [64 h, 64 h + 64) of every 128-key tile and one thread per query
+// row: load S and dP, release dP, compute dS = P (dP - D) with P = exp2(S scale log2e - lse log2e)
+// (0 outside the row's visible key range), write dS as bf16 over its own half of S
 template <int HD>
 __device__ void q_softmax(const BwdTcParams &p, const QWork &w, uint32_t bar0, uint32_t tmem) {
     using C = QCfg<HD>;
@@ -744,27 +798,37 @@ __device__ void q_softmax(const BwdTcParams &p, const QWork &w, uint32_t bar0, u
             nvis = p.causal ? vis32(p.split, qpos, s_cur, p.c, p.rd) : before32(p.split, se, s_cur, p.c, p.rd);
             klo = before32(p.split, sa, s_cur, p.c, p.rd);
         }
-        ok = tc::mbar_wait(BAR(C::SP_FULL + b), (t >> 1) & 1u, p.status, USP_ERR_TIMEOUT, kWaitNs);
+        ok = tc::mbar_wait(BAR(C::S_FULL + b), (t >> 1) & 1u, p.status, USP_ERR_TIMEOUT, kWaitNs) &&
+             tc::mbar_wait(BAR(C::DP_FULL), t & 1u, p.status, USP_ERR_TIMEOUT, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t tS = tmem + lane_off + C::colS(b) + 32u * half;
-        const uint32_t tP = tmem + lane_off + C::colP(b) + 32u * half;
-        uint32_t sv[32], dpv[32];
-        tc::tmem_ld32(tS, sv);
-        tc::tmem_ld32(tP, dpv);
-        // key it.kt * 64 + 32 half + e is visible iff it lies in the row's range [klo, nvis)
-        const int c0 = (int)(it.kt * kT) + 32 * half;
-        const int lo = (int)klo - c0;
-        const int hi = row_ok ? (int)nvis - c0 : 0;
+        const uint32_t tS = tmem + lane_off + C::colS(b) + 64u * half;
+        const uint32_t tP = tmem + lane_off + C::colP() + 64u * half;
+        uint32_t sv[2][32], dpv[2][32];
+        tc::tmem_ld32(tS, sv[0]);
+        tc::tmem_ld32(tS + 32, sv[1]);
+        tc::tmem_ld32(tP, dpv[0]);
+        tc::tmem_ld32(tP + 32, dpv[1]);
         tc::tmem_ld_wait();
-        uint32_t pk[16], dk[16];
-        p_ds_half(sv, dpv, l2, dd, sl2, lo, hi, pk, dk);
-        tc::tmem_st16(tP, dk);
+        // dP is in registers: the next dP may be computed into the buffer
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(BAR(C::DP_FREE));
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            // key it.kt * 128 + 64 half + 32 c + e is visible iff it lies in the row's range [klo, nvis)
+            const int c0 = (int)(it.kt * kKT) + 64 * half + 32 * c;
+            const int lo = (int)klo - c0;
+            const int hi = row_ok ? (int)nvis - c0 : 0;
+            uint32_t pk[16], dk[16];
+            p_ds_half(sv[c], dpv[c], l2, dd, sl2, lo, hi, pk, dk);
+            tc::tmem_st16(tS + 16 * c, dk);
+        }
         tc::tmem_st_wait();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(BAR(C::P_FULL + b));
+        if (lane == 0) tc::mbar_arrive(BAR(C::DS_FULL + b));
         kiter_advance(p, w, it);
     }
     if (!ok) return;
@@ -803,14 +867,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     if (threadIdx.x == 0) {
         *skip_flag = (*reinterpret_cast<volatile int *>(p.status) != 0) ? 1u : 0u;
         tc::mbar_init(bar0 + 8u * C::QO_FULL, 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            tc::mbar_init(bar0 + 8u * (C::KV_FULL + s), 1);
-            tc::mbar_init(bar0 + 8u * (C::KV_EMPTY + s), 1);
+        for (int s = 0; s < C::kKS; ++s) {
+            tc::mbar_init(bar0 + 8u * (C::K_FULL + s), 1);
+            tc::mbar_init(bar0 + 8u * (C::K_EMPTY + s), 1);
+        }
+        for (int s = 0; s < C::kVS; ++s) {
+            tc::mbar_init(bar0 + 8u * (C::V_FULL + s), 1);
+            tc::mbar_init(bar0 + 8u * (C::V_EMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(bar0 + 8u * (C::SP_FULL + b), 1);
-            tc::mbar_init(bar0 + 8u * (C::P_FULL + b), 8);
+            tc::mbar_init(bar0 + 8u * (C::S_FULL + b), 1);
+            tc::mbar_init(bar0 + 8u * (C::DS_FULL + b), 8);
         }
+        tc::mbar_init(bar0 + 8u * C::DP_FULL, 1);
+        tc::mbar_init(bar0 + 8u * C::DP_FREE, 8);
         tc::mbar_init(bar0 + 8u * C::ACC_FULL, 1);
         tc::mbar_init(bar0 + 8u * C::DONE, 1);
         tc::fence_barrier_init();
@@ -831,16 +901,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     const uint32_t tmem = *tmem_slot;
     const bool skip = *skip_flag != 0;
     const QWork w = q_decode(p);
-    if (!skip) {
-        if (warp == kProducerWarp) {
-            if (lane == 0) q_producer<HD>(p, w, sbase, bar0);
+    if (warp >= 8) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQControlRegs));
+        if (!skip) {
+            if (warp == kProducerWarp && lane == 0) q_producer<HD>(p, w, sbase, bar0);
+            else if (warp == kMmaWarp && lane == 0) q_mma<HD>(p, w, sbase, bar0, tmem);
             __syncwarp();
-        } else if (warp == kMmaWarp) {
-            if (lane == 0) q_mma<HD>(p, w, sbase, bar0, tmem);
-            __syncwarp();
-        } else if (warp < 8) {
-            q_softmax<HD>(p, w, bar0, tmem);
         }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQSoftmaxRegs));
+        if (!skip) q_softmax<HD>(p, w, bar0, tmem);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -869,6 +939,13 @@ int launch_typed(BwdTcParams &kv, BwdTcParams &q, uint32_t grid_kv, uint32_t gri
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return USP_ERR_CUDA;
     int rc = prepare(attn_bwd_dkv_kernel<HD>, KvCfg<HD>::kSmemBytes, set_kv[dev]);
     if (rc) return rc;
+    if (!set_q[dev]) {
+        // setmaxnreg.inc can only be granted from registers the launch holds: refuse a build whose
+        // register count would make the split wait
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, attn_bwd_dq_kernel<HD>) != cudaSuccess) return USP_ERR_CUDA;
+        if ((long)fa.numRegs * kThreads < 2L * 128 * kQSoftmaxRegs + 128L * kQControlRegs) return USP_ERR_UNSUPPORTED;
+    }
     if ((rc = prepare(attn_bwd_dq_kernel<HD>, QCfg<HD>::kSmemBytes, set_q[dev]))) return rc;
     attn_bwd_dkv_kernel<HD><<<grid_kv, kThreads, KvCfg<HD>::kSmemBytes, s>>>(kv);
     attn_bwd_dq_kernel<HD><<<grid_q, kThreads, QCfg<HD>::kSmemBytes, s>>>(q);
@@ -908,7 +985,7 @@ int launch_attn_bwd_tc(const BwdArgs &a, cudaStream_t s) {
     if (!make_tmap(&kv.t_big0, f.k, kv_rows, f.hd, 128) || !make_tmap(&kv.t_big1, f.v, kv_rows, f.hd, 128) ||
         !make_tmap(&kv.t_small0, f.q, q_rows, f.hd, kT) || !make_tmap(&kv.t_small1, a.dout, q_rows, f.hd, kT) ||
         !make_tmap(&q.t_big0, f.q, q_rows, f.hd, 128) || !make_tmap(&q.t_big1, a.dout, q_rows, f.hd, 128) ||
-        !make_tmap(&q.t_small0, f.k, kv_rows, f.hd, kT) || !make_tmap(&q.t_small1, f.v, kv_rows, f.hd, kT))
+        !make_tmap(&q.t_small0, f.k, kv_rows, f.hd, kKT) || !make_tmap(&q.t_small1, f.v, kv_rows, f.hd, kKT))
         return USP_ERR_CUDA;
     kv.g0 = static_cast<__nv_bfloat16 *>(a.dk);
     kv.g1 = static_cast<__nv_bfloat16 *>(a.dv);
