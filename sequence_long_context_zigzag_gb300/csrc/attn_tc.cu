@@ -8,8 +8,15 @@
 // no partial ever leaves the chip (the fused-merge epilogue). USP_MODE_STEP / USP_MODE_ACCUM run a
 // single ring step and write its partial, or merge it into (out, lse) in the epilogue.
 //
-// Kernel design (one CTA = 256 query rows = two 128-row Q tiles of one (r, u, h, b)):
-//   warp 8      TMA producer: Q0, Q1 once; K and V tiles (128 keys x hd) through a ring of stages.
+// Kernel design. A unit of work is 256 query rows = two 128-row Q tiles of one (r, u, h, b). The
+// kernel is persistent: one CTA per SM walks a static list of units, and its roles run through the
+// units without a CTA-wide barrier, so one unit's epilogue overlaps the next unit's Q / K loads and
+// first S products. Units are numbered heaviest first (see decode_work for the order of heads), and
+// round k of gridDim.x units goes to the CTAs in order for even k and in reverse for odd k, which
+// balances the rounds' decreasing costs.
+//   warp 8      TMA producer: Q0, Q1 once per unit (after both issuers' last S product of the previous
+//               unit has completed); K and V tiles (128 keys x hd) through a ring of stages that runs on
+//               across units.
 //   warps 9, 10 MMA issuers, one thread per Q tile i: S_i = Q_i K^T and O_i += P_i V on tcgen05
 //               (kind::f16, bf16 in, fp32 accumulators in tensor memory), issue order PV_i(j),
 //               S_i(j+1), so the tensor core works on one tile while the other tile's softmax runs.
@@ -17,7 +24,8 @@
 //               its S row from TMEM, masks partial tiles, updates the running max with a lazy
 //               rescale (O and l are rescaled only when the max grows by more than 2^8), writes
 //               P = 2^(S*scale*log2e - m) as bf16 back into TMEM (the A operand of the PV MMA), and
-//               finally normalises O and writes out (bf16) and lse (fp32).
+//               at the end of each unit normalises O and writes out (bf16) and lse (fp32), then hands
+//               O's columns back to the issuer for the next unit.
 //   warp 11     holds no role; with warps 8-10 it forms the control warpgroup that hands registers
 //               to the softmax warpgroups (setmaxnreg).
 //   TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+hd) O1 [256+hd, 256+2hd); P_i aliases S_i.
@@ -28,6 +36,8 @@
 // Every wait is bounded (2 s): on expiry the kernel records USP_ERR_TIMEOUT in the device status
 // word, drains what it has in flight and returns.
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "tc_common.cuh"
 #include "tc_ptx.cuh"
@@ -90,9 +100,12 @@ template <int HD> struct Cfg {
     static constexpr int O_FULL = P_FULL + 2;         // [2]
     static constexpr int DONE = O_FULL + 2;           // [2]
     static constexpr int TURN = DONE + 2;             // [2]: issuer i may issue its next burst
-    static constexpr int kNumBars = TURN + 2;
-    static constexpr int kXch = kBar + kNumBars * 8;           // softmax exchange: 2 tiles x 3 kSplit x 128 floats
-    static constexpr int kTmemSlot = kXch + (kSplit > 1 ? 2 * 3 * kSplit * 128 * 4 : 0);
+    static constexpr int Q_EMPTY = TURN + 2;          // both issuers' S products of a unit are done
+    static constexpr int O_EMPTY = Q_EMPTY + 1;       // [2]: the softmax has read O_i of a unit
+    static constexpr int kNumBars = O_EMPTY + 2;
+    static constexpr int kXch = kBar + kNumBars * 8;           // softmax exchange: 2 tiles x 4 kSplit x 128 floats
+    static constexpr int kTmemSlot = kXch + (kSplit > 1 ? 2 * 4 * kSplit * 128 * 4 : 0);
+    // at kTmemSlot: tensor memory address, skip flag
     static constexpr int kSmemBytes = kTmemSlot + 16 + 1024;  // + slack for 1024-byte alignment
     __device__ static constexpr uint32_t colS(int i) { return 128u * (uint32_t)i; }
     __device__ static constexpr uint32_t colO(int i) { return 256u + (uint32_t)(HD * i); }
@@ -103,14 +116,15 @@ struct TcParams {
     __nv_bfloat16 *out;
     float *lse;
     int *status;
-    uint32_t bs, Lr, c, rd, ud, Hl, Hkl, G, npairs;
+    uint32_t bs, Lr, c, rd, ud, Hl, Hkl, npairs, units;
+    uint32_t Gl, ngroups, nouter, sg;  // unit numbering: see decode_work
     int causal, mode, step, lpt, split, ring_rank_only;
     float scale_log2;
     const int32_t *cu;  // packed samples' cumulative lengths, or nullptr
     uint32_t nseq, L;
 };
 
-// The work of one CTA and the walk over its KV tiles (identical in every role). Positions and row
+// The work of one unit and the walk over its KV tiles (identical in every role). Positions and row
 // indices fit in 31 bits (the entry point rejects larger tensors), so 32-bit arithmetic is used.
 struct Work {
     uint32_t r, u, hl, b, kh;
@@ -128,6 +142,7 @@ struct Tile {
     uint32_t kv_row;  // first row of the tile in k / v
     bool act[2];      // the Q tile needs this KV tile
     bool full[2];     // every key of the tile is visible to every row of the Q tile
+    bool first, last; // first / last tile of its unit (set by cursor_next only)
 };
 
 // Per ring step, the keys of rank s's block visible to a row form a range of its rows [lo, hi)
@@ -141,17 +156,36 @@ struct TileIter {
     uint32_t lomin[2], lomax[2];
 };
 
+// The k-th unit of this CTA: round k covers units [k G, (k + 1) G) of the heaviest-first numbering,
+// in CTA order for even k and in reverse order for odd k. False when the CTA has no k-th unit.
+__device__ __forceinline__ bool unit_index(const TcParams &p, uint32_t k, uint32_t &x) {
+    const uint32_t G = gridDim.x, b = blockIdx.x;
+    x = k * G + ((k & 1u) ? G - 1 - b : b);
+    return x < p.units;
+}
+
 template <bool PK>
-__device__ __forceinline__ Work decode_work(const TcParams &p) {
+__device__ __forceinline__ Work decode_work(const TcParams &p, uint32_t x) {
     Work w;
-    uint32_t x = blockIdx.x;
-    const uint32_t inner = p.ud * p.Hl * p.bs;
-    const uint32_t outer = x / inner;
-    uint32_t in = x % inner;
-    w.hl = in % p.Hl;  // heads fastest: CTAs that run together on a GQA group share K/V in L2
-    in /= p.Hl;
-    w.b = in % p.bs;
-    w.u = in / p.bs;
+    // Units that read the same K/V (one local KV head of one Ulysses rank and batch element: a
+    // group of Gl query heads x nouter 256-row blocks) are numbered in super-groups of sg groups.
+    // Inside a super-group the blocks go heaviest first (outer), each block across the super-group's
+    // heads. When every head's K/V fits in L2 together, one super-group holds all heads (the SMs
+    // spread their reads over all heads' K/V); otherwise a super-group's K/V is kept to half of L2,
+    // so the SMs work on few heads at a time and read their K/V from L2 after the first touch, even
+    // though the static schedule lets units that share K/V drift apart in time.
+    const uint32_t per_group = p.nouter * p.Gl;
+    const uint32_t g0 = x / (p.sg * per_group) * p.sg;
+    const uint32_t n = min(p.sg, p.ngroups - g0);
+    const uint32_t xl = x - g0 * per_group;
+    const uint32_t outer = xl / (n * p.Gl);
+    const uint32_t rem = xl % (n * p.Gl);
+    const uint32_t grp = g0 + rem / p.Gl;
+    w.b = grp % p.bs;
+    const uint32_t uk = grp / p.bs;  // u Hkl + kh
+    w.kh = uk % p.Hkl;
+    w.u = uk / p.Hkl;
+    w.hl = w.kh * p.Gl + rem % p.Gl;
     uint32_t qp;
     if (p.ring_rank_only > 0) {
         // one ring rank's share only, its later rows (more keys) first
@@ -175,7 +209,6 @@ __device__ __forceinline__ Work decode_work(const TcParams &p) {
         w.r = outer % p.rd;
         qp = p.npairs - 1 - outer / p.rd;
     }
-    w.kh = w.hl / p.G;
     w.q_row_base = (((w.r * p.ud + w.u) * p.Hl + w.hl) * p.bs + w.b) * p.Lr;
     for (int i = 0; i < 2; ++i) {
         w.q0[i] = qp * 256 + i * 128;
@@ -263,48 +296,89 @@ __device__ __forceinline__ bool iter_next(const TcParams &p, const Work &w, Tile
     return true;
 }
 
+// The CTA's tiles as one stream across its units (units without a tile are passed over), for the
+// MMA issuers, whose bursts run from one unit into the next.
+struct Cursor {
+    uint32_t k;  // sequence number of the next unit to open
+    bool live;   // w / it hold an open unit
+    Work w;
+    TileIter it;
+};
+
+template <bool PK>
+__device__ __forceinline__ bool cursor_next(const TcParams &p, Cursor &c, Tile &tl) {
+    bool first = false;
+    while (!(c.live && iter_next<PK>(p, c.w, c.it, tl))) {
+        uint32_t x;
+        if (!unit_index(p, c.k, x)) {
+            c.live = false;
+            return false;
+        }
+        ++c.k;
+        c.w = decode_work<PK>(p, x);
+        iter_init<PK>(p, c.w, c.it);
+        c.live = true;
+        first = true;
+    }
+    TileIter peek = c.it;
+    Tile d;
+    tl.first = first;
+    tl.last = !iter_next<PK>(p, c.w, peek, d);
+    return true;
+}
+
 // ------------------------------------------------------------------------------------------------
 // roles
 // ------------------------------------------------------------------------------------------------
-// One thread issues every copy: Q0 and Q1 once, then for each KV tile K into a K stage and V into a
-// V stage, each waiting only for its own stage to be released.
+// One thread issues every copy: per unit Q0 and Q1 (once both issuers have finished the previous
+// unit's S products, which read Q), then for each KV tile K into a K stage and V into a V stage, each
+// waiting only for its own stage to be released. Stage fills are counted across units.
 template <int HD, bool PK>
-__device__ void producer_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0) {
+__device__ void producer_role(const TcParams &p, uint32_t sbase, uint32_t bar0) {
     using C = Cfg<HD>;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
     auto wait = [&](int bar, uint32_t parity) {
         return tc::mbar_wait(BAR(bar), parity, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
     };
     const uint32_t sQ = sbase + C::kQ, sK = sbase + C::kK, sV = sbase + C::kV;
-    tc::mbar_arrive_expect_tx(BAR(C::Q_FULL), 2 * C::kTileBytes);
-    for (int i = 0; i < 2; ++i)
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-            tc::tma_load_2d(sQ + i * C::kTileBytes + bx * C::kBoxBytes, &p.tq, bx * 64,
-                            (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
-    uint32_t kfills = 0, vfills = 0;  // stage fills issued
-    TileIter it;
-    iter_init<PK>(p, w, it);
-    Tile tl;
+    uint32_t kfills = 0, vfills = 0, nq = 0;  // stage fills and Q loads issued
     bool ok = true;
-    while (ok && iter_next<PK>(p, w, it, tl)) {
-        const uint32_t st = kfills % C::kStages;
-        const uint32_t ph = ((kfills / C::kStages) & 1u) ^ 1u;
-        if (!(ok = wait(C::K_EMPTY + st, ph))) break;
-        tc::mbar_arrive_expect_tx(BAR(C::K_FULL + st), C::kTileBytes);
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-            tc::tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.tk, bx * 64, (int32_t)tl.kv_row,
-                            BAR(C::K_FULL + st));
-        ++kfills;
-        if (!(ok = wait(C::V_EMPTY + st, ph))) break;
-        tc::mbar_arrive_expect_tx(BAR(C::V_FULL + st), C::kTileBytes);
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-            tc::tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.tv, bx * 64, (int32_t)tl.kv_row,
-                            BAR(C::V_FULL + st));
-        ++vfills;
+    for (uint32_t k = 0; ok; ++k) {
+        uint32_t x;
+        if (!unit_index(p, k, x)) break;
+        const Work w = decode_work<PK>(p, x);
+        TileIter it;
+        iter_init<PK>(p, w, it);
+        Tile tl;
+        if (!iter_next<PK>(p, w, it, tl)) continue;  // a unit without a tile loads nothing
+        if (nq > 0 && !(ok = wait(C::Q_EMPTY, (nq - 1) & 1u))) break;
+        tc::mbar_arrive_expect_tx(BAR(C::Q_FULL), 2 * C::kTileBytes);
+        for (int i = 0; i < 2; ++i)
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+                tc::tma_load_2d(sQ + i * C::kTileBytes + bx * C::kBoxBytes, &p.tq, bx * 64,
+                                (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
+        ++nq;
+        do {
+            const uint32_t st = kfills % C::kStages;
+            const uint32_t ph = ((kfills / C::kStages) & 1u) ^ 1u;
+            if (!(ok = wait(C::K_EMPTY + st, ph))) break;
+            tc::mbar_arrive_expect_tx(BAR(C::K_FULL + st), C::kTileBytes);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+                tc::tma_load_2d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.tk, bx * 64, (int32_t)tl.kv_row,
+                                BAR(C::K_FULL + st));
+            ++kfills;
+            if (!(ok = wait(C::V_EMPTY + st, ph))) break;
+            tc::mbar_arrive_expect_tx(BAR(C::V_FULL + st), C::kTileBytes);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+                tc::tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.tv, bx * 64, (int32_t)tl.kv_row,
+                                BAR(C::V_FULL + st));
+            ++vfills;
+        } while (iter_next<PK>(p, w, it, tl));
     }
     if (!ok) {
         // drain: wait (bounded) for the copies this thread issued, so none lands after the CTA exits
-        wait(C::Q_FULL, 0);
+        // (Q loads are issued one at a time, each after the previous one was consumed)
+        if (nq > 0) wait(C::Q_FULL, (nq - 1) & 1u);
         for (uint32_t f = kfills > C::kStages ? kfills - C::kStages : 0; f < kfills; ++f)
             wait(C::K_FULL + f % C::kStages, (f / C::kStages) & 1u);
         for (uint32_t f = vfills > C::kStages ? vfills - C::kStages : 0; f < vfills; ++f)
@@ -348,8 +422,14 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 // them, and when the softmax sees S_i(j+1) complete, PV_i(j) is complete too (which makes its
 // in-place rescale of O_i safe). The tcgen05 fence follows only the wait on the softmax threads' P
 // (TMA completion is ordered by the mbarrier).
+// The bursts run on from one unit into the next. After the last S of a unit each issuer commits to
+// Q_EMPTY (the producer then loads the next unit's Q); after the last PV of a unit it commits O_FULL_i.
+// When tile j+1 opens a new unit, burst j is split in two turns, PV_i(j) and S_i(j+1), so that no
+// issuer waits for the new Q while holding its turn; and the first PV of a unit waits for O_EMPTY_i,
+// the softmax's read-out of the previous unit's O_i. A Q tile without a visible key in a unit takes
+// no O_FULL / O_EMPTY round (the softmax skips it too).
 template <int HD, bool PK>
-__device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint32_t bar0, uint32_t tmem, int i) {
+__device__ void mma_role(const TcParams &p, uint32_t sbase, uint32_t bar0, uint32_t tmem, int i) {
     using C = Cfg<HD>;
     auto BAR = [&](int k) { return bar0 + 8u * k; };
     auto wait = [&](int bar, uint32_t parity) {
@@ -369,27 +449,38 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
     // (j >= -1) waits for issuer 0's burst j
     uint32_t turns = 0;
     auto take_turn = [&]() { return wait(my_turn, (turns++) & 1u); };
-    bool ok = wait(C::Q_FULL, 0);
-    TileIter it;
-    iter_init<PK>(p, w, it);
+    // S_i of tile t from K stage st, and this issuer's releases of the stage (and of Q after a unit's
+    // last tile)
+    auto s_burst = [&](const Tile &t, uint32_t st) {
+        if (i ? t.act[1] : t.act[0]) {
+            issue_s<HD>(tS, qdesc, kdesc0 + stage_off(st));
+            tc::mma_commit(BAR(barS));
+        }
+        tc::mma_commit(BAR(C::K_EMPTY + st));
+        if (t.last) tc::mma_commit(BAR(C::Q_EMPTY));
+    };
+    Cursor cs;
+    cs.k = 0;
+    cs.live = false;
     Tile cur, nxt;
-    bool have = ok && iter_next<PK>(p, w, it, cur);
-    uint32_t pc = 0, started = 0;
-    uint32_t j = 0;
+    bool have = cursor_next<PK>(p, cs, cur);
+    bool ok = true;
+    uint32_t pc = 0, started = 0;  // P waits; a PV of the current unit has been issued
+    uint32_t nq = 0, no = 0;       // Q loads consumed; O_i read-outs handed to the softmax
+    uint32_t j = 0;                // tiles of the stream (stage ring position)
     if (have) {
-        ok = wait(C::K_FULL + 0, 0);
+        ok = wait(C::Q_FULL, 0) && wait(C::K_FULL + 0, 0);
+        nq = 1;
         if (ok && i == 1) ok = take_turn();
         if (ok) {
-            if (i ? cur.act[1] : cur.act[0]) {
-                issue_s<HD>(tS, qdesc, kdesc0);
-                tc::mma_commit(BAR(barS));
-            }
-            tc::mma_commit(BAR(C::K_EMPTY + 0));
+            s_burst(cur, 0);
             tc::mbar_arrive(BAR(other_turn));
         }
     }
     while (ok && have) {
-        const bool have_n = iter_next<PK>(p, w, it, nxt);
+        // after a unit's last tile the next unit is opened once this unit's PV and O_FULL are issued
+        // (below), off the path from the softmax's last P to the PV that reads it
+        bool have_n = !cur.last && cursor_next<PK>(p, cs, nxt);
         const uint32_t st = j % C::kStages, ph = (j / C::kStages) & 1u;
         const uint32_t stn = (j + 1) % C::kStages, phn = ((j + 1) / C::kStages) & 1u;
         const bool act = i ? cur.act[1] : cur.act[0];
@@ -399,6 +490,7 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
         // runs ahead
         if (!(ok = wait(C::V_FULL + st, ph))) break;
         if (act && !(ok = wait(barP, pc & 1u))) break;
+        if (act && !started && no > 0 && !(ok = wait(C::O_EMPTY + i, (no - 1) & 1u))) break;
         if (have_n && !(ok = wait(C::K_FULL + stn, phn))) break;
         if (!(ok = take_turn())) break;
         if (act) {
@@ -408,20 +500,29 @@ __device__ void mma_role(const TcParams &p, const Work &w, uint32_t sbase, uint3
             started = 1;
         }
         tc::mma_commit(BAR(C::V_EMPTY + st));  // this issuer no longer reads V(j)
-        if (have_n) {
-            if (i ? nxt.act[1] : nxt.act[0]) {
-                issue_s<HD>(tS, qdesc, kdesc0 + stage_off(stn));
-                tc::mma_commit(BAR(barS));
+        if (cur.last) {
+            if (started) {
+                tc::mma_commit(BAR(C::O_FULL + i));
+                ++no;
             }
-            tc::mma_commit(BAR(C::K_EMPTY + stn));  // this issuer no longer reads K(j+1)
+            started = 0;
         }
+        if (have_n) s_burst(nxt, stn);
         tc::mbar_arrive(BAR(other_turn));
+        if (cur.last && (have_n = cursor_next<PK>(p, cs, nxt))) {
+            // tile j+1 opens a new unit
+            if (!(ok = wait(C::Q_FULL, nq & 1u))) break;
+            ++nq;
+            if (!(ok = wait(C::K_FULL + stn, phn))) break;
+            if (!(ok = take_turn())) break;
+            s_burst(nxt, stn);
+            tc::mbar_arrive(BAR(other_turn));
+        }
         cur = nxt;
         have = have_n;
         ++j;
     }
     if (!ok) tc::mbar_arrive(BAR(other_turn));  // let the other issuer reach its own bounded exit
-    tc::mma_commit(BAR(C::O_FULL + i));
     // every MMA of this issuer has finished before tensor memory is released
     tc::mma_commit(BAR(C::DONE + i));
     wait(C::DONE + i, 0);
@@ -512,9 +613,11 @@ __device__ __forceinline__ bool pair_sync_and(int i, bool v) {
 // A failed (timed-out) wait in any warp is passed on through the same exchange (a barrier that ANDs
 // the threads' results), so every warp of the tile leaves the loop at the same KV tile and none is
 // left waiting at the barrier.
+// One call handles one unit; ns (S tiles consumed) and no (O read-outs) run on across units, as the
+// barrier phases do. Returns false after a failed wait.
 template <int HD, bool PK>
-__device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem, int i, int hf,
-                             float *xch) {
+__device__ __forceinline__ bool softmax_unit(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem, int i,
+                                             int hf, float *xch, uint32_t k, uint32_t &ns, uint32_t &no) {
     using C = Cfg<HD>;
     constexpr int kCh = 4 / kSplit;  // 32-column chunks per warpgroup
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -526,6 +629,7 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     const uint32_t barS = bar0 + 8u * (C::S_FULL + i);
     const uint32_t barP = bar0 + 8u * (C::P_FULL + i);
     const uint32_t barO = bar0 + 8u * (C::O_FULL + i);
+    const uint32_t barOE = bar0 + 8u * (C::O_EMPTY + i);
     const uint32_t q0 = i ? w.q0[1] : w.q0[0];
     const bool valid = i ? w.valid[1] : w.valid[0];
     const uint32_t row_local = q0 + row;
@@ -535,8 +639,9 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     if constexpr (PK) sample_bounds(p.cu, p.nseq, qpos_row, p.L, sa_row, se_row);
     const float sl2 = p.scale_log2;
     const uint64_t sl22 = tc::pack2(sl2, sl2);
-    // exchange slots of this tile: maxima [parity][warpgroup][row], then row sums [warpgroup][row]
-    float *xt = xch + i * (3 * kSplit * 128);
+    // exchange slots of this tile: maxima [tile parity][warpgroup][row], then row sums
+    // [unit parity][warpgroup][row]
+    float *xt = xch + i * (4 * kSplit * 128);
 
     float m_used = -INFINITY, l = 0.f;
     uint32_t n_act = 0;
@@ -556,7 +661,7 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
                            : (PK ? before32(p.split, se_row, s_cur, p.c, p.rd) : p.Lr);
             if constexpr (PK) lim_lo = before32(p.split, sa_row, s_cur, p.c, p.rd);
         }
-        ok = tc::mbar_wait(barS, n_act & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+        ok = tc::mbar_wait(barS, ns & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         uint32_t sr[kCh][32];
         float mx = -INFINITY;
@@ -584,7 +689,7 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
         if (kSplit > 1) {
             // partial maxima through shared memory, double-buffered by tile; the barrier also ANDs
             // every thread's wait result, so all warps of the tile leave together on a failure
-            float *slot = xt + (n_act & 1u) * (kSplit * 128);
+            float *slot = xt + (ns & 1u) * (kSplit * 128);
             slot[hf * 128 + row] = mx;
             ok = pair_sync_and(i, ok);
             if (!ok) break;
@@ -629,11 +734,12 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(barP);
         ++n_act;
+        ++ns;
     }
-    if (!ok) return;
+    if (!ok) return false;
     if (kSplit > 1) {
         // the row sum is the sum of the warpgroups' shares
-        float *ls = xt + 2 * kSplit * 128;
+        float *ls = xt + (2 + (k & 1u)) * kSplit * 128;  // by unit parity: a partner may still read the last one
         ls[hf * 128 + row] = l;
         pair_sync(i);
         l = 0.f;
@@ -649,20 +755,26 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
     __nv_bfloat16 *orow = p.out + grow * HD;
     constexpr int kOc = (HD / 32) / kSplit;  // 32-column chunks of O per warpgroup
     if (n_act > 0) {
-        ok = tc::mbar_wait(barO, 0, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+        ok = tc::mbar_wait(barO, no & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
-        if (!ok) return;
+        if (!ok) return false;
+        ++no;
         tc::fence_after_sync();
+        // all of this warpgroup's O columns in one round trip, then O_i goes back to the issuer
+        uint32_t o[kOc][32];
 #pragma unroll
-        for (int oc = hf * kOc; oc < (hf + 1) * kOc; ++oc) {
-            uint32_t o[32];
-            tc::tmem_ld32(tO + oc * 32, o);
-            tc::tmem_ld_wait();
-            if (row_ok) {
+        for (int oc = 0; oc < kOc; ++oc) tc::tmem_ld32(tO + (hf * kOc + oc) * 32, o[oc]);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(barOE);
+        if (row_ok) {
+#pragma unroll
+            for (int oc = 0; oc < kOc; ++oc) {
                 float v[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = u2f(o[e]) * inv_l;
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + oc * 32);
+                for (int e = 0; e < 32; ++e) v[e] = u2f(o[oc][e]) * inv_l;
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + (hf * kOc + oc) * 32);
                 if (p.mode == USP_MODE_ACCUM) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -693,6 +805,18 @@ __device__ void softmax_role(const TcParams &p, const Work &w, uint32_t bar0, ui
         for (int q = hf * (HD / 8) / kSplit; q < (hf + 1) * (HD / 8) / kSplit; ++q) dst[q] = make_uint4(0, 0, 0, 0);
     }
     if (row_ok && hf == 0) p.lse[grow] = lse_out;
+    return true;
+}
+
+template <int HD, bool PK>
+__device__ void softmax_role(const TcParams &p, uint32_t bar0, uint32_t tmem, int i, int hf, float *xch) {
+    uint32_t ns = 0, no = 0;
+    for (uint32_t k = 0;; ++k) {
+        uint32_t x;
+        if (!unit_index(p, k, x)) break;
+        const Work w = decode_work<PK>(p, x);
+        if (!softmax_unit<HD, PK>(p, w, bar0, tmem, i, hf, xch, k, ns, no)) return;
+    }
 }
 
 template <int HD, bool PK>
@@ -727,6 +851,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         tc::mbar_init(bar0 + 8u * (C::DONE + 1), 1);
         tc::mbar_init(bar0 + 8u * C::TURN, 1);
         tc::mbar_init(bar0 + 8u * (C::TURN + 1), 1);
+        tc::mbar_init(bar0 + 8u * C::Q_EMPTY, 2);  // one commit per MMA issuer
+        tc::mbar_init(bar0 + 8u * C::O_EMPTY, 4 * kSplit);  // one arrive per softmax warp
+        tc::mbar_init(bar0 + 8u * (C::O_EMPTY + 1), 4 * kSplit);
         tc::fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -743,24 +870,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const bool skip = *skip_flag != 0;
-    const Work w = decode_work<PK>(p);
 
     if (warp >= kSoftmaxWarps) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
         if (!skip) {
             if (warp == kProducerWarp && lane == 0)
-                producer_role<HD, PK>(p, w, sbase, bar0);
+                producer_role<HD, PK>(p, sbase, bar0);
             else if (warp == kMmaWarp && lane == 0)
-                mma_role<HD, PK>(p, w, sbase, bar0, tmem, 0);
+                mma_role<HD, PK>(p, sbase, bar0, tmem, 0);
             else if (warp == kMmaWarp1 && lane == 0)
-                mma_role<HD, PK>(p, w, sbase, bar0, tmem, 1);
+                mma_role<HD, PK>(p, sbase, bar0, tmem, 1);
             __syncwarp();
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         // warpgroup g: Q tile g / kSplit, column share g % kSplit
         const int g = warp >> 2;
-        if (!skip) softmax_role<HD, PK>(p, w, bar0, tmem, g / kSplit, g % kSplit, reinterpret_cast<float *>(smem + C::kXch));
+        if (!skip)
+            softmax_role<HD, PK>(p, bar0, tmem, g / kSplit, g % kSplit, reinterpret_cast<float *>(smem + C::kXch));
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -817,7 +944,6 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     p.c = (uint32_t)(a.L / (2 * a.rd));
     p.Hl = (uint32_t)(a.hq / a.ud);
     p.Hkl = (uint32_t)heads_per_rank(a.hkv, a.ud);
-    p.G = (uint32_t)(a.hq / a.hkv);
     p.npairs = (p.Lr + 255) / 256;
     p.causal = a.causal;
     p.mode = a.mode;
@@ -830,13 +956,26 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     p.nseq = (uint32_t)a.nseq;
     p.L = (uint32_t)a.L;
     const uint64_t ranks = a.ring_rank_only > 0 ? 1 : (uint64_t)p.rd;
-    const uint64_t grid = ranks * p.ud * p.Hl * p.bs * p.npairs;
-    if (grid == 0) return USP_OK;
-    if (grid >= (1ull << 31)) return USP_ERR_UNSUPPORTED;
+    const uint64_t units = ranks * p.ud * p.Hl * p.bs * p.npairs;
+    if (units == 0) return USP_OK;
+    if (units >= (1ull << 31)) return USP_ERR_UNSUPPORTED;
+    p.units = (uint32_t)units;
+    // unit numbering: groups of units sharing K/V (4 L hd bytes of K and V per group); all groups
+    // in one super-group when their K/V fits in the 126 MiB L2 (with a little spill), else
+    // super-groups of at most 64 MiB of K/V
+    p.Gl = p.Hl / p.Hkl;
+    p.ngroups = p.ud * p.Hkl * p.bs;
+    p.nouter = (uint32_t)ranks * p.npairs;
+    const uint64_t kv_group = 4ull * (uint64_t)a.L * (uint64_t)a.hd;
+    p.sg = (uint64_t)p.ngroups * kv_group <= (160ull << 20)
+               ? p.ngroups
+               : (uint32_t)std::max<uint64_t>(1, std::min<uint64_t>(p.ngroups, (64ull << 20) / kv_group));
+    // persistent: one CTA per SM (the shared-memory footprint allows one), each walking its units
+    const uint32_t grid = (uint32_t)std::min<uint64_t>(units, (uint64_t)std::max(di->sm_count, 1));
     // packed samples run a separate instantiation, so the one-sample kernel carries none of their code
     if (p.cu)
-        return a.hd == 128 ? launch_typed<128, true>(p, (uint32_t)grid, s) : launch_typed<64, true>(p, (uint32_t)grid, s);
-    return a.hd == 128 ? launch_typed<128, false>(p, (uint32_t)grid, s) : launch_typed<64, false>(p, (uint32_t)grid, s);
+        return a.hd == 128 ? launch_typed<128, true>(p, grid, s) : launch_typed<64, true>(p, grid, s);
+    return a.hd == 128 ? launch_typed<128, false>(p, grid, s) : launch_typed<64, false>(p, grid, s);
 }
 
 }  // namespace usp
