@@ -76,6 +76,11 @@ static_assert(kSoftmaxRegs % 8 == 0 && kControlRegs % 8 == 0 && kControlRegs >= 
                   2 * kSplit * kSoftmaxRegs + kControlRegs == kLaunchRegs * kWarps / 4,
               "register split must use exactly the launch's registers");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// packed samples: cu_seqlens entries kept in shared memory (every role decodes every unit, with four
+// binary searches, and every softmax thread searches its row's sample); longer arrays are read from
+// global memory
+constexpr int kCuCache = 4096;
+constexpr uint64_t kSuperGroupKV = 64ull << 20;  // K/V bytes per super-group of units (launch_attn_tc)
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 
@@ -105,8 +110,9 @@ template <int HD> struct Cfg {
     static constexpr int kNumBars = O_EMPTY + 2;
     static constexpr int kXch = kBar + kNumBars * 8;           // softmax exchange: 2 tiles x 4 kSplit x 128 floats
     static constexpr int kTmemSlot = kXch + (kSplit > 1 ? 2 * 4 * kSplit * 128 * 4 : 0);
-    // at kTmemSlot: tensor memory address, skip flag
-    static constexpr int kSmemBytes = kTmemSlot + 16 + 1024;  // + slack for 1024-byte alignment
+    // at kTmemSlot: tensor memory address, skip flag; then (packed samples only) a copy of cu_seqlens
+    static constexpr int kCu = kTmemSlot + 16;
+    static constexpr int kSmemBytes = kCu + 1024;  // + slack for 1024-byte alignment
     __device__ static constexpr uint32_t colS(int i) { return 128u * (uint32_t)i; }
     __device__ static constexpr uint32_t colO(int i) { return 256u + (uint32_t)(HD * i); }
 };
@@ -142,7 +148,7 @@ struct Tile {
     uint32_t kv_row;  // first row of the tile in k / v
     bool act[2];      // the Q tile needs this KV tile
     bool full[2];     // every key of the tile is visible to every row of the Q tile
-    bool first, last; // first / last tile of its unit (set by cursor_next only)
+    bool first;       // first tile of its unit (set by cursor_next only)
 };
 
 // Per ring step, the keys of rank s's block visible to a row form a range of its rows [lo, hi)
@@ -164,8 +170,35 @@ __device__ __forceinline__ bool unit_index(const TcParams &p, uint32_t k, uint32
     return x < p.units;
 }
 
+// sample_bounds on the shared-memory copy of cu_seqlens (at shared address cu_s)
+__device__ __forceinline__ void sample_bounds_smem(uint32_t cu_s, uint32_t nseq, uint32_t g, uint32_t L, uint32_t &a,
+                                                   uint32_t &e) {
+    auto ld = [](uint32_t addr) {
+        int32_t v;
+        asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr));
+        return v;
+    };
+    uint32_t lo = 0, hi = nseq;
+    while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (ld(cu_s + 4u * mid) <= (int32_t)g) lo = mid;
+        else hi = mid;
+    }
+    const int32_t a0 = ld(cu_s + 4u * lo), e0 = ld(cu_s + 4u * lo + 4u);
+    a = (a0 < 0 || (uint32_t)a0 > g) ? (a0 < 0 ? 0u : g) : (uint32_t)a0;
+    e = (e0 <= (int32_t)g) ? g + 1 : ((uint32_t)e0 > L ? L : (uint32_t)e0);
+}
+
+// the sample [a, e) of global position g: from the shared-memory copy when cu_seqlens fits there
+// (cu_s != 0), else from global memory
+__device__ __forceinline__ void sample_of(const TcParams &p, uint32_t cu_s, uint32_t g, uint32_t &a, uint32_t &e) {
+    if (cu_s) sample_bounds_smem(cu_s, p.nseq, g, p.L, a, e);
+    else sample_bounds(p.cu, p.nseq, g, p.L, a, e);
+}
+
+// cu_s: shared address of the cu_seqlens copy, or 0 (packed samples only)
 template <bool PK>
-__device__ __forceinline__ Work decode_work(const TcParams &p, uint32_t x) {
+__device__ __forceinline__ Work decode_work(const TcParams &p, uint32_t cu_s, uint32_t x) {
     Work w;
     // Units that read the same K/V (one local KV head of one Ulysses rank and batch element: a
     // group of Gl query heads x nouter 256-row blocks) are numbered in super-groups of sg groups.
@@ -219,8 +252,8 @@ __device__ __forceinline__ Work decode_work(const TcParams &p, uint32_t x) {
         w.sa_first[i] = w.sa_last[i] = 0;
         w.se_first[i] = w.se_last[i] = p.L;
         if constexpr (PK) {
-            sample_bounds(p.cu, p.nseq, w.qpos_min[i], p.L, w.sa_first[i], w.se_first[i]);
-            sample_bounds(p.cu, p.nseq, w.qpos_max[i], p.L, w.sa_last[i], w.se_last[i]);
+            sample_of(p, cu_s, w.qpos_min[i], w.sa_first[i], w.se_first[i]);
+            sample_of(p, cu_s, w.qpos_max[i], w.sa_last[i], w.se_last[i]);
         }
     }
     w.t_begin = p.mode == USP_MODE_FUSED ? 0 : p.step;
@@ -306,7 +339,7 @@ struct Cursor {
 };
 
 template <bool PK>
-__device__ __forceinline__ bool cursor_next(const TcParams &p, Cursor &c, Tile &tl) {
+__device__ __forceinline__ bool cursor_next(const TcParams &p, uint32_t cu_s, Cursor &c, Tile &tl) {
     bool first = false;
     while (!(c.live && iter_next<PK>(p, c.w, c.it, tl))) {
         uint32_t x;
@@ -315,15 +348,12 @@ __device__ __forceinline__ bool cursor_next(const TcParams &p, Cursor &c, Tile &
             return false;
         }
         ++c.k;
-        c.w = decode_work<PK>(p, x);
+        c.w = decode_work<PK>(p, cu_s, x);
         iter_init<PK>(p, c.w, c.it);
         c.live = true;
         first = true;
     }
-    TileIter peek = c.it;
-    Tile d;
     tl.first = first;
-    tl.last = !iter_next<PK>(p, c.w, peek, d);
     return true;
 }
 
@@ -334,7 +364,7 @@ __device__ __forceinline__ bool cursor_next(const TcParams &p, Cursor &c, Tile &
 // unit's S products, which read Q), then for each KV tile K into a K stage and V into a V stage, each
 // waiting only for its own stage to be released. Stage fills are counted across units.
 template <int HD, bool PK>
-__device__ void producer_role(const TcParams &p, uint32_t sbase, uint32_t bar0) {
+__device__ void producer_role(const TcParams &p, uint32_t cu_s, uint32_t sbase, uint32_t bar0) {
     using C = Cfg<HD>;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
     auto wait = [&](int bar, uint32_t parity) {
@@ -346,19 +376,22 @@ __device__ void producer_role(const TcParams &p, uint32_t sbase, uint32_t bar0) 
     for (uint32_t k = 0; ok; ++k) {
         uint32_t x;
         if (!unit_index(p, k, x)) break;
-        const Work w = decode_work<PK>(p, x);
+        const Work w = decode_work<PK>(p, cu_s, x);
         TileIter it;
         iter_init<PK>(p, w, it);
         Tile tl;
-        if (!iter_next<PK>(p, w, it, tl)) continue;  // a unit without a tile loads nothing
-        if (nq > 0 && !(ok = wait(C::Q_EMPTY, (nq - 1) & 1u))) break;
-        tc::mbar_arrive_expect_tx(BAR(C::Q_FULL), 2 * C::kTileBytes);
-        for (int i = 0; i < 2; ++i)
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-                tc::tma_load_2d(sQ + i * C::kTileBytes + bx * C::kBoxBytes, &p.tq, bx * 64,
-                                (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
-        ++nq;
-        do {
+        bool first = true;  // a unit without a tile loads nothing
+        while (ok && iter_next<PK>(p, w, it, tl)) {
+            if (first) {
+                first = false;
+                if (nq > 0 && !(ok = wait(C::Q_EMPTY, (nq - 1) & 1u))) break;
+                tc::mbar_arrive_expect_tx(BAR(C::Q_FULL), 2 * C::kTileBytes);
+                for (int i = 0; i < 2; ++i)
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        tc::tma_load_2d(sQ + i * C::kTileBytes + bx * C::kBoxBytes, &p.tq, bx * 64,
+                                        (int32_t)(w.q_row_base + w.q0[i]), BAR(C::Q_FULL));
+                ++nq;
+            }
             const uint32_t st = kfills % C::kStages;
             const uint32_t ph = ((kfills / C::kStages) & 1u) ^ 1u;
             if (!(ok = wait(C::K_EMPTY + st, ph))) break;
@@ -373,7 +406,7 @@ __device__ void producer_role(const TcParams &p, uint32_t sbase, uint32_t bar0) 
                 tc::tma_load_2d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.tv, bx * 64, (int32_t)tl.kv_row,
                                 BAR(C::V_FULL + st));
             ++vfills;
-        } while (iter_next<PK>(p, w, it, tl));
+        }
     }
     if (!ok) {
         // drain: wait (bounded) for the copies this thread issued, so none lands after the CTA exits
@@ -422,14 +455,16 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 // them, and when the softmax sees S_i(j+1) complete, PV_i(j) is complete too (which makes its
 // in-place rescale of O_i safe). The tcgen05 fence follows only the wait on the softmax threads' P
 // (TMA completion is ordered by the mbarrier).
-// The bursts run on from one unit into the next. After the last S of a unit each issuer commits to
-// Q_EMPTY (the producer then loads the next unit's Q); after the last PV of a unit it commits O_FULL_i.
+// The bursts run on from one unit into the next. At the start of the burst of a unit's last tile each
+// issuer commits to Q_EMPTY (its S products of the unit were all issued in earlier bursts; once both
+// issuers' commits arrive, the producer loads the next unit's Q), and after the last PV it commits
+// O_FULL_i.
 // When tile j+1 opens a new unit, burst j is split in two turns, PV_i(j) and S_i(j+1), so that no
 // issuer waits for the new Q while holding its turn; and the first PV of a unit waits for O_EMPTY_i,
 // the softmax's read-out of the previous unit's O_i. A Q tile without a visible key in a unit takes
 // no O_FULL / O_EMPTY round (the softmax skips it too).
 template <int HD, bool PK>
-__device__ void mma_role(const TcParams &p, uint32_t sbase, uint32_t bar0, uint32_t tmem, int i) {
+__device__ void mma_role(const TcParams &p, uint32_t cu_s, uint32_t sbase, uint32_t bar0, uint32_t tmem, int i) {
     using C = Cfg<HD>;
     auto BAR = [&](int k) { return bar0 + 8u * k; };
     auto wait = [&](int bar, uint32_t parity) {
@@ -449,21 +484,19 @@ __device__ void mma_role(const TcParams &p, uint32_t sbase, uint32_t bar0, uint3
     // (j >= -1) waits for issuer 0's burst j
     uint32_t turns = 0;
     auto take_turn = [&]() { return wait(my_turn, (turns++) & 1u); };
-    // S_i of tile t from K stage st, and this issuer's releases of the stage (and of Q after a unit's
-    // last tile)
+    // S_i of tile t from K stage st, and this issuer's release of the stage
     auto s_burst = [&](const Tile &t, uint32_t st) {
         if (i ? t.act[1] : t.act[0]) {
             issue_s<HD>(tS, qdesc, kdesc0 + stage_off(st));
             tc::mma_commit(BAR(barS));
         }
         tc::mma_commit(BAR(C::K_EMPTY + st));
-        if (t.last) tc::mma_commit(BAR(C::Q_EMPTY));
     };
     Cursor cs;
     cs.k = 0;
     cs.live = false;
     Tile cur, nxt;
-    bool have = cursor_next<PK>(p, cs, cur);
+    bool have = cursor_next<PK>(p, cu_s, cs, cur);
     bool ok = true;
     uint32_t pc = 0, started = 0;  // P waits; a PV of the current unit has been issued
     uint32_t nq = 0, no = 0;       // Q loads consumed; O_i read-outs handed to the softmax
@@ -478,12 +511,13 @@ __device__ void mma_role(const TcParams &p, uint32_t sbase, uint32_t bar0, uint3
         }
     }
     while (ok && have) {
-        // after a unit's last tile the next unit is opened once this unit's PV and O_FULL are issued
-        // (below), off the path from the softmax's last P to the PV that reads it
-        bool have_n = !cur.last && cursor_next<PK>(p, cs, nxt);
+        const bool have_n = cursor_next<PK>(p, cu_s, cs, nxt);
+        const bool last = !have_n || nxt.first;      // tile j is the last of its unit
+        const bool boundary = have_n && nxt.first;  // tile j+1 opens a new unit
         const uint32_t st = j % C::kStages, ph = (j / C::kStages) & 1u;
         const uint32_t stn = (j + 1) % C::kStages, phn = ((j + 1) / C::kStages) & 1u;
         const bool act = i ? cur.act[1] : cur.act[0];
+        if (last) tc::mma_commit(BAR(C::Q_EMPTY));  // this issuer's S products of the unit are issued
         // operands first: every issuer waits for a stage's fill before releasing it, even when its Q
         // tile skips the tile, so neither issuer can release fill f + kStages before the producer has
         // refilled the stage (which needs both releases of fill f): the shared release barrier never
@@ -491,7 +525,7 @@ __device__ void mma_role(const TcParams &p, uint32_t sbase, uint32_t bar0, uint3
         if (!(ok = wait(C::V_FULL + st, ph))) break;
         if (act && !(ok = wait(barP, pc & 1u))) break;
         if (act && !started && no > 0 && !(ok = wait(C::O_EMPTY + i, (no - 1) & 1u))) break;
-        if (have_n && !(ok = wait(C::K_FULL + stn, phn))) break;
+        if (have_n && !boundary && !(ok = wait(C::K_FULL + stn, phn))) break;
         if (!(ok = take_turn())) break;
         if (act) {
             ++pc;
@@ -500,17 +534,16 @@ __device__ void mma_role(const TcParams &p, uint32_t sbase, uint32_t bar0, uint3
             started = 1;
         }
         tc::mma_commit(BAR(C::V_EMPTY + st));  // this issuer no longer reads V(j)
-        if (cur.last) {
+        if (last) {
             if (started) {
                 tc::mma_commit(BAR(C::O_FULL + i));
                 ++no;
             }
             started = 0;
         }
-        if (have_n) s_burst(nxt, stn);
+        if (have_n && !boundary) s_burst(nxt, stn);
         tc::mbar_arrive(BAR(other_turn));
-        if (cur.last && (have_n = cursor_next<PK>(p, cs, nxt))) {
-            // tile j+1 opens a new unit
+        if (boundary) {
             if (!(ok = wait(C::Q_FULL, nq & 1u))) break;
             ++nq;
             if (!(ok = wait(C::K_FULL + stn, phn))) break;
@@ -616,8 +649,9 @@ __device__ __forceinline__ bool pair_sync_and(int i, bool v) {
 // One call handles one unit; ns (S tiles consumed) and no (O read-outs) run on across units, as the
 // barrier phases do. Returns false after a failed wait.
 template <int HD, bool PK>
-__device__ __forceinline__ bool softmax_unit(const TcParams &p, const Work &w, uint32_t bar0, uint32_t tmem, int i,
-                                             int hf, float *xch, uint32_t k, uint32_t &ns, uint32_t &no) {
+__device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, const Work &w, uint32_t bar0,
+                                             uint32_t tmem, int i, int hf, float *xch, uint32_t k, uint32_t &ns,
+                                             uint32_t &no) {
     using C = Cfg<HD>;
     constexpr int kCh = 4 / kSplit;  // 32-column chunks per warpgroup
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -636,7 +670,7 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, const Work &w, u
     const bool row_ok = valid && row_local < p.Lr;
     const uint32_t qpos_row = pos32(p.split, w.r, min(row_local, p.Lr - 1), p.c, p.rd);
     uint32_t sa_row = 0, se_row = p.L;  // the row's sample (packed sequences)
-    if constexpr (PK) sample_bounds(p.cu, p.nseq, qpos_row, p.L, sa_row, se_row);
+    if constexpr (PK) sample_of(p, cu_s, qpos_row, sa_row, se_row);
     const float sl2 = p.scale_log2;
     const uint64_t sl22 = tc::pack2(sl2, sl2);
     // exchange slots of this tile: maxima [tile parity][warpgroup][row], then row sums
@@ -809,13 +843,14 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, const Work &w, u
 }
 
 template <int HD, bool PK>
-__device__ void softmax_role(const TcParams &p, uint32_t bar0, uint32_t tmem, int i, int hf, float *xch) {
+__device__ void softmax_role(const TcParams &p, uint32_t cu_s, uint32_t bar0, uint32_t tmem, int i, int hf,
+                             float *xch) {
     uint32_t ns = 0, no = 0;
     for (uint32_t k = 0;; ++k) {
         uint32_t x;
         if (!unit_index(p, k, x)) break;
-        const Work w = decode_work<PK>(p, x);
-        if (!softmax_unit<HD, PK>(p, w, bar0, tmem, i, hf, xch, k, ns, no)) return;
+        const Work w = decode_work<PK>(p, cu_s, x);
+        if (!softmax_unit<HD, PK>(p, cu_s, w, bar0, tmem, i, hf, xch, k, ns, no)) return;
     }
 }
 
@@ -860,6 +895,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
         tc::tmem_relinquish();
     }
+    // packed samples: cu_seqlens into shared memory (when it fits), read by every role's decode
+    uint32_t cu_s = 0;
+    if constexpr (PK) {
+        if (p.nseq + 1 <= (uint32_t)kCuCache) {
+            int32_t *cs = reinterpret_cast<int32_t *>(smem + C::kCu);
+            for (uint32_t e = threadIdx.x; e <= p.nseq; e += kThreads) cs[e] = p.cu[e];
+            cu_s = sbase + C::kCu;
+        }
+    }
     if (warp == kProducerWarp && lane == 0) {
         tc::prefetch_tmap(&p.tq);
         tc::prefetch_tmap(&p.tk);
@@ -875,11 +919,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
         if (!skip) {
             if (warp == kProducerWarp && lane == 0)
-                producer_role<HD, PK>(p, sbase, bar0);
+                producer_role<HD, PK>(p, cu_s, sbase, bar0);
             else if (warp == kMmaWarp && lane == 0)
-                mma_role<HD, PK>(p, sbase, bar0, tmem, 0);
+                mma_role<HD, PK>(p, cu_s, sbase, bar0, tmem, 0);
             else if (warp == kMmaWarp1 && lane == 0)
-                mma_role<HD, PK>(p, sbase, bar0, tmem, 1);
+                mma_role<HD, PK>(p, cu_s, sbase, bar0, tmem, 1);
             __syncwarp();
         }
     } else {
@@ -887,7 +931,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         // warpgroup g: Q tile g / kSplit, column share g % kSplit
         const int g = warp >> 2;
         if (!skip)
-            softmax_role<HD, PK>(p, bar0, tmem, g / kSplit, g % kSplit, reinterpret_cast<float *>(smem + C::kXch));
+            softmax_role<HD, PK>(p, cu_s, bar0, tmem, g / kSplit, g % kSplit,
+                                 reinterpret_cast<float *>(smem + C::kXch));
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -903,6 +948,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 template <int HD, bool PK>
 int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
     using C = Cfg<HD>;
+    constexpr int kSmem = C::kSmemBytes + (PK ? kCuCache * 4 : 0);
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -913,12 +960,12 @@ int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
         if (cudaFuncGetAttributes(&fa, attn_tc_kernel<HD, PK>) != cudaSuccess) return USP_ERR_CUDA;
         if ((long)fa.numRegs * kThreads < 2L * kSplit * 128 * kSoftmaxRegs + 128L * kControlRegs)
             return USP_ERR_UNSUPPORTED;
-        if (cudaFuncSetAttribute(attn_tc_kernel<HD, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        if (cudaFuncSetAttribute(attn_tc_kernel<HD, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
             cudaSuccess)
             return USP_ERR_CUDA;
         attr_set[dev] = true;
     }
-    attn_tc_kernel<HD, PK><<<grid, kThreads, C::kSmemBytes, s>>>(prm);
+    attn_tc_kernel<HD, PK><<<grid, kThreads, kSmem, s>>>(prm);
     return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA;
 }
 
@@ -960,16 +1007,20 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     if (units == 0) return USP_OK;
     if (units >= (1ull << 31)) return USP_ERR_UNSUPPORTED;
     p.units = (uint32_t)units;
-    // unit numbering: groups of units sharing K/V (4 L hd bytes of K and V per group); all groups
-    // in one super-group when their K/V fits in the 126 MiB L2 (with a little spill), else
-    // super-groups of at most 64 MiB of K/V
+    // unit numbering: groups of units sharing K/V (4 L hd bytes of K and V per group), in
+    // super-groups of kSuperGroupKV of K/V where that saves DRAM traffic: not when all groups' K/V
+    // fits in the 126 MiB L2 (with a little spill), not when one group's K/V alone is larger than the
+    // budget, and not for packed samples (a unit then reads only its own sample's K/V). Working on
+    // fewer heads at a time costs time of its own (measured: 7% at L = 8192 with two super-groups,
+    // 50% for packed samples of 1024 with one head per super-group, 1.6% at L = 262144 with one of
+    // two 128 MiB groups per super-group), while at L = 131072 (32 groups of 64 MiB) one group per
+    // super-group cuts DRAM reads from 151 to 60 GB per launch.
     p.Gl = p.Hl / p.Hkl;
     p.ngroups = p.ud * p.Hkl * p.bs;
     p.nouter = (uint32_t)ranks * p.npairs;
     const uint64_t kv_group = 4ull * (uint64_t)a.L * (uint64_t)a.hd;
-    p.sg = (uint64_t)p.ngroups * kv_group <= (160ull << 20)
-               ? p.ngroups
-               : (uint32_t)std::max<uint64_t>(1, std::min<uint64_t>(p.ngroups, (64ull << 20) / kv_group));
+    const bool grouped = !p.cu && (uint64_t)p.ngroups * kv_group > (160ull << 20) && kv_group <= kSuperGroupKV;
+    p.sg = grouped ? (uint32_t)std::min<uint64_t>(p.ngroups, kSuperGroupKV / kv_group) : p.ngroups;
     // persistent: one CTA per SM (the shared-memory footprint allows one), each walking its units
     const uint32_t grid = (uint32_t)std::min<uint64_t>(units, (uint64_t)std::max(di->sm_count, 1));
     // packed samples run a separate instantiation, so the one-sample kernel carries none of their code

@@ -76,6 +76,23 @@ def test_one_sample_equals_unpacked():
     assert torch.equal(a, b) and torch.equal(la, lb)
 
 
+def test_many_samples_past_the_shared_memory_copy():
+    """More samples than the forward kernel keeps in shared memory (4095): the sample search falls
+    back to global memory. L = 8192 as 5462 samples of 1 or 2 tokens, every row against the oracle."""
+    L, hq, hkv, hd, ud, rd = 8192, 4, 2, 128, 2, 2
+    lens = [1 + (i % 2) for i in range(5462)]
+    lens[-1] = L - sum(lens[:-1])
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    assert cu[-1] == L and len(cu) - 1 > 4095 and min(lens) >= 1
+    q, k, v = make_qkv(1, L, hq, hkv, hd, "bf16", seed=77)
+    cud = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    out, lse = usp.usp_attention(q.cuda(), k.cuda(), v.cuda(), ud=ud, rd=rd, cu_seqlens=cud)
+    usp.usp_check()
+    check(out, lse, q, k, v, cu)
+
+
 def test_packing_full_size_sampled():
     """The L = 32768 GQA workload packed as 32 samples of 1024, at full size: sampled rows against
     the oracle's per-sample attention."""
