@@ -49,31 +49,22 @@ namespace {
 
 constexpr int kM = 128;  // query rows per tile
 constexpr int kN = 128;  // keys per tile
-// softmax warpgroups per Q tile (each owns 128 / kSplit columns of every S row). Two per tile (640
-// threads, a shared-memory max exchange per KV tile) measured 6% slower than one on GB300, so one is
-// the default.
-#ifndef USP_SOFTMAX_SPLIT
-#define USP_SOFTMAX_SPLIT 1
-#endif
-constexpr int kSplit = USP_SOFTMAX_SPLIT;
-static_assert(kSplit == 1 || kSplit == 2, "softmax split must be 1 or 2");
-constexpr int kSoftmaxWarps = 8 * kSplit;      // 2 Q tiles x kSplit warpgroups x 4 warps
+// one softmax warpgroup per Q tile (two per tile, 640 threads with a shared-memory max exchange per
+// KV tile, measured 6% slower on GB300)
+constexpr int kSoftmaxWarps = 8;               // 2 Q tiles x 4 warps
 constexpr int kWarps = kSoftmaxWarps + 4;      // plus the control warpgroup
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;    // issues Q tile 0's MMAs; allocates and frees tensor memory
 constexpr int kMmaWarp1 = kSoftmaxWarps + 2;   // issues Q tile 1's MMAs
 // Register split per warpgroup (setmaxnreg). The launch grants kThreads x kLaunchRegs registers; the
-// softmax warpgroups take 2 kSplit x 128 x kSoftmaxRegs and the control warpgroup keeps
+// softmax warpgroups take 2 x 128 x kSoftmaxRegs and the control warpgroup keeps
 // 128 x kControlRegs, together exactly the launch's registers, so the increase can always be granted.
 constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
-#ifndef USP_SOFTMAX_REGS
-#define USP_SOFTMAX_REGS (kSplit == 1 ? 208 : 104)
-#endif
-constexpr int kSoftmaxRegs = USP_SOFTMAX_REGS;
-constexpr int kControlRegs = kLaunchRegs * kWarps / 4 - 2 * kSplit * kSoftmaxRegs;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kControlRegs = kLaunchRegs * kWarps / 4 - 2 * kSoftmaxRegs;
 static_assert(kSoftmaxRegs % 8 == 0 && kControlRegs % 8 == 0 && kControlRegs >= 24 && kControlRegs <= 256 &&
-                  2 * kSplit * kSoftmaxRegs + kControlRegs == kLaunchRegs * kWarps / 4,
+                  2 * kSoftmaxRegs + kControlRegs == kLaunchRegs * kWarps / 4,
               "register split must use exactly the launch's registers");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // packed samples: cu_seqlens entries kept in shared memory (every role decodes every unit, with four
@@ -108,8 +99,7 @@ template <int HD> struct Cfg {
     static constexpr int Q_EMPTY = TURN + 2;          // both issuers' S products of a unit are done
     static constexpr int O_EMPTY = Q_EMPTY + 1;       // [2]: the softmax has read O_i of a unit
     static constexpr int kNumBars = O_EMPTY + 2;
-    static constexpr int kXch = kBar + kNumBars * 8;           // softmax exchange: 2 tiles x 4 kSplit x 128 floats
-    static constexpr int kTmemSlot = kXch + (kSplit > 1 ? 2 * 4 * kSplit * 128 * 4 : 0);
+    static constexpr int kTmemSlot = kBar + kNumBars * 8;
     // at kTmemSlot: tensor memory address, skip flag; then (packed samples only) a copy of cu_seqlens
     static constexpr int kCu = kTmemSlot + 16;
     static constexpr int kSmemBytes = kCu + 1024;  // + slack for 1024-byte alignment
@@ -602,58 +592,19 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&r)[32], uint64_t sl22
     }
 }
 
-// TMEM loads / stores of 16 or 32 columns, chosen by the array's size
-template <int W> __device__ __forceinline__ void tmem_ldw(uint32_t a, uint32_t (&r)[W]) {
-    static_assert(W == 16 || W == 32, "16 or 32 columns");
-    if constexpr (W == 16) tc::tmem_ld16(a, r);
-    else tc::tmem_ld32(a, r);
-}
-template <int W> __device__ __forceinline__ void tmem_stw(uint32_t a, const uint32_t (&r)[W]) {
-    static_assert(W == 16 || W == 32, "16 or 32 columns");
-    if constexpr (W == 16) tc::tmem_st16(a, r);
-    else tc::tmem_st32(a, r);
-}
-
-// named barrier of the kSplit softmax warpgroups of Q tile i (id 0 is __syncthreads)
-__device__ __forceinline__ void pair_sync(int i) {
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + i), "r"(kSplit * 128) : "memory");
-}
-
-// the same barrier, returning to every participating thread whether all of them passed v = true
-__device__ __forceinline__ bool pair_sync_and(int i, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(1 + i), "r"(kSplit * 128)
-        : "memory");
-    return r != 0;
-}
-
-// The softmax of Q tile i, shared by kSplit warpgroups: warpgroup hf owns columns
-// [hf 128 / kSplit, (hf + 1) 128 / kSplit) of every S row (one thread per query row; TMEM lane =
-// row). Per KV tile each thread reads its columns of the row from TMEM in one round trip, the
-// warpgroups exchange their partial row maxima through shared memory (so both apply the same max
-// and make the same rescale decision), and O and l are rescaled only when the running max grows by
-// more than 2^8 (lazy rescale: exact, because the final normalisation uses the same stale max; each
-// warpgroup rescales its own columns of O and keeps its own share of l). P = 2^(s*scale*log2e - m)
-// is packed to bf16 and written over the start of S, where the PV MMA reads it as its A operand: a
-// warpgroup's P columns may lie over another warpgroup's S columns, but every warpgroup has loaded
-// its S before the max exchange, and P is written after it.
-// A failed (timed-out) wait in any warp is passed on through the same exchange (a barrier that ANDs
-// the threads' results), so every warp of the tile leaves the loop at the same KV tile and none is
-// left waiting at the barrier.
+// The softmax of Q tile i: one thread per query row (TMEM lane = row). Per KV tile each thread reads
+// its S row from TMEM in one round trip, and O and l are rescaled only when the running max grows by
+// more than 2^8 (lazy rescale: exact, because the final normalisation uses the same stale max).
+// P = 2^(s*scale*log2e - m) is packed to bf16 and written over the start of S, where the PV MMA
+// reads it as its A operand. A failed (timed-out) wait in any lane makes the whole warp leave (the
+// warps of the tile then fail their own next waits, which the recorded status ends quickly).
 // One call handles one unit; ns (S tiles consumed) and no (O read-outs) run on across units, as the
 // barrier phases do. Returns false after a failed wait.
 template <int HD, bool PK>
 __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, const Work &w, uint32_t bar0,
-                                             uint32_t tmem, int i, int hf, float *xch, uint32_t k, uint32_t &ns,
-                                             uint32_t &no) {
+                                             uint32_t tmem, int i, uint32_t &ns, uint32_t &no) {
     using C = Cfg<HD>;
-    constexpr int kCh = 4 / kSplit;  // 32-column chunks per warpgroup
+    constexpr int kCh = 4;  // 32-column chunks of an S row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wq = warp & 3;
     const uint32_t row = wq * 32 + lane;
@@ -673,9 +624,6 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
     if constexpr (PK) sample_of(p, cu_s, qpos_row, sa_row, se_row);
     const float sl2 = p.scale_log2;
     const uint64_t sl22 = tc::pack2(sl2, sl2);
-    // exchange slots of this tile: maxima [tile parity][warpgroup][row], then row sums
-    // [unit parity][warpgroup][row]
-    float *xt = xch + i * (4 * kSplit * 128);
 
     float m_used = -INFINITY, l = 0.f;
     uint32_t n_act = 0;
@@ -702,7 +650,7 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
         if (ok) {
             tc::fence_after_sync();
 #pragma unroll
-            for (int cc = 0; cc < kCh; ++cc) tc::tmem_ld32(tS + (hf * kCh + cc) * 32, sr[cc]);
+            for (int cc = 0; cc < kCh; ++cc) tc::tmem_ld32(tS + cc * 32, sr[cc]);
             tc::tmem_ld_wait();
             if (!full) {
                 const int ll = (int)lim - (int)(tl.kt * kN);
@@ -710,25 +658,15 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
                 if constexpr (PK) {
                     const int lo_local = (int)lim_lo - (int)(tl.kt * kN);
 #pragma unroll
-                    for (int cc = 0; cc < kCh; ++cc) mask_chunk2(sr[cc], (hf * kCh + cc) * 32, lo_local, lim_local);
+                    for (int cc = 0; cc < kCh; ++cc) mask_chunk2(sr[cc], cc * 32, lo_local, lim_local);
                 } else {
 #pragma unroll
-                    for (int cc = 0; cc < kCh; ++cc) mask_chunk(sr[cc], (hf * kCh + cc) * 32, lim_local);
+                    for (int cc = 0; cc < kCh; ++cc) mask_chunk(sr[cc], cc * 32, lim_local);
                 }
             }
 #pragma unroll
             for (int cc = 0; cc < kCh; ++cc) mx = fmaxf(mx, chunk_max(sr[cc]));
             mx *= sl2;
-        }
-        if (kSplit > 1) {
-            // partial maxima through shared memory, double-buffered by tile; the barrier also ANDs
-            // every thread's wait result, so all warps of the tile leave together on a failure
-            float *slot = xt + (ns & 1u) * (kSplit * 128);
-            slot[hf * 128 + row] = mx;
-            ok = pair_sync_and(i, ok);
-            if (!ok) break;
-#pragma unroll
-            for (int g = 0; g < kSplit; ++g) mx = fmaxf(mx, slot[g * 128 + row]);
         }
         if (!ok) break;
         const bool need = mx > m_used + kRescaleThreshold;
@@ -737,16 +675,15 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
             const float alpha = need ? tc::ex2(m_used - m_new) : 1.f;  // 0 on the first visible tile
             if (need) m_used = m_new;
             if (n_act > 0) {
-                // this warpgroup's columns of O (16 at a time when split: the S row is still live)
-                constexpr int kW = kSplit > 1 ? 16 : 32;
+                // O, 32 columns at a time (the S row is still live in registers)
 #pragma unroll 1
-                for (int oc = hf * (HD / kW) / kSplit; oc < (hf + 1) * (HD / kW) / kSplit; ++oc) {
-                    uint32_t o[kW];
-                    tmem_ldw(tO + oc * kW, o);
+                for (int oc = 0; oc < HD / 32; ++oc) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tO + oc * 32, o);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < kW; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
-                    tmem_stw(tO + oc * kW, o);
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
+                    tc::tmem_st32(tO + oc * 32, o);
                 }
             }
             l *= alpha;
@@ -758,7 +695,7 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
         for (int cc = 0; cc < kCh; ++cc) {
             uint32_t pk[16];
             chunk_exp(sr[cc], sl22, nmb2, sacc, pk);
-            tc::tmem_st16(tS + (hf * kCh + cc) * 16, pk);
+            tc::tmem_st16(tS + cc * 16, pk);
         }
         float s0, s1;
         tc::unpack2(sacc, s0, s1);
@@ -771,33 +708,24 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
         ++ns;
     }
     if (!ok) return false;
-    if (kSplit > 1) {
-        // the row sum is the sum of the warpgroups' shares
-        float *ls = xt + (2 + (k & 1u)) * kSplit * 128;  // by unit parity: a partner may still read the last one
-        ls[hf * 128 + row] = l;
-        pair_sync(i);
-        l = 0.f;
-#pragma unroll
-        for (int g = 0; g < kSplit; ++g) l += ls[g * 128 + row];
-    }
-    // ---- epilogue: normalise, merge (ACCUM), store this warpgroup's columns ------------------
+    // ---- epilogue: normalise, merge (ACCUM), store ------------------
     const size_t grow = (size_t)w.q_row_base + row_local;
     const float lse_cur = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     float w_old = 0.f, w_new = 1.f, lse_out = lse_cur;
     if (p.mode == USP_MODE_ACCUM && row_ok) merge_weights(p.lse[grow], lse_cur, w_old, w_new, lse_out);
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16 *orow = p.out + grow * HD;
-    constexpr int kOc = (HD / 32) / kSplit;  // 32-column chunks of O per warpgroup
+    constexpr int kOc = HD / 32;  // 32-column chunks of O
     if (n_act > 0) {
         ok = tc::mbar_wait(barO, no & 1u, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) return false;
         ++no;
         tc::fence_after_sync();
-        // all of this warpgroup's O columns in one round trip, then O_i goes back to the issuer
+        // all of O's columns in one round trip, then O_i goes back to the issuer
         uint32_t o[kOc][32];
 #pragma unroll
-        for (int oc = 0; oc < kOc; ++oc) tc::tmem_ld32(tO + (hf * kOc + oc) * 32, o[oc]);
+        for (int oc = 0; oc < kOc; ++oc) tc::tmem_ld32(tO + oc * 32, o[oc]);
         tc::tmem_ld_wait();
         tc::fence_before_sync();
         __syncwarp();
@@ -808,7 +736,7 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
                 float v[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = u2f(o[oc][e]) * inv_l;
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + (hf * kOc + oc) * 32);
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + oc * 32);
                 if (p.mode == USP_MODE_ACCUM) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -836,21 +764,20 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
     } else if (row_ok && p.mode != USP_MODE_ACCUM) {
         // no visible key in this pass: the empty partial (0, -inf)
         uint4 *dst = reinterpret_cast<uint4 *>(orow);
-        for (int q = hf * (HD / 8) / kSplit; q < (hf + 1) * (HD / 8) / kSplit; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+        for (int q = 0; q < HD / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
     }
-    if (row_ok && hf == 0) p.lse[grow] = lse_out;
+    if (row_ok) p.lse[grow] = lse_out;
     return true;
 }
 
 template <int HD, bool PK>
-__device__ void softmax_role(const TcParams &p, uint32_t cu_s, uint32_t bar0, uint32_t tmem, int i, int hf,
-                             float *xch) {
+__device__ void softmax_role(const TcParams &p, uint32_t cu_s, uint32_t bar0, uint32_t tmem, int i) {
     uint32_t ns = 0, no = 0;
     for (uint32_t k = 0;; ++k) {
         uint32_t x;
         if (!unit_index(p, k, x)) break;
         const Work w = decode_work<PK>(p, cu_s, x);
-        if (!softmax_unit<HD, PK>(p, cu_s, w, bar0, tmem, i, hf, xch, k, ns, no)) return;
+        if (!softmax_unit<HD, PK>(p, cu_s, w, bar0, tmem, i, ns, no)) return;
     }
 }
 
@@ -879,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         tc::mbar_init(bar0 + 8u * C::Q_FULL, 1);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(bar0 + 8u * (C::S_FULL + i), 1);
-            tc::mbar_init(bar0 + 8u * (C::P_FULL + i), 4 * kSplit);  // one arrive per softmax warp
+            tc::mbar_init(bar0 + 8u * (C::P_FULL + i), 4);  // one arrive per softmax warp
             tc::mbar_init(bar0 + 8u * (C::O_FULL + i), 1);
         }
         tc::mbar_init(bar0 + 8u * C::DONE, 1);
@@ -887,8 +814,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         tc::mbar_init(bar0 + 8u * C::TURN, 1);
         tc::mbar_init(bar0 + 8u * (C::TURN + 1), 1);
         tc::mbar_init(bar0 + 8u * C::Q_EMPTY, 2);  // one commit per MMA issuer
-        tc::mbar_init(bar0 + 8u * C::O_EMPTY, 4 * kSplit);  // one arrive per softmax warp
-        tc::mbar_init(bar0 + 8u * (C::O_EMPTY + 1), 4 * kSplit);
+        tc::mbar_init(bar0 + 8u * C::O_EMPTY, 4);  // one arrive per softmax warp
+        tc::mbar_init(bar0 + 8u * (C::O_EMPTY + 1), 4);
         tc::fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -928,11 +855,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-        // warpgroup g: Q tile g / kSplit, column share g % kSplit
-        const int g = warp >> 2;
-        if (!skip)
-            softmax_role<HD, PK>(p, cu_s, bar0, tmem, g / kSplit, g % kSplit,
-                                 reinterpret_cast<float *>(smem + C::kXch));
+        // warpgroup i: Q tile i
+        if (!skip) softmax_role<HD, PK>(p, cu_s, bar0, tmem, warp >> 2);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -958,7 +882,7 @@ int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
         // build whose register count would make the warpgroup split wait forever
         cudaFuncAttributes fa{};
         if (cudaFuncGetAttributes(&fa, attn_tc_kernel<HD, PK>) != cudaSuccess) return USP_ERR_CUDA;
-        if ((long)fa.numRegs * kThreads < 2L * kSplit * 128 * kSoftmaxRegs + 128L * kControlRegs)
+        if ((long)fa.numRegs * kThreads < 2L * 128 * kSoftmaxRegs + 128L * kControlRegs)
             return USP_ERR_UNSUPPORTED;
         if (cudaFuncSetAttribute(attn_tc_kernel<HD, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
             cudaSuccess)
