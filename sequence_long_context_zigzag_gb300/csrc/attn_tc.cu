@@ -193,10 +193,9 @@ __device__ __forceinline__ Work decode_work(const TcParams &p, uint32_t cu_s, ui
     // Units that read the same K/V (one local KV head of one Ulysses rank and batch element: a
     // group of Gl query heads x nouter 256-row blocks) are numbered in super-groups of sg groups.
     // Inside a super-group the blocks go heaviest first (outer), each block across the super-group's
-    // heads. When every head's K/V fits in L2 together, one super-group holds all heads (the SMs
-    // spread their reads over all heads' K/V); otherwise a super-group's K/V is kept to half of L2,
-    // so the SMs work on few heads at a time and read their K/V from L2 after the first touch, even
-    // though the static schedule lets units that share K/V drift apart in time.
+    // heads. sg is all groups unless a smaller super-group saves DRAM traffic (launch_attn_tc): then
+    // the SMs work on one or two heads at a time and read their K/V from L2 after the first touch,
+    // even though the static schedule lets units that share K/V drift apart in time.
     const uint32_t per_group = p.nouter * p.Gl;
     const uint32_t g0 = x / (p.sg * per_group) * p.sg;
     const uint32_t n = min(p.sg, p.ngroups - g0);
@@ -287,7 +286,7 @@ __device__ __forceinline__ void iter_init(const TcParams &p, const Work &w, Tile
     iter_setup<PK>(p, w, it);
 }
 
-// the next KV tile that at least one Q tile of the CTA needs (packed samples can leave gaps between
+// the next KV tile that at least one Q tile of the unit needs (packed samples can leave gaps between
 // the two Q tiles' key ranges; every role skips the same tiles)
 template <bool PK>
 __device__ __forceinline__ bool iter_next(const TcParams &p, const Work &w, TileIter &it, Tile &tl) {
