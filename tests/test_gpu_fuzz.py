@@ -1,0 +1,98 @@
+"""Seeded random shapes through the whole forward (split, all-to-all, ring attention, inverse) against
+the oracle, through the C ABI.
+
+The persistent tensor-core kernel carries its barrier phases, stage ring and tensor-memory hand-offs
+from one unit of 256 query rows into the next, and its units come in many kinds: no visible key,
+one KV tile, ragged Q tiles, packed samples that leave gaps, GQA groups and replicated K/V. Each case
+below draws a shape (batch, length, heads, head dim, ring and Ulysses degrees, causal or not, packed
+or not) from a seeded generator, runs usp_attention, and compares sampled rows with the oracle's
+direct attention; a few cases also fold the single ring steps (STEP, then ACCUM) back into the whole
+ring. Bars as elsewhere: out max-abs 2e-2, lse relative 1e-3 with denominator max(|lse|, 1)."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_long_context_zigzag_gb300 as usp
+from seeded_inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+OUT_TOL = 2e-2
+LSE_TOL = 1e-3
+N_CASES = 40
+
+
+def draw(seed):
+    rnd = random.Random(seed)
+    rd = rnd.choice([1, 2, 3, 4, 5])
+    ud = rnd.choice([1, 2, 4])
+    hd = rnd.choice([64, 128])
+    # query heads a multiple of ud; KV heads dividing them and either dividing by ud or dividing ud
+    while True:
+        hq = ud * rnd.choice([1, 2, 3, 4])
+        hkv = rnd.choice([h for h in range(1, hq + 1) if hq % h == 0])
+        if hkv % ud == 0 or ud % hkv == 0:
+            break
+    step = 2 * rd * ud
+    L = step * rnd.randint(max(1, 256 // step), max(2, 3072 // step))
+    bs = rnd.choice([1, 1, 2])
+    causal = rnd.random() < 0.8
+    cu = None
+    if rnd.random() < 0.3:
+        n = rnd.randint(2, 9)
+        cuts = sorted(rnd.sample(range(1, L), n - 1))
+        cu = [0] + cuts + [L]
+    return dict(bs=bs, L=L, hq=hq, hkv=hkv, hd=hd, ud=ud, rd=rd, causal=causal, cu=cu)
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_random_shape_matches_oracle(case):
+    c = draw(9000 + case)
+    q, k, v = make_qkv(c["bs"], c["L"], c["hq"], c["hkv"], c["hd"], "bf16", seed=9000 + case)
+    kw = {}
+    if c["cu"] is not None:
+        kw["cu_seqlens"] = torch.tensor(c["cu"], dtype=torch.int32, device="cuda")
+    out, lse = usp.usp_attention(q.cuda(), k.cuda(), v.cuda(), ud=c["ud"], rd=c["rd"], causal=c["causal"], **kw)
+    usp.usp_check()
+    rnd = random.Random(case)
+    L = c["L"]
+    rows = sorted(set(rnd.sample(range(L), min(L, 48)) + [0, L - 1]))
+    o_ref, l_ref = oracle.attn_direct(q, k, v, causal=c["causal"], rows=rows, cu_seqlens=c["cu"])
+    o = out[:, rows].float().cpu().numpy().astype(np.float64)
+    ls = lse[:, rows].cpu().numpy().astype(np.float64)
+    assert np.abs(o - o_ref).max() <= OUT_TOL, c
+    both_inf = np.isneginf(ls) & np.isneginf(l_ref)
+    d = np.where(both_inf, 0.0, np.abs(ls - l_ref) / np.maximum(np.abs(l_ref), 1.0))
+    assert float(np.nan_to_num(d, nan=np.inf).max()) <= LSE_TOL, c
+
+
+@pytest.mark.parametrize("case", range(0, N_CASES, 5))
+def test_random_shape_steps_fold_into_the_ring(case):
+    """Single ring steps merged in place (STEP, then ACCUM) give the whole-ring result."""
+    c = draw(9000 + case)
+    q, k, v = make_qkv(c["bs"], c["L"], c["hq"], c["hkv"], c["hd"], "bf16", seed=9000 + case)
+    rd, ud, L, bs, hd = c["rd"], c["ud"], c["L"], c["bs"], c["hd"]
+    Lr = L // rd
+    qh = torch.empty(rd, ud, c["hq"] // ud, bs, Lr, hd, device="cuda", dtype=torch.bfloat16)
+    kh = torch.empty(rd, ud, usp.heads_per_rank(c["hkv"], ud), bs, Lr, hd, device="cuda", dtype=torch.bfloat16)
+    vh = torch.empty_like(kh)
+    usp.usp_extract_a2a([q.cuda(), k.cuda(), v.cuda()], [qh, kh, vh], rd, ud)
+    kw = {}
+    if c["cu"] is not None:
+        kw["cu_seqlens"] = torch.tensor(c["cu"], dtype=torch.int32, device="cuda")
+    fo = torch.empty_like(qh)
+    fl = torch.empty(qh.shape[:5], device="cuda", dtype=torch.float32)
+    usp.usp_attn_fwd(qh, kh, vh, fo, fl, hkv=c["hkv"], causal=c["causal"], **kw)
+    ao = torch.empty_like(qh)
+    al = torch.empty_like(fl)
+    for t in range(rd):
+        usp.usp_attn_fwd(qh, kh, vh, ao, al, hkv=c["hkv"], causal=c["causal"],
+                         mode=usp.USP_MODE_STEP if t == 0 else usp.USP_MODE_ACCUM, step=t, **kw)
+    usp.usp_check()
+    assert (ao.float() - fo.float()).abs().max().item() <= OUT_TOL, c
+    fin = torch.isfinite(fl)
+    assert torch.equal(fin, torch.isfinite(al)), c
+    d = (al[fin] - fl[fin]).abs() / fl[fin].abs().clamp(min=1.0)
+    assert d.numel() == 0 or d.max().item() <= LSE_TOL, c
