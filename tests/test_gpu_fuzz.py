@@ -1,5 +1,5 @@
-"""Seeded random shapes through the whole forward (split, all-to-all, ring attention, inverse) against
-the oracle, through the C ABI.
+"""Seeded random shapes through the whole forward (split, all-to-all, ring attention, inverse) and
+the whole backward against the oracle, through the C ABI.
 
 The persistent tensor-core kernel carries its barrier phases, stage ring and tensor-memory hand-offs
 from one unit of 256 query rows into the next, and its units come in many kinds: no visible key,
@@ -7,7 +7,8 @@ one KV tile, ragged Q tiles, packed samples that leave gaps, GQA groups and repl
 below draws a shape (batch, length, heads, head dim, ring and Ulysses degrees, causal or not, packed
 or not) from a seeded generator, runs usp_attention, and compares sampled rows with the oracle's
 direct attention; a few cases also fold the single ring steps (STEP, then ACCUM) back into the whole
-ring. Bars as elsewhere: out max-abs 2e-2, lse relative 1e-3 with denominator max(|lse|, 1)."""
+ring; twelve smaller draws run the backward (dq, dk, dv). Bars as elsewhere: out max-abs 2e-2, lse
+relative 1e-3 with denominator max(|lse|, 1); gradients max|g - g_ref| / max(max|g_ref|, 1) 2e-2."""
 import random
 
 import numpy as np
@@ -96,3 +97,40 @@ def test_random_shape_steps_fold_into_the_ring(case):
     assert torch.equal(fin, torch.isfinite(al)), c
     d = (al[fin] - fl[fin]).abs() / fl[fin].abs().clamp(min=1.0)
     assert d.numel() == 0 or d.max().item() <= LSE_TOL, c
+
+
+def draw_bwd(seed):
+    """A smaller random shape for the backward (the oracle's gradients are full O(L^2) sums)."""
+    c = draw(seed)
+    rnd = random.Random(seed + 1)
+    step = 2 * c["rd"] * c["ud"]
+    c["L"] = step * rnd.randint(max(1, 256 // step), max(2, 1536 // step))
+    if c["cu"] is not None:
+        n = rnd.randint(2, 6)
+        cuts = sorted(rnd.sample(range(1, c["L"]), n - 1))
+        c["cu"] = [0] + cuts + [c["L"]]
+    return c
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_shape_backward_matches_oracle(case):
+    """usp_forward then usp_backward (natural order in and out) against the oracle's fp64 gradients:
+    max|g - g_ref| / max(max|g_ref|, 1) <= 2e-2, the forward's out bound."""
+    c = draw_bwd(9500 + case)
+    bs, L, hq, hkv, hd = c["bs"], c["L"], c["hq"], c["hkv"], c["hd"]
+    q, k, v = make_qkv(bs, L, hq, hkv, hd, "bf16", seed=9500 + case)
+    g, _, _ = make_qkv(bs, L, hq, hkv, hd, "bf16", seed=9700 + case)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    kw = {}
+    if c["cu"] is not None:
+        kw["cu_seqlens"] = torch.tensor(c["cu"], dtype=torch.int32, device="cuda")
+    out = torch.empty_like(qd)
+    lse = torch.empty(bs, L, hq, device="cuda")
+    usp.usp_forward(qd, kd, vd, out, lse, c["ud"], c["rd"], causal=c["causal"], **kw)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    usp.usp_backward(qd, kd, vd, out, lse, gd, dq, dk, dv, c["ud"], c["rd"], causal=c["causal"], **kw)
+    usp.usp_check()
+    rq, rk, rv = oracle.attn_direct_bwd(q, k, v, g, causal=c["causal"], cu_seqlens=c["cu"])
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        err = np.abs(got.float().cpu().numpy().astype(np.float64) - ref).max() / max(np.abs(ref).max(), 1.0)
+        assert err <= OUT_TOL, (c, err)
