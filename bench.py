@@ -12,6 +12,7 @@ runs an independent replica: the virtual-rank grid lives inside one device, noth
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -43,7 +44,8 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about half a second of steps, at least 20)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -99,7 +101,9 @@ def load_peaks():
 # clocks during the timed region
 # ------------------------------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms from start() to stop(); stop(t0, t1) keeps the samples whose
+    timestamps fall inside the timed region [t0, t1] (host wall clock), or all of them if none do."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -113,12 +117,12 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
                  "-i", str(self.idx)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if not self.proc:
             return None
         self.proc.terminate()
@@ -126,25 +130,27 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx = max(mx, float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
                 except ValueError:
                     continue
-                for nm, val in zip(names, parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(nm)
         os.unlink(self.path)
-        if not sm:
+        inside = [r for r in rows if t0 is not None and t0 <= r[0] <= t1]
+        window = "timed region" if inside else "sampler run (no sample fell inside the timed region)"
+        use = inside or rows
+        if not use:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = sorted({nm for r in use for nm, val in zip(names, r[3]) if val.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "window": window}
 
 
 def gpu_index(local_rank):
@@ -383,12 +389,16 @@ def run_reference(args, dist):
     wi = args.workload
     w = WORKLOADS[wi]
     q, k, v = make_workload_qkv(w, default_seed(wi))
-    # a fixed bounded sample per step, sized for roughly 2 s of work on this host
+    if args.steps is None:
+        args.steps = 5
+    # a fixed bounded sample per step, sized so that the whole run takes about a minute and a half on
+    # this host (2 s per step at most)
+    per_step = min(2.0, max(0.05, 90.0 / (args.steps + args.warmup)))
     probe = list(range(w.L // 8, w.L, w.L // 4))[:4]
     t0 = time.perf_counter()
     oracle.attn_direct(q, k, v, causal=w.causal, rows=probe)
     per_row = max((time.perf_counter() - t0) / len(probe), 1e-6)
-    n = max(1, min(w.L, int(2.0 / per_row)))
+    n = max(1, min(w.L, int(per_step / per_row)))
     rows = list(range(0, w.L, max(1, w.L // n)))[:n]
     for _ in range(args.warmup):
         oracle.attn_direct(q, k, v, causal=w.causal, rows=rows)
@@ -453,21 +463,31 @@ def main():
     for _ in range(args.warmup):
         step.run()
     usp.usp_check()
+    if args.steps is None:
+        # about half a second of timed steps (at least 20), the same count on every rank
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step.run()
+        torch.cuda.synchronize()
+        args.steps = int(dist.max(min(2000.0, max(20.0, 0.5 / max(time.perf_counter() - t0, 1e-6)))))
 
     # ---- device-timed region ----------------------------------------------------------------
     sampler = ClockSampler(gpu_index(dist.local_rank))
     dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
+    time.sleep(0.3)  # nvidia-smi's start-up, so that its samples cover the timed region
     st = torch.cuda.current_stream()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
     ev0.record(st)
     for _ in range(args.steps):
         step.run(record=True)
     ev1.record(st)
     torch.cuda.synchronize()
+    t_wall1 = time.time()
     dist.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_wall0, t_wall1)
     usp.usp_check()
     t_step = ev0.elapsed_time(ev1) / 1e3 / args.steps
     t_step_max = dist.max(t_step)
@@ -510,7 +530,7 @@ def main():
     balance = rank_balance(usp, w, q, k, v) if w.rd > 1 else None
 
     # ---- the backward of one head group's ring attention (outside the timed region) ----------
-    backward = time_backward(usp, w, step, reps=max(3, args.steps // 2))
+    backward = time_backward(usp, w, step, reps=min(20, max(3, args.steps // 2)))
     packed = packing(usp, w, step)
 
     # ---- CPU baseline (the oracle on the host cores), rank 0 at N = 1 -----------------------
