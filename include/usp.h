@@ -334,6 +334,18 @@ USP_API size_t usp_backward_workspace_size(usp_attn_desc d, int head_chunk);
  * USP_OK, USP_ERR_TIMEOUT, or USP_ERR_CUDA if the synchronisation itself failed. */
 USP_API int usp_check(usp_stream_t stream);
 
+/*
+ * usp_selftest_timeout -- exercises the failure path of the bounded device-side waits without a
+ * fault: one CTA waits, through the same bounded mbarrier wait every kernel of this library uses, on
+ * a barrier nothing ever arrives on, for at most limit_us microseconds. The wait runs out, the kernel
+ * records USP_ERR_TIMEOUT in the device status word and returns; the context stays usable.
+ * usp_check then reports USP_ERR_TIMEOUT and clears the word; the tensor-core (bf16) attention
+ * kernels, the ones with device-side waits, do no work when launched while the word is set
+ * (usp_check reports the timeout for them too).
+ *   limit_us : 1 .. 1000000, else USP_ERR_INVALID_ARG.
+ */
+USP_API int usp_selftest_timeout(int64_t limit_us, usp_stream_t stream);
+
 /* Static, human-readable text for a status code. */
 USP_API const char *usp_strerror(int status);
 

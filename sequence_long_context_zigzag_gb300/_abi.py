@@ -95,6 +95,8 @@ def load():
     lib.usp_lse_merge.restype = ctypes.c_int
     lib.usp_check.argtypes = [vp]
     lib.usp_check.restype = ctypes.c_int
+    lib.usp_selftest_timeout.argtypes = [i64, vp]
+    lib.usp_selftest_timeout.restype = ctypes.c_int
     lib.usp_strerror.argtypes = [ctypes.c_int]
     lib.usp_strerror.restype = ctypes.c_char_p
     lib.usp_version.argtypes = []

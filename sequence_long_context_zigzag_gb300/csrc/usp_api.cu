@@ -2,6 +2,7 @@
 #include <math.h>
 #include <mutex>
 
+#include "tc_ptx.cuh"
 #include "usp_internal.cuh"
 
 // One status word per device: kernels whose bounded waits run out write a nonzero code here.
@@ -59,6 +60,20 @@ static int check_ptr_align(const void *a, const void *b, int64_t row_bytes) {
     if (!aligned(a, al) || !aligned(b, al)) return USP_ERR_ALIGN;
     return USP_OK;
 }
+
+namespace {
+// one thread waits (bounded) on an mbarrier that nothing arrives on: the wait runs out and records
+// USP_ERR_TIMEOUT, exactly as a stalled wait inside the attention kernels would
+__global__ void selftest_timeout_kernel(int *status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        const uint32_t b = tc::smem_u32(&bar);
+        tc::mbar_init(b, 1);
+        tc::fence_barrier_init();
+        tc::mbar_wait(b, 0, status, USP_ERR_TIMEOUT, limit_ns);
+    }
+}
+}  // namespace
 
 }  // namespace usp
 
@@ -252,6 +267,15 @@ int usp_lse_merge(void *o_acc, float *lse_acc, const void *o_new, const float *l
         return USP_ERR_ALIGN;
     return launch_lse_merge(o_acc, lse_acc, o_new, lse_new, rows, hd, dtype,
                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_selftest_timeout(int64_t limit_us, usp_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return USP_ERR_INVALID_ARG;
+    const DeviceInfo *di = device_info();
+    if (!di) return USP_ERR_CUDA;
+    usp::selftest_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(di->status,
+                                                                                  (uint64_t)limit_us * 1000ull);
+    return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA;
 }
 
 int usp_check(usp_stream_t stream) {

@@ -111,6 +111,12 @@ def test_attn_rejects(kw, code):
     assert _abi.load().usp_attn_fwd(BAD, BAD, BAD, BAD, BAD, desc(**kw), None) == code
 
 
+def test_selftest_timeout_rejects_limits():
+    lib = _abi.load()
+    assert lib.usp_selftest_timeout(0, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_selftest_timeout(1000001, None) == _abi.USP_ERR_INVALID_ARG
+
+
 def test_attn_null_and_empty():
     lib = _abi.load()
     assert lib.usp_attn_fwd(None, None, None, None, None, desc(), None) == _abi.USP_ERR_INVALID_ARG
