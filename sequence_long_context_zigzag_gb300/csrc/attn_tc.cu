@@ -448,10 +448,13 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 // issuer commits to Q_EMPTY (its S products of the unit were all issued in earlier bursts; once both
 // issuers' commits arrive, the producer loads the next unit's Q), and after the last PV it commits
 // O_FULL_i.
-// When tile j+1 opens a new unit, burst j is split in two turns, PV_i(j) and S_i(j+1), so that no
-// issuer waits for the new Q while holding its turn; and the first PV of a unit waits for O_EMPTY_i,
-// the softmax's read-out of the previous unit's O_i. A Q tile without a visible key in a unit takes
-// no O_FULL / O_EMPTY round (the softmax skips it too).
+// When tile j+1 opens a new unit, S_i(j+1) leaves the turn order: issuer i releases its turn after
+// PV_i(j), waits for the new Q and K(j+1) and issues S_i(j+1) at once, without waiting for the other
+// issuer's last PV (which waits for the other softmax's last tile), so the unit's first S products
+// run while the softmaxes finish the old unit; both issuers skip the turn there, so their turn
+// counts stay equal. The first PV of a unit waits for O_EMPTY_i, the softmax's read-out of the
+// previous unit's O_i. A Q tile without a visible key in a unit takes no O_FULL / O_EMPTY round (the
+// softmax skips it too).
 template <int HD, bool PK>
 __device__ void mma_role(const TcParams &p, uint32_t cu_s, uint32_t sbase, uint32_t bar0, uint32_t tmem, int i) {
     using C = Cfg<HD>;
@@ -536,9 +539,7 @@ __device__ void mma_role(const TcParams &p, uint32_t cu_s, uint32_t sbase, uint3
             if (!(ok = wait(C::Q_FULL, nq & 1u))) break;
             ++nq;
             if (!(ok = wait(C::K_FULL + stn, phn))) break;
-            if (!(ok = take_turn())) break;
             s_burst(nxt, stn);
-            tc::mbar_arrive(BAR(other_turn));
         }
         cur = nxt;
         have = have_n;
