@@ -127,8 +127,8 @@ USP_API int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_strea
 
 /*
  * usp_extract_a2a -- the zigzag split followed by AllToAll4D (steps a1 + a2) in one pass, for up to
- * four tensors (e.g. Q, K and V) in one launch; inverse != 0 runs AllToAll4D's inverse followed by
- * the inverse split (a5 + a7).
+ * four tensors (e.g. Q, K and V, or out and lse) in one launch; inverse != 0 runs AllToAll4D's
+ * inverse followed by the inverse split (a5 + a7).
  * Source: USP review, Algorithm 2 and section 三 (AllToAll4D). Composing the two maps gives
  *   head-sharded[r][u'][h'][b][p] = natural[b][zig(r, p)][h0 + u' Hl + h'],
  * i.e. row p of ring rank r is global token zig(r, p) (the all-to-all gathers the Ulysses ranks'
@@ -142,8 +142,9 @@ USP_API int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_strea
  *               inverse != 0: the other way round (with H < ud, the sum of each head's replicas,
  *               as usp_a2a4d dir = -1); heads outside the window of the natural tensor are left
  *               untouched.
- *   d         : HOST array of n dims; bs, L, rd, ud, hd and dtype must agree (USP_ERR_SHAPE
- *               otherwise); H, H_total and h0 may differ (Q and K/V head counts under GQA).
+ *   d         : HOST array of n dims; bs, L, rd, ud and split must agree (USP_ERR_SHAPE
+ *               otherwise); H, H_total and h0 may differ (Q and K/V head counts under GQA), and so
+ *               may hd and dtype (out rows of hd elements with lse rows of one fp32, hd = 1).
  * Alignment and overlap rules as for usp_extract_local.
  */
 USP_API int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_dims *d, int inverse,

@@ -144,7 +144,7 @@ def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int =
 def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=None, Hs=None, split="zigzag",
                     stream=None):
     """Zigzag split then AllToAll4D in one pass (inverse: AllToAll4D's inverse then the inverse split),
-    for up to four tensors in one launch. inverse=False: srcs[k] natural (bs, L, H_total, hd) (or
+    for up to four tensors in one launch (their rows may differ: out and lse go back together). inverse=False: srcs[k] natural (bs, L, H_total, hd) (or
     (bs, L, H_total) for lse) -> dsts[k] head-sharded [rd][ud][H/ud][bs][Lr](, hd) ([rd][ud][1]... with
     replicated heads when H < ud, as usp_a2a4d); inverse=True the other way round. Tensor k moves heads
     [h0s[k], h0s[k] + Hs[k]) of its natural tensor."""

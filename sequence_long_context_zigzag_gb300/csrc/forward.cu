@@ -152,14 +152,11 @@ int usp_forward(const void *q, const void *k, const void *v, void *out, float *l
         ad.hq = s.hc;
         ad.hkv = s.hkc;
         if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, stream))) return rc;
-        const void *os[1] = {oh};
-        void *od[1] = {out};
-        usp_dims odims[1] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype)};
-        if ((rc = usp_extract_a2a(1, os, od, odims, 1, stream))) return rc;
-        const void *ls[1] = {lh};
-        void *ld[1] = {lse};
-        usp_dims ldims[1] = {dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
-        if ((rc = usp_extract_a2a(1, ls, ld, ldims, 1, stream))) return rc;
+        // out and lse back to natural order in one launch
+        const void *os[2] = {oh, lh};
+        void *od[2] = {out, lse};
+        usp_dims odims[2] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype), dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
+        if ((rc = usp_extract_a2a(2, os, od, odims, 1, stream))) return rc;
     }
     return USP_OK;
 }
@@ -228,14 +225,10 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
         ad.hkv = s.hkc;
         if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, cs))) return rc;
         if (g >= 2) chk(cudaStreamWaitEvent(hp.comp, hp.out_free[sl], 0) == cudaSuccess);
-        const void *os[1] = {oh};
-        void *od[1] = {out_o[sl]};
-        usp_dims odims[1] = {dims_of(s, s.hc, s.hc, 0, s.hd, d.dtype)};
-        if ((rc = usp_extract_a2a(1, os, od, odims, 1, cs))) return rc;
-        const void *ls[1] = {lh};
-        void *ldst[1] = {lse_all};
-        usp_dims ldims[1] = {dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
-        if ((rc = usp_extract_a2a(1, ls, ldst, ldims, 1, cs))) return rc;
+        const void *os[2] = {oh, lh};
+        void *od[2] = {out_o[sl], lse_all};
+        usp_dims odims[2] = {dims_of(s, s.hc, s.hc, 0, s.hd, d.dtype), dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
+        if ((rc = usp_extract_a2a(2, os, od, odims, 1, cs))) return rc;
         chk(cudaEventRecord(hp.out_ready[sl], hp.comp) == cudaSuccess);
         // device -> host: this group's output window
         chk(cudaStreamWaitEvent(hp.d2h, hp.out_ready[sl], 0) == cudaSuccess);

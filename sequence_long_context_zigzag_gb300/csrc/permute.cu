@@ -14,10 +14,12 @@
 //
 // Work split: one warp owns a batch of 32 logical rows. Lane l computes the source and destination
 // row of row l of the batch (integer index math with multiply-high division), publishes them in
-// shared memory, then the warp copies the whole batch with lane-consecutive 16-byte vectors, so each
-// load and store instruction covers contiguous row segments (a 256-byte row is one half-warp).
-// Loads are issued in groups of 8 before their stores to keep enough bytes in flight for HBM.
-// Up to four tensors (e.g. Q, K and V) share one launch; batches are numbered across them.
+// shared memory, then the warp copies the whole batch with lane-consecutive 16-byte vectors (4-byte
+// words for rows that are not a multiple of 16 bytes, such as lse), so each load and store
+// instruction covers contiguous row segments (a 256-byte row is one half-warp). Loads are issued in
+// groups of 8 before their stores to keep enough bytes in flight for HBM. Up to four tensors (e.g.
+// Q, K and V, or out and lse) share one launch; batches are numbered across them, and each tensor
+// has its own row size.
 #include "usp_device.cuh"
 #include "usp_internal.cuh"
 
@@ -29,7 +31,9 @@ struct PermJobK {
     char *dst;
     uint32_t nrows, batch0;  // logical rows; first warp batch of this tensor
     uint32_t H, Ht, h0, Hl;
+    uint32_t vec16, vpr;       // copy units: 16-byte vectors (vec16) or 4-byte words; units per row
     FastDiv f_H, f_Hl, f_rep;  // f_rep: ranks sharing one head (1 unless H < ud in a forward a2a)
+    FastDiv f_vpr;
 };
 
 struct PermK {
@@ -38,8 +42,7 @@ struct PermK {
     uint32_t nbatch;  // total warp batches over all tensors
     uint32_t bs, L, rd, ud, Lu, Lr, c;
     int r_fixed, u_fixed;
-    uint32_t vpr;  // units (16-byte vectors or 4-byte words) per row
-    FastDiv f_vpr, f_Lu, f_bs, f_ud, f_Lr;
+    FastDiv f_Lu, f_bs, f_ud, f_Lr;
 };
 
 // map logical row i of tensor j to (source row, destination row) in units of rows
@@ -99,13 +102,38 @@ __device__ __forceinline__ T load_stream(const T *p) { return __ldcs(p); }
 constexpr int kWarps = 8;
 constexpr int kGroup = 8;
 
-template <typename T>  // T = uint4 (16-byte units) or unsigned int (4-byte units)
+// the warp's batch of rows_here rows, in units U (uint4: 16-byte vectors, unsigned int: 4-byte words)
+template <typename U>
+__device__ __forceinline__ void copy_batch(const PermJobK &jb, const int64_t *s_src, const int64_t *s_dst,
+                                           uint32_t rows_here, int lane) {
+    const uint32_t units_here = rows_here * jb.vpr;
+    const U *src = reinterpret_cast<const U *>(jb.src);
+    U *dst = reinterpret_cast<U *>(jb.dst);
+    for (uint32_t base = 0; base < units_here; base += 32 * kGroup) {
+        U buf[kGroup];
+        int64_t doff[kGroup];
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+            const uint32_t v = base + k * 32 + lane;
+            doff[k] = -1;
+            if (v < units_here) {
+                uint32_t rr, col;
+                jb.f_vpr.divmod(v, rr, col);
+                buf[k] = load_stream(src + s_src[rr] * jb.vpr + col);
+                doff[k] = s_dst[rr] * jb.vpr + col;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k)
+            if (doff[k] >= 0) dst[doff[k]] = buf[k];
+    }
+}
+
 __global__ void __launch_bounds__(kWarps * 32) permute_rows_kernel(const __grid_constant__ PermK p) {
     __shared__ int64_t s_src[kWarps][32];
     __shared__ int64_t s_dst[kWarps][32];
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
-    const uint32_t total_units = 32u * p.vpr;
     for (uint32_t batch = blockIdx.x * kWarps + w; batch < p.nbatch; batch += gridDim.x * kWarps) {
         int jx = 0;
 #pragma unroll
@@ -121,27 +149,8 @@ __global__ void __launch_bounds__(kWarps * 32) permute_rows_kernel(const __grid_
         s_dst[w][lane] = dr;
         __syncwarp();
         const uint32_t rows_here = min(32u, jb.nrows - row0);
-        const uint32_t units_here = rows_here * p.vpr;
-        const T *src = reinterpret_cast<const T *>(jb.src);
-        T *dst = reinterpret_cast<T *>(jb.dst);
-        for (uint32_t base = 0; base < total_units; base += 32 * kGroup) {
-            T buf[kGroup];
-            int64_t doff[kGroup];
-#pragma unroll
-            for (int k = 0; k < kGroup; ++k) {
-                const uint32_t v = base + k * 32 + lane;
-                doff[k] = -1;
-                if (v < units_here) {
-                    uint32_t rr, col;
-                    p.f_vpr.divmod(v, rr, col);
-                    buf[k] = load_stream(src + s_src[w][rr] * p.vpr + col);
-                    doff[k] = s_dst[w][rr] * p.vpr + col;
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kGroup; ++k)
-                if (doff[k] >= 0) dst[doff[k]] = buf[k];
-        }
+        if (jb.vec16) copy_batch<uint4>(jb, s_src[w], s_dst[w], rows_here, lane);
+        else copy_batch<unsigned int>(jb, s_src[w], s_dst[w], rows_here, lane);
         __syncwarp();
     }
 }
@@ -208,7 +217,7 @@ __global__ void __launch_bounds__(256) replica_sum_kernel(const __grid_constant_
 }
 
 int launch_replica_sum(const PermArgs &a, const PermJob &j, int sms, cudaStream_t s) {
-    if (a.row_bytes % 16 != 0 || (a.dtype != USP_BF16 && a.dtype != USP_F32)) return USP_ERR_UNSUPPORTED;
+    if (j.row_bytes % 16 != 0 || (j.dtype != USP_BF16 && j.dtype != USP_F32)) return USP_ERR_UNSUPPORTED;
     RepSumK p{};
     p.src = j.src;
     p.dst = j.dst;
@@ -224,7 +233,7 @@ int launch_replica_sum(const PermArgs &a, const PermJob &j, int sms, cudaStream_
     p.Lr = (uint32_t)(a.L / a.rd);
     p.Lu = p.Lr / p.ud;
     p.c = (uint32_t)(a.L / (2 * a.rd));
-    p.vpr = (uint32_t)(a.row_bytes / 16);
+    p.vpr = (uint32_t)(j.row_bytes / 16);
     const int64_t nvec = (int64_t)a.rd * p.Lr * a.bs * j.H * p.vpr;
     if (nvec == 0) return USP_OK;
     if (nvec >= (int64_t(1) << 31)) return USP_ERR_UNSUPPORTED;
@@ -236,7 +245,7 @@ int launch_replica_sum(const PermArgs &a, const PermJob &j, int sms, cudaStream_
     p.f_vpr = FastDiv(p.vpr);
     int64_t blocks = (nvec + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-    replica_sum_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, a.dtype == USP_BF16 ? 1 : 0);
+    replica_sum_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, j.dtype == USP_BF16 ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA;
 }
 
@@ -275,9 +284,6 @@ int launch_permute(const PermArgs &a, cudaStream_t s) {
     p.c = (uint32_t)(a.L / (2 * a.rd));
     p.r_fixed = a.r_fixed;
     p.u_fixed = a.u_fixed;
-    const bool vec16 = (a.row_bytes % 16) == 0;
-    p.vpr = (uint32_t)(a.row_bytes / (vec16 ? 16 : 4));
-    if ((int64_t)32 * p.vpr >= (int64_t(1) << 31)) return USP_ERR_UNSUPPORTED;
     const int64_t ranks = (a.r_fixed >= 0) ? 1 : (int64_t)a.rd * a.ud;
     const bool to_heads = a.mode == PERM_A2A_FWD || a.mode == PERM_FUSED_FWD;
     int64_t nbatch = 0;
@@ -287,6 +293,12 @@ int launch_permute(const PermArgs &a, cudaStream_t s) {
         jk.src = j.src;
         jk.dst = j.dst;
         jk.H = (uint32_t)j.H;
+        const bool vec16 = (j.row_bytes % 16) == 0;
+        const int64_t vpr = j.row_bytes / (vec16 ? 16 : 4);
+        if (vpr < 1 || 32 * vpr >= (int64_t(1) << 31)) return USP_ERR_UNSUPPORTED;
+        jk.vec16 = vec16 ? 1u : 0u;
+        jk.vpr = (uint32_t)vpr;
+        jk.f_vpr = FastDiv(jk.vpr);
         jk.Ht = (uint32_t)j.H_total;
         jk.h0 = (uint32_t)j.h0;
         // a forward all-to-all of fewer heads than Ulysses ranks replicates: one head per rank
@@ -306,7 +318,6 @@ int launch_permute(const PermArgs &a, cudaStream_t s) {
     if (nbatch == 0) return USP_OK;
     if (nbatch >= (int64_t(1) << 31)) return USP_ERR_UNSUPPORTED;
     p.nbatch = (uint32_t)nbatch;
-    p.f_vpr = FastDiv(p.vpr);
     p.f_Lu = FastDiv(p.Lu);
     p.f_bs = FastDiv(p.bs);
     p.f_ud = FastDiv(p.ud);
@@ -314,10 +325,7 @@ int launch_permute(const PermArgs &a, cudaStream_t s) {
     int64_t blocks = (nbatch + kWarps - 1) / kWarps;
     const int64_t cap = (int64_t)di->sm_count * 8;
     if (blocks > cap) blocks = cap;
-    if (vec16)
-        permute_rows_kernel<uint4><<<(unsigned)blocks, kWarps * 32, 0, s>>>(p);
-    else
-        permute_rows_kernel<unsigned int><<<(unsigned)blocks, kWarps * 32, 0, s>>>(p);
+    permute_rows_kernel<<<(unsigned)blocks, kWarps * 32, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA;
 }
 

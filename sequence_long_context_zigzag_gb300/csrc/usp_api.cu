@@ -108,12 +108,11 @@ int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, int invers
     PermArgs a{};
     a.njobs = 1;
     a.job[0] = PermJob{static_cast<const char *>(src), static_cast<char *>(dst), d.H, d.H_total ? d.H_total : d.H,
-                       d.h0};
+                       d.h0, row_bytes, d.dtype};
     a.mode = inverse ? PERM_EXTRACT_INV : PERM_EXTRACT;
     a.split = d.split;
-    a.dtype = d.dtype;
     a.bs = d.bs; a.L = d.L;
-    a.rd = d.rd; a.ud = d.ud; a.row_bytes = row_bytes;
+    a.rd = d.rd; a.ud = d.ud;
     a.r_fixed = vr >= 0 ? vr / d.ud : -1;
     a.u_fixed = vr >= 0 ? vr % d.ud : -1;
     return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
@@ -130,11 +129,10 @@ int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stre
     PermArgs a{};
     a.njobs = 1;
     a.job[0] = PermJob{static_cast<const char *>(src), static_cast<char *>(dst), d.H, d.H_total ? d.H_total : d.H,
-                       d.h0};
+                       d.h0, row_bytes, d.dtype};
     a.mode = dir > 0 ? PERM_A2A_FWD : PERM_A2A_INV;
-    a.dtype = d.dtype;
     a.bs = d.bs; a.L = d.L;
-    a.rd = d.rd; a.ud = d.ud; a.row_bytes = row_bytes;
+    a.rd = d.rd; a.ud = d.ud;
     a.r_fixed = -1; a.u_fixed = -1;
     return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -152,25 +150,22 @@ int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_d
         const usp_dims &dk = d[k];
         int rc = check_dims(dk, 2);
         if (rc) return rc;
-        if (dk.bs != d[0].bs || dk.L != d[0].L || dk.rd != d[0].rd || dk.ud != d[0].ud || dk.hd != d[0].hd ||
-            dk.dtype != d[0].dtype || dk.split != d[0].split)
+        if (dk.bs != d[0].bs || dk.L != d[0].L || dk.rd != d[0].rd || dk.ud != d[0].ud || dk.split != d[0].split)
             return USP_ERR_SHAPE;
         work += dk.bs * dk.L * (int64_t)dk.H;
         a.job[k] = PermJob{static_cast<const char *>(src[k]), static_cast<char *>(dst[k]), dk.H,
-                           dk.H_total ? dk.H_total : dk.H, dk.h0};
+                           dk.H_total ? dk.H_total : dk.H, dk.h0, (int64_t)dk.hd * elem_size(dk.dtype), dk.dtype};
     }
     if (work == 0) return USP_OK;
-    const int64_t row_bytes = (int64_t)d[0].hd * elem_size(d[0].dtype);
     for (int k = 0; k < n; ++k) {
         if (d[k].H == 0) continue;
         if (!src[k] || !dst[k]) return USP_ERR_INVALID_ARG;
-        int rc = check_ptr_align(src[k], dst[k], row_bytes);
+        int rc = check_ptr_align(src[k], dst[k], a.job[k].row_bytes);
         if (rc) return rc;
     }
     a.split = d[0].split;
-    a.dtype = d[0].dtype;
     a.bs = d[0].bs; a.L = d[0].L;
-    a.rd = d[0].rd; a.ud = d[0].ud; a.row_bytes = row_bytes;
+    a.rd = d[0].rd; a.ud = d[0].ud;
     return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -117,12 +117,14 @@ enum PermMode {
 
 constexpr int kMaxPermJobs = 4;
 
-// One tensor moved by a permute launch; every tensor of a launch shares the mode, the grid and the
-// row size, and may differ in its head window.
+// One tensor moved by a permute launch; every tensor of a launch shares the mode and the grid, and
+// may differ in its head window and its row (e.g. out rows of hd elements and lse rows of one fp32).
 struct PermJob {
     const char *src;
     char *dst;
     int32_t H, H_total, h0;
+    int64_t row_bytes;  // bytes of one (token, head) row: a multiple of 4
+    int32_t dtype;      // element type (the replica sum of an inverse all-to-all adds values)
 };
 
 struct PermArgs {
@@ -133,8 +135,6 @@ struct PermArgs {
     int64_t bs, L;
     int32_t rd, ud;
     int32_t r_fixed, u_fixed;  // >= 0 when only one virtual rank takes part (extract only)
-    int64_t row_bytes;
-    int32_t dtype;             // element type (the replica sum of an inverse all-to-all adds values)
 };
 int launch_permute(const PermArgs &a, cudaStream_t s);
 

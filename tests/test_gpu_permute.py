@@ -174,3 +174,30 @@ def test_fused_head_windows_and_lse_rows():
     got = bits(lse_nat)
     assert np.array_equal(got[:, :, 6:], want) and not got[:, :, :6].any()
     usp.usp_check()
+
+
+@pytest.mark.parametrize("dtype,hd,rd,ud,bs,L", [(torch.bfloat16, 128, 4, 2, 1, 1024), (torch.float32, 64, 3, 2, 2, 768),
+                                                (torch.bfloat16, 64, 5, 1, 1, 1000)])
+def test_out_and_lse_rows_in_one_launch(dtype, hd, rd, ud, bs, L):
+    """out (rows of hd elements) and lse (rows of one fp32) back to natural order in one launch, for a
+    head window of wider natural tensors: equal to the oracle's inverse all-to-all then inverse split
+    of each, and to one launch per tensor; heads outside the window untouched."""
+    Ht, h0, H = 3 * ud, ud, 2 * ud
+    Lr = L // rd
+    o_hs = rand((rd, ud, H // ud, bs, Lr, hd), dtype, seed=L + hd)
+    l_hs = rand((rd, ud, H // ud, bs, Lr), torch.float32, seed=L + 1)
+    od, ld = o_hs.to(DEV), l_hs.to(DEV)
+    o_nat = torch.zeros(bs, L, Ht, hd, dtype=dtype, device=DEV)
+    l_nat = torch.zeros(bs, L, Ht, device=DEV)
+    usp.usp_extract_a2a([od, ld], [o_nat, l_nat], rd, ud, inverse=True, h0s=[h0, h0], Hs=[H, H])
+    o_want = oracle.extract_inverse(oracle.a2a_inv(bits(o_hs), ud), L, rd, ud)
+    l_want = oracle.extract_inverse(oracle.a2a_inv(bits(l_hs)[..., None], ud), L, rd, ud)[..., 0]
+    og, lg = bits(o_nat), bits(l_nat)
+    assert np.array_equal(og[:, :, h0:h0 + H], o_want) and np.array_equal(lg[:, :, h0:h0 + H], l_want)
+    assert not og[:, :, :h0].any() and not og[:, :, h0 + H:].any()
+    assert not lg[:, :, :h0].any() and not lg[:, :, h0 + H:].any()
+    o1, l1 = torch.zeros_like(o_nat), torch.zeros_like(l_nat)
+    usp.usp_extract_a2a([od], [o1], rd, ud, inverse=True, h0s=[h0], Hs=[H])
+    usp.usp_extract_a2a([ld], [l1], rd, ud, inverse=True, h0s=[h0], Hs=[H])
+    assert torch.equal(o1, o_nat) and torch.equal(l1, l_nat)
+    usp.usp_check()
