@@ -153,6 +153,12 @@ def test_extract_a2a_rejects():
     # a head count the Ulysses degree does not divide
     assert lib.usp_extract_a2a(1, two, two, (_abi.UspDims * 1)(dims(H=3)), 0, None) == _abi.USP_ERR_SHAPE
     assert lib.usp_extract_a2a(2, two, two, (_abi.UspDims * 2)(dims(), dims(H=2)), 0, None) == _abi.USP_ERR_ALIGN
+    # rows may differ between the tensors of one launch (out with lse): past the shape checks, the
+    # misaligned pointers are what is rejected
+    out_lse = (_abi.UspDims * 2)(dims(), dims(hd=1, dtype=_abi.USP_F32))
+    assert lib.usp_extract_a2a(2, two, two, out_lse, 1, None) == _abi.USP_ERR_ALIGN
+    # but not the split
+    assert lib.usp_extract_a2a(2, two, two, (_abi.UspDims * 2)(dims(), dims(split=1)), 1, None) == _abi.USP_ERR_SHAPE
 
 
 def test_forward_workspace_and_rejects():
