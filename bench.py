@@ -175,7 +175,7 @@ class Step:
         hc = w.head_chunk or w.hq
         G = w.hq // w.hkv
         hkc = hc // G
-        Lr = L // rd
+        Lu, Lr = L // (rd * ud), L // rd
         dev, dt = q.device, q.dtype
         self.groups = [(g0, g0 // G) for g0 in range(0, w.hq, hc)]
         self.hc, self.hkc = hc, hkc
@@ -185,8 +185,8 @@ class Step:
         self.vh = torch.empty_like(self.kh)
         self.oh = torch.empty_like(self.qh)
         self.lh = torch.empty(rd, ud, hc // ud, bs, Lr, device=dev, dtype=torch.float32)
-        self.o_nat = torch.empty(bs, L, w.hq, hd, device=dev, dtype=dt)
-        self.l_nat = torch.empty(bs, L, w.hq, device=dev, dtype=torch.float32)
+        self.o_loc = torch.empty(rd, ud, bs, Lu, w.hq, hd, device=dev, dtype=dt)
+        self.l_loc = torch.empty(rd, ud, bs, Lu, w.hq, device=dev, dtype=torch.float32)
         es = q.element_size()
         # algorithmic permute bytes per step: one read + one write of every moved tensor (the composed
         # split + all-to-all reads and writes each of Q, K, V once; replicated K/V heads are read once
@@ -215,9 +215,9 @@ class Step:
             if record:
                 e2 = torch.cuda.Event(enable_timing=True)
                 e2.record(st)
-            # AllToAll4D's inverse and the inverse split of out and lse, one launch
-            usp.usp_extract_a2a([self.oh, self.lh], [self.o_nat, self.l_nat], rd, ud, inverse=True,
-                                h0s=[g0, g0], Hs=[self.hc, self.hc])
+            # AllToAll4D's inverse of out and lse, one launch
+            usp.usp_a2a4d_multi([self.oh, self.lh], [self.o_loc, self.l_loc], rd, ud, -1, h0s=[g0, g0],
+                                Hs=[self.hc, self.hc])
             if record:
                 e3 = torch.cuda.Event(enable_timing=True)
                 e3.record(st)
@@ -543,7 +543,7 @@ def main():
         peak = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
         hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
         ws_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, step.qh, step.kh, step.vh, step.oh,
-                                                                step.o_nat))
+                                                                step.o_loc))
         line = {
             "metric": "fwd causal-adjusted attention TFLOP/s (bf16) and % of GB300 dense peak; permute GB/s",
             "value": dist.world * flops / t_step_max / 1e12,

@@ -126,6 +126,21 @@ USP_API int usp_extract_local(const void *src, void *dst, usp_dims d, int vr, in
 USP_API int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stream);
 
 /*
+ * usp_a2a4d_multi -- usp_a2a4d for up to four tensors in one launch (e.g. step a5 of out and lse
+ * together). Source: as usp_a2a4d.
+ *
+ *   n         : number of tensors, 1 <= n <= 4
+ *   src, dst  : HOST arrays of n DEVICE pointers, each pair as src / dst of usp_a2a4d.
+ *   d         : HOST array of n dims; bs, L, rd and ud must agree (USP_ERR_SHAPE otherwise); H,
+ *               H_total, h0, hd and dtype may differ (out rows of hd elements with lse rows, hd = 1).
+ *   dir       : +1 or -1 for every tensor, as usp_a2a4d.
+ * Bit-exactly the result of one usp_a2a4d call per tensor. Alignment and overlap rules as for
+ * usp_extract_local, per tensor.
+ */
+USP_API int usp_a2a4d_multi(int n, const void *const *src, void *const *dst, const usp_dims *d, int dir,
+                            usp_stream_t stream);
+
+/*
  * usp_extract_a2a -- the zigzag split followed by AllToAll4D (steps a1 + a2) in one pass, for up to
  * four tensors (e.g. Q, K and V, or out and lse) in one launch; inverse != 0 runs AllToAll4D's
  * inverse followed by the inverse split (a5 + a7).

@@ -23,7 +23,7 @@ from . import _abi
 from ._abi import (USP_BF16, USP_F32, USP_MODE_ACCUM, USP_MODE_FUSED, USP_MODE_STEP, UspAttnDesc, UspDims,
                    UspError)
 
-__all__ = ["usp_extract_local", "usp_a2a4d", "usp_extract_a2a", "usp_attn_fwd", "usp_lse_merge", "usp_check", "usp_attention",
+__all__ = ["usp_extract_local", "usp_a2a4d", "usp_a2a4d_multi", "usp_extract_a2a", "usp_attn_fwd", "usp_lse_merge", "usp_check", "usp_attention",
            "usp_attention_host", "usp_forward", "usp_forward_host", "usp_forward_workspace_size",
            "usp_forward_noalloc", "heads_per_rank",
            "usp_attn_bwd_delta", "usp_attn_bwd", "usp_backward", "usp_backward_workspace_size", "UspAttentionFunction",
@@ -112,13 +112,7 @@ def heads_per_rank(H: int, ud: int) -> int:
     return 1 if ud % H == 0 else 0
 
 
-def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int = 1, h0: int = 0,
-              H: Optional[int] = None, stream=None) -> torch.Tensor:
-    """AllToAll4D inside every Ulysses group: dir=+1 sequence-sharded [rd][ud][bs][Lu][H_total][hd]
-    -> head-sharded [rd][ud][H/ud][bs][Lr][hd]; dir=-1 back. lse tensors drop the trailing hd axis.
-    dir=+1 with H < ud (ud % H == 0, K/V under GQA/MQA) replicates: head-sharded is
-    [rd][ud][1][bs][Lr][hd], rank u' holding head u' // (ud // H); dir=-1 then sums each head's
-    replicas (the adjoint, for gradients)."""
+def _a2a4d_dims(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int, h0: int, H: Optional[int]):
     _dev(src, dst)
     seq, hs = (src, dst) if dir > 0 else (dst, src)
     _need(seq.dtype == hs.dtype, "dtype mismatch")
@@ -135,10 +129,36 @@ def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int =
     _need(Hl > 0, "heads must divide by ud or divide ud")
     L = Lu * ud * rd
     _need(hs.numel() == rd * ud * Hl * bs * ud * Lu * hd, "head-sharded tensor has the wrong size")
-    d = UspDims(bs, L, H, hd, _dtype_code(seq), rd, ud, Ht, h0, 0)
+    return UspDims(bs, L, H, hd, _dtype_code(seq), rd, ud, Ht, h0, 0)
+
+
+def usp_a2a4d(src: torch.Tensor, dst: torch.Tensor, rd: int, ud: int, dir: int = 1, h0: int = 0,
+              H: Optional[int] = None, stream=None) -> torch.Tensor:
+    """AllToAll4D inside every Ulysses group: dir=+1 sequence-sharded [rd][ud][bs][Lu][H_total][hd]
+    -> head-sharded [rd][ud][H/ud][bs][Lr][hd]; dir=-1 back. lse tensors drop the trailing hd axis.
+    dir=+1 with H < ud (ud % H == 0, K/V under GQA/MQA) replicates: head-sharded is
+    [rd][ud][1][bs][Lr][hd], rank u' holding head u' // (ud // H); dir=-1 then sums each head's
+    replicas (the adjoint, for gradients)."""
+    d = _a2a4d_dims(src, dst, rd, ud, dir, h0, H)
     _abi.check("usp_a2a4d", _abi.load().usp_a2a4d(_ptr(src), _ptr(dst), d, 1 if dir > 0 else -1,
                                                  _stream(stream)))
     return dst
+
+
+def usp_a2a4d_multi(srcs, dsts, rd: int, ud: int, dir: int = 1, h0s=None, Hs=None, stream=None):
+    """usp_a2a4d for up to four tensors in one launch (their rows may differ: out and lse together);
+    tensor k moves heads [h0s[k], h0s[k] + Hs[k]) of its sequence-sharded tensor."""
+    srcs, dsts = list(srcs), list(dsts)
+    n = len(srcs)
+    _need(1 <= n <= 4 and len(dsts) == n, "one to four tensors")
+    h0s = [0] * n if h0s is None else list(h0s)
+    Hs = [None] * n if Hs is None else list(Hs)
+    dims = [_a2a4d_dims(srcs[k], dsts[k], rd, ud, dir, h0s[k], Hs[k]) for k in range(n)]
+    vp = ctypes.c_void_p
+    _abi.check("usp_a2a4d_multi", _abi.load().usp_a2a4d_multi(
+        n, (vp * n)(*[_ptr(x) for x in srcs]), (vp * n)(*[_ptr(x) for x in dsts]), (UspDims * n)(*dims),
+        1 if dir > 0 else -1, _stream(stream)))
+    return dsts
 
 
 def usp_extract_a2a(srcs, dsts, rd: int, ud: int, inverse: bool = False, h0s=None, Hs=None, split="zigzag",

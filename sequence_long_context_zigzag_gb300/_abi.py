@@ -72,6 +72,9 @@ def load():
     lib.usp_extract_a2a.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(UspDims),
                                     ctypes.c_int, vp]
     lib.usp_extract_a2a.restype = ctypes.c_int
+    lib.usp_a2a4d_multi.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(UspDims),
+                                    ctypes.c_int, vp]
+    lib.usp_a2a4d_multi.restype = ctypes.c_int
     lib.usp_forward.argtypes = [vp, vp, vp, vp, vp, UspAttnDesc, ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.usp_forward.restype = ctypes.c_int
     lib.usp_forward_host.argtypes = [vp, vp, vp, vp, vp, UspAttnDesc, ctypes.c_int, vp, ctypes.c_size_t, vp]

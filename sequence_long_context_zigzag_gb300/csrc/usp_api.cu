@@ -137,12 +137,13 @@ int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stre
     return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_dims *d, int inverse,
-                    usp_stream_t stream) {
+// the multi-tensor permutes: usp_extract_a2a (split + all-to-all composed) and usp_a2a4d_multi
+static int permute_multi(int n, const void *const *src, void *const *dst, const usp_dims *d, int mode,
+                         usp_stream_t stream) {
     if (n < 1 || n > kMaxPermJobs || !src || !dst || !d) return USP_ERR_INVALID_ARG;
     PermArgs a{};
     a.njobs = n;
-    a.mode = inverse ? PERM_FUSED_INV : PERM_FUSED_FWD;
+    a.mode = mode;
     a.r_fixed = -1;
     a.u_fixed = -1;
     int64_t work = 0;
@@ -150,7 +151,10 @@ int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_d
         const usp_dims &dk = d[k];
         int rc = check_dims(dk, 2);
         if (rc) return rc;
-        if (dk.bs != d[0].bs || dk.L != d[0].L || dk.rd != d[0].rd || dk.ud != d[0].ud || dk.split != d[0].split)
+        // the split matters only to the composed modes (the all-to-all alone does not use it)
+        const bool fused = mode == PERM_FUSED_FWD || mode == PERM_FUSED_INV;
+        if (dk.bs != d[0].bs || dk.L != d[0].L || dk.rd != d[0].rd || dk.ud != d[0].ud ||
+            (fused && dk.split != d[0].split))
             return USP_ERR_SHAPE;
         work += dk.bs * dk.L * (int64_t)dk.H;
         a.job[k] = PermJob{static_cast<const char *>(src[k]), static_cast<char *>(dst[k]), dk.H,
@@ -167,6 +171,17 @@ int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_d
     a.bs = d[0].bs; a.L = d[0].L;
     a.rd = d[0].rd; a.ud = d[0].ud;
     return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_extract_a2a(int n, const void *const *src, void *const *dst, const usp_dims *d, int inverse,
+                    usp_stream_t stream) {
+    return permute_multi(n, src, dst, d, inverse ? PERM_FUSED_INV : PERM_FUSED_FWD, stream);
+}
+
+int usp_a2a4d_multi(int n, const void *const *src, void *const *dst, const usp_dims *d, int dir,
+                    usp_stream_t stream) {
+    if (dir != 1 && dir != -1) return USP_ERR_INVALID_ARG;
+    return permute_multi(n, src, dst, d, dir > 0 ? PERM_A2A_FWD : PERM_A2A_INV, stream);
 }
 
 // checks shared by the forward and backward attention entry points; fills the kernel arguments

@@ -161,6 +161,21 @@ def test_extract_a2a_rejects():
     assert lib.usp_extract_a2a(2, two, two, (_abi.UspDims * 2)(dims(), dims(split=1)), 1, None) == _abi.USP_ERR_SHAPE
 
 
+def test_a2a4d_multi_rejects():
+    import ctypes
+    lib = _abi.load()
+    vp = ctypes.c_void_p
+    two = (vp * 2)(BAD, BAD)
+    one = (_abi.UspDims * 1)(dims())
+    assert lib.usp_a2a4d_multi(0, two, two, one, 1, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_a2a4d_multi(5, two, two, one, 1, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_a2a4d_multi(1, two, two, one, 0, None) == _abi.USP_ERR_INVALID_ARG
+    assert lib.usp_a2a4d_multi(2, two, two, (_abi.UspDims * 2)(dims(), dims(L=128)), -1, None) == _abi.USP_ERR_SHAPE
+    # out with lse rows, and a split the all-to-all alone does not use: past the shape checks
+    out_lse = (_abi.UspDims * 2)(dims(), dims(hd=1, dtype=_abi.USP_F32, split=1))
+    assert lib.usp_a2a4d_multi(2, two, two, out_lse, -1, None) == _abi.USP_ERR_ALIGN
+
+
 def test_forward_workspace_and_rejects():
     lib = _abi.load()
     d = desc(L=1024, hq=8, hkv=2, ud=2, rd=2)

@@ -201,3 +201,39 @@ def test_out_and_lse_rows_in_one_launch(dtype, hd, rd, ud, bs, L):
     usp.usp_extract_a2a([ld], [l1], rd, ud, inverse=True, h0s=[h0], Hs=[H])
     assert torch.equal(o1, o_nat) and torch.equal(l1, l_nat)
     usp.usp_check()
+
+
+@pytest.mark.parametrize("dtype,hd,rd,ud,bs,L", [(torch.bfloat16, 128, 4, 2, 1, 1024), (torch.float32, 64, 2, 4, 2, 512)])
+def test_a2a4d_multi_out_and_lse(dtype, hd, rd, ud, bs, L):
+    """usp_a2a4d_multi: step a5 of out (rows of hd elements) and lse (rows of one fp32) in one launch
+    for a head window of wider sequence-sharded tensors, equal to the oracle's inverse all-to-all and
+    to one launch per tensor; then the forward direction of Q-like and replicated K-like tensors in
+    one launch, equal to one launch per tensor."""
+    Ht, h0, H = 3 * ud, ud, 2 * ud
+    Lr, Lu = L // rd, L // (rd * ud)
+    o_hs = rand((rd, ud, H // ud, bs, Lr, hd), dtype, seed=L + hd + 7)
+    l_hs = rand((rd, ud, H // ud, bs, Lr), torch.float32, seed=L + 8)
+    od, ld = o_hs.to(DEV), l_hs.to(DEV)
+    o_seq = torch.zeros(rd, ud, bs, Lu, Ht, hd, dtype=dtype, device=DEV)
+    l_seq = torch.zeros(rd, ud, bs, Lu, Ht, device=DEV)
+    usp.usp_a2a4d_multi([od, ld], [o_seq, l_seq], rd, ud, -1, h0s=[h0, h0], Hs=[H, H])
+    og, lg = bits(o_seq), bits(l_seq)
+    assert np.array_equal(og[:, :, :, :, h0:h0 + H], oracle.a2a_inv(bits(o_hs), ud))
+    assert np.array_equal(lg[:, :, :, :, h0:h0 + H], oracle.a2a_inv(bits(l_hs)[..., None], ud)[..., 0])
+    assert not og[..., :h0, :].any() and not og[..., h0 + H:, :].any()
+    assert not lg[..., :h0].any() and not lg[..., h0 + H:].any()
+    o1, l1 = torch.zeros_like(o_seq), torch.zeros_like(l_seq)
+    usp.usp_a2a4d(od, o1, rd, ud, -1, h0=h0, H=H)
+    usp.usp_a2a4d(ld, l1, rd, ud, -1, h0=h0, H=H)
+    assert torch.equal(o1, o_seq) and torch.equal(l1, l_seq)
+    # forward: ud query heads and one KV head (replicated on every Ulysses rank) in one launch
+    q_seq = rand((rd, ud, bs, Lu, ud, hd), dtype, seed=L + 9).to(DEV)
+    k_seq = rand((rd, ud, bs, Lu, 1, hd), dtype, seed=L + 10).to(DEV)
+    q_hs = torch.empty(rd, ud, 1, bs, Lr, hd, dtype=dtype, device=DEV)
+    k_hs = torch.empty(rd, ud, 1, bs, Lr, hd, dtype=dtype, device=DEV)
+    usp.usp_a2a4d_multi([q_seq, k_seq], [q_hs, k_hs], rd, ud, 1)
+    q1, k1 = torch.empty_like(q_hs), torch.empty_like(k_hs)
+    usp.usp_a2a4d(q_seq, q1, rd, ud, 1)
+    usp.usp_a2a4d(k_seq, k1, rd, ud, 1)
+    assert torch.equal(q1, q_hs) and torch.equal(k1, k_hs)
+    usp.usp_check()
