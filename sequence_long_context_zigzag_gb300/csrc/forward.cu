@@ -284,15 +284,13 @@ int usp_backward(const void *q, const void *k, const void *v, const void *out, c
         ad.hq = s.hc;
         ad.hkv = s.hkc;
         if ((rc = usp_attn_bwd(qh, kh, vh, gh, lh, dh, dqh, dkh, dvh, ad, stream))) return rc;
-        const void *qs[1] = {dqh};
-        void *qd[1] = {dq};
-        usp_dims qdims[1] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype)};
-        if ((rc = usp_extract_a2a(1, qs, qd, qdims, 1, stream))) return rc;
-        // the KV gradients: inverse all-to-all (summing the replicas of replicated heads) and split
-        const void *ks[2] = {dkh, dvh};
-        void *kd[2] = {dk, dv};
-        usp_dims kdims[2] = {dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype), dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype)};
-        if ((rc = usp_extract_a2a(2, ks, kd, kdims, 1, stream))) return rc;
+        // the gradients back to natural order in one call: inverse all-to-all and split (the KV
+        // gradients of replicated heads sum their replicas, in a launch of their own)
+        const void *gs[3] = {dqh, dkh, dvh};
+        void *gd[3] = {dq, dk, dv};
+        usp_dims gdims[3] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype), dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype),
+                             dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype)};
+        if ((rc = usp_extract_a2a(3, gs, gd, gdims, 1, stream))) return rc;
     }
     return USP_OK;
 }
