@@ -1,5 +1,6 @@
 """bench.py's JSON contract pieces that need no GPU: both arms report one metric string and one
-config, and the config's L2 statement is computed from the shapes of the buffers the step uses."""
+config, the config's L2 statement is computed from the shapes of the buffers the step uses, and the
+clock record keeps the samples of the timed region and the throttle reasons seen in them."""
 import torch
 
 import bench
@@ -32,3 +33,45 @@ def test_reference_arm_reports_the_same_metric_and_config(capsys, monkeypatch):
     assert line["impl"] == "reference" and line["metric"] == bench.METRIC
     assert line["config"] == bench.workload_config(WORKLOADS[0])
     assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+
+
+class _DoneProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _sampler_with(lines, tmp_path):
+    s = bench.ClockSampler(0)
+    path = tmp_path / "clocks.csv"
+    path.write_text("".join(x + "\n" for x in lines))
+    s.path, s.proc = str(path), _DoneProc()
+    return s
+
+
+def _row(t, mhz, slow="Not Active", cap="Not Active"):
+    # timestamp, index, clocks.sm, clocks.max.sm, power, active mask, hw_slowdown, hw_thermal,
+    # sw_thermal, sw_power_cap (the sampler's query, csv without header or units)
+    return f"2026/01/01 00:00:{t:06.3f}, 0, {mhz}, 2070, 1300.00, 0x0000000000000000, {slow}, Not Active, " \
+           f"Not Active, {cap}"
+
+
+def test_clock_sampler_keeps_the_timed_region(tmp_path):
+    import datetime
+    base = datetime.datetime(2026, 1, 1).timestamp()
+    lines = [_row(1.0, 1200), _row(2.0, 2000, cap="Active"), _row(2.05, 2040), _row(2.1, 2070),
+             _row(3.0, 900, slow="Active"), "garbage line", ""]
+    got = _sampler_with(lines, tmp_path).stop(base + 1.5, base + 2.5)
+    assert got["window"] == "timed region" and got["samples"] == 3
+    assert got["sm_mhz"] == 2040 and got["sm_max_mhz"] == 2070
+    assert got["reasons"] == ["sw_power_cap"]  # the hw_slowdown sample is outside the region
+
+
+def test_clock_sampler_falls_back_to_every_sample(tmp_path):
+    import datetime
+    base = datetime.datetime(2026, 1, 1).timestamp()
+    got = _sampler_with([_row(1.0, 1500, slow="Active"), _row(1.2, 1700)], tmp_path).stop(base + 5, base + 6)
+    assert got["window"].startswith("sampler run") and got["samples"] == 2
+    assert got["reasons"] == ["hw_slowdown"] and got["sm_mhz"] == 1600
