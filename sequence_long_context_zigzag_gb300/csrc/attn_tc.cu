@@ -876,7 +876,7 @@ int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static bool attr_set[64] = {};
     int dev = 0;
-    cudaGetDevice(&dev);
+    if (cudaGetDevice(&dev) != cudaSuccess) return USP_ERR_CUDA;
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         // setmaxnreg.inc can only be granted from registers the launch already holds: never launch a
         // build whose register count would make the warpgroup split wait forever
