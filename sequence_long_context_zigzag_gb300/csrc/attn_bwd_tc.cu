@@ -32,6 +32,7 @@
 // dq kernel: dQ [0,hd) S_b hd + 128b + [0,64) dP_b + [64,128).
 // Every wait is bounded (2 s): on expiry the kernel records USP_ERR_TIMEOUT, drains and returns.
 #include <cuda.h>
+#include <mutex>
 
 #include "tc_common.cuh"
 #include "tc_ptx.cuh"
@@ -935,8 +936,10 @@ int prepare(Kern kern, int smem, bool &done) {
 template <int HD>
 int launch_typed(BwdTcParams &kv, BwdTcParams &q, uint32_t grid_kv, uint32_t grid_q, cudaStream_t s) {
     static bool set_kv[64] = {}, set_q[64] = {};
+    static std::mutex set_mu;  // host threads may make their first launch at the same time
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return USP_ERR_CUDA;
+    std::unique_lock<std::mutex> lk(set_mu);
     int rc = prepare(attn_bwd_dkv_kernel<HD>, KvCfg<HD>::kSmemBytes, set_kv[dev]);
     if (rc) return rc;
     if (!set_q[dev]) {
@@ -947,6 +950,7 @@ int launch_typed(BwdTcParams &kv, BwdTcParams &q, uint32_t grid_kv, uint32_t gri
         if ((long)fa.numRegs * kThreads < 2L * 128 * kQSoftmaxRegs + 128L * kQControlRegs) return USP_ERR_UNSUPPORTED;
     }
     if ((rc = prepare(attn_bwd_dq_kernel<HD>, QCfg<HD>::kSmemBytes, set_q[dev]))) return rc;
+    lk.unlock();
     attn_bwd_dkv_kernel<HD><<<grid_kv, kThreads, KvCfg<HD>::kSmemBytes, s>>>(kv);
     attn_bwd_dq_kernel<HD><<<grid_q, kThreads, QCfg<HD>::kSmemBytes, s>>>(q);
     return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA;

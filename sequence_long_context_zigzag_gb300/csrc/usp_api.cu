@@ -260,7 +260,13 @@ int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *
     AttnArgs a = attn_args(d);
     a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (d.dtype == USP_BF16) return launch_attn_tc(a, s);
+    if (d.dtype == USP_BF16) {
+        // the tensor-core launcher sets each kernel's shared-memory attribute on its first launch on
+        // a device and remembers it; host threads launching at the same time take turns here
+        static std::mutex tc_mu;
+        std::lock_guard<std::mutex> lk(tc_mu);
+        return launch_attn_tc(a, s);
+    }
     return launch_attn_simt(a, s);
 }
 
