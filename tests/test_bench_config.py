@@ -75,3 +75,30 @@ def test_clock_sampler_falls_back_to_every_sample(tmp_path):
     got = _sampler_with([_row(1.0, 1500, slow="Active"), _row(1.2, 1700)], tmp_path).stop(base + 5, base + 6)
     assert got["window"].startswith("sampler run") and got["samples"] == 2
     assert got["reasons"] == ["hw_slowdown"] and got["sm_mhz"] == 1600
+
+
+def test_traffic_is_reported_only_for_the_captured_source(monkeypatch, tmp_path):
+    """roofline.traffic comes from the committed ncu summary only while the forward kernel's sources
+    hash to the value recorded there, and only for the workload it was captured on."""
+    rec = bench.traffic_for_current_kernel(bench.DEFAULT_WORKLOAD)
+    assert rec is None or rec > 0
+    assert bench.traffic_for_current_kernel(bench.DEFAULT_WORKLOAD + 1) is None
+    f = tmp_path / "summary.md"
+    f.write_text("attn_src_sha256_16: 0000000000000000\ndram_bytes_per_launch: 123\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.traffic_for_current_kernel(bench.DEFAULT_WORKLOAD) is None
+    f.write_text(f"attn_src_sha256_16: {bench.attn_src_hash()}\ndram_bytes_per_launch: 123\n")
+    assert bench.traffic_for_current_kernel(bench.DEFAULT_WORKLOAD) == 123
+
+
+def test_e2e_head_groups_are_valid():
+    """The host-buffer pipeline's head groups divide the heads and keep whole KV groups on every
+    Ulysses rank (or replicate one KV head)."""
+    for w in WORKLOADS:
+        hc = bench.e2e_head_chunk(w)
+        if hc is None:
+            continue
+        G = w.hq // w.hkv
+        assert w.hq % hc == 0 and hc % G == 0 and hc % w.ud == 0
+        hkc = hc // G
+        assert hkc % w.ud == 0 or w.ud % hkc == 0
