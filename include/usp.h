@@ -282,8 +282,12 @@ USP_API size_t usp_forward_workspace_size(usp_attn_desc d, int head_chunk, int h
  *   (usp_forward_workspace_size(d, head_chunk, 0)) exceeds USP_NOALLOC_SCRATCH_BYTES return
  *   USP_ERR_UNSUPPORTED before anything runs: choose a smaller head_chunk (e.g. L = 8192, hd = 128,
  *   bf16 fits with 2 query heads per group for MHA).
+ *   The device is the CURRENT device (cudaGetDevice): q, k, v, out, lse and the stream must belong to
+ *   it, since the array used is the current device's copy.
  *   The first call on a device looks up the array's device address (once per device, cached); make
- *   that first call before any stream capture begins.
+ *   that first call before any stream capture begins. The cached address is not refreshed: after a
+ *   cudaDeviceReset of that device (which unloads the library's module there), do not call this
+ *   entry point again in the same process.
  *   Every call on a device uses the same array, and calls that overlap on the GPU race on it (e.g.
  *   two streams at once): order them on one stream. The array keeps the last call's contents; the
  *   call writes every workspace byte it reads, so nothing needs to start at zero.

@@ -361,12 +361,16 @@ def usp_forward_noalloc(q, k, v, out, lse, ud: int, rd: int, causal: bool = True
                         head_chunk: Optional[int] = None, stream=None):
     """usp_forward with the library's own fixed scratch array instead of a caller workspace: for
     callers that cannot allocate device memory (see include/usp.h). Shapes whose workspace exceeds
-    the array (32 MiB) raise UspError (USP_ERR_UNSUPPORTED); calls must not overlap on the GPU."""
+    the array (32 MiB) raise UspError (USP_ERR_UNSUPPORTED); calls must not overlap on the GPU.
+    The library uses the current device's array, so the call runs with the tensors' device current
+    (all five tensors must be on one device)."""
     _dev(q, k, v, out, lse)
+    _need(all(t.device == q.device for t in (k, v, out, lse)), "q, k, v, out, lse must be on one device")
     _check_natural(q, k, v, out, lse)
     d = _forward_desc(q, k, ud, rd, causal, scale)
-    _abi.check("usp_forward_noalloc", _abi.load().usp_forward_noalloc(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d, int(head_chunk or 0), _stream(stream)))
+    with torch.cuda.device(q.device):
+        _abi.check("usp_forward_noalloc", _abi.load().usp_forward_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), d, int(head_chunk or 0), _stream(stream)))
     return out, lse
 
 

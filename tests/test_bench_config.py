@@ -78,17 +78,37 @@ def test_clock_sampler_falls_back_to_every_sample(tmp_path):
 
 
 def test_traffic_is_reported_only_for_the_captured_source(monkeypatch, tmp_path):
-    """roofline.traffic comes from the committed ncu summary only while the forward kernel's sources
+    """roofline.traffic comes from the committed ncu record only while the forward kernel's sources
     hash to the value recorded there, and only for the workload it was captured on."""
-    rec = bench.traffic_for_current_kernel(bench.DEFAULT_WORKLOAD)
-    assert rec is None or rec > 0
-    assert bench.traffic_for_current_kernel(bench.DEFAULT_WORKLOAD + 1) is None
-    f = tmp_path / "summary.md"
-    f.write_text("attn_src_sha256_16: 0000000000000000\ndram_bytes_per_launch: 123\n")
+    import json
+    for w in WORKLOADS:
+        rec = bench.traffic_for_current_kernel(w)
+        assert rec is None or rec > 0
+    f = tmp_path / "traffic.json"
+    w = WORKLOADS[bench.DEFAULT_WORKLOAD]
+    f.write_text(json.dumps({"records": [{"workload": w.name, "attn_src_sha256_16": "0" * 16,
+                                          "dram_bytes_per_launch": 123}]}))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
-    assert bench.traffic_for_current_kernel(bench.DEFAULT_WORKLOAD) is None
-    f.write_text(f"attn_src_sha256_16: {bench.attn_src_hash()}\ndram_bytes_per_launch: 123\n")
-    assert bench.traffic_for_current_kernel(bench.DEFAULT_WORKLOAD) == 123
+    assert bench.traffic_for_current_kernel(w) is None
+    f.write_text(json.dumps({"records": [{"workload": w.name, "attn_src_sha256_16": bench.attn_src_hash(),
+                                          "dram_bytes_per_launch": 123}]}))
+    assert bench.traffic_for_current_kernel(w) == 123
+    assert bench.traffic_for_current_kernel(WORKLOADS[0]) is None
+
+
+def test_peak_follows_the_timed_region():
+    """A timed region shorter than a second is a burst (the burst cuBLAS rate applies); a longer one
+    runs under the power cap (the sustained rate)."""
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    v, why = bench.pick_peak(peaks, "measured", 0.01)
+    assert v == 1900.0 and "bf16_tflops " in why.replace("=", " ")
+    v, why = bench.pick_peak(peaks, "measured", 7.0)
+    assert v == 1700.0 and "bf16_tflops_sustained" in why
+
+
+def test_default_workload_is_the_largest_single_gpu_one():
+    w = WORKLOADS[bench.DEFAULT_WORKLOAD]
+    assert w.L == max(x.L for x in WORKLOADS) and w.dtype == "bf16" and w.head_chunk == 8
 
 
 def test_e2e_head_groups_are_valid():

@@ -1,6 +1,9 @@
-"""Parity at the five workloads' full sizes, in the launch configuration the bench times: the whole
-USP-Attention forward on the GPU against the oracle's direct attention on all rows (tiny workload)
-or on seeded sampled rows plus the chunk-boundary rows (the others)."""
+"""Parity at the workloads' full sizes, in the launch configuration the bench times: the whole
+USP-Attention forward on the GPU against the oracle's direct attention on every row (the tiny and the
+L = 8192 workloads) or on seeded sampled rows plus the chunk-boundary rows (the longer ones), and for
+the L = 32768 GQA workload additionally on every row of four query heads, one in each of four KV
+groups (all 32 heads on every row would take the oracle about 8.8e12 fp64 operations, minutes of the
+host's cores)."""
 import numpy as np
 import pytest
 import torch
@@ -12,6 +15,12 @@ from seeded_inputs import WORKLOADS, default_seed, make_rows, make_workload_qkv
 pytestmark = pytest.mark.gpu
 
 
+def _errors(out, lse, o_ref, l_ref):
+    err_o = np.abs(out - o_ref).max()
+    err_l = (np.abs(lse - l_ref) / np.maximum(np.abs(l_ref), 1.0)).max()
+    return err_o, err_l
+
+
 @pytest.mark.parametrize("wi", range(len(WORKLOADS)))
 def test_workload_matches_oracle(wi):
     w = WORKLOADS[wi]
@@ -20,14 +29,34 @@ def test_workload_matches_oracle(wi):
     out, lse = usp.usp_attention(q.cuda(), k.cuda(), v.cuda(), ud=w.ud, rd=w.rd, causal=w.causal,
                                  head_chunk=w.head_chunk)
     usp.usp_check()
-    n = w.sample_rows if w.sample_rows is not None else (512 if w.L > 4096 else None)
+    n = w.sample_rows
     rows = np.arange(w.L) if n is None else np.array(make_rows(w.L, w.c, n, seed))
     o_ref, l_ref = oracle.attn_direct(q, k, v, causal=w.causal, rows=rows)
     rows_t = torch.as_tensor(rows, device="cuda")
     o = out.index_select(1, rows_t).float().cpu().numpy()
     l = lse.index_select(1, rows_t).cpu().numpy()
-    err_o = np.abs(o - o_ref).max()
-    err_l = (np.abs(l - l_ref) / np.maximum(np.abs(l_ref), 1.0)).max()
+    err_o, err_l = _errors(o, l, o_ref, l_ref)
     print(f"{w.name}: rows={len(rows)} out max-abs {err_o:.3e} lse rel {err_l:.3e}")
     assert err_o <= 2e-2
     assert err_l <= 1e-3
+
+
+def test_gqa_L32768_every_row_of_four_heads():
+    wi = 2
+    w = WORKLOADS[wi]
+    assert w.L == 32768 and w.hq == 32 and w.hkv == 8
+    seed = default_seed(wi)
+    q, k, v = make_workload_qkv(w, seed)
+    out, lse = usp.usp_attention(q.cuda(), k.cuda(), v.cuda(), ud=w.ud, rd=w.rd, causal=w.causal,
+                                 head_chunk=w.head_chunk)
+    usp.usp_check()
+    G = w.hq // w.hkv
+    for g, off in ((0, 0), (3, 1), (5, 2), (7, 3)):   # KV group g, query head g*G + off
+        h = g * G + off
+        o_ref, l_ref = oracle.attn_direct(q[:, :, h:h + 1], k[:, :, g:g + 1], v[:, :, g:g + 1], causal=w.causal)
+        o = out[:, :, h:h + 1].float().cpu().numpy()
+        l = lse[:, :, h:h + 1].cpu().numpy()
+        err_o, err_l = _errors(o, l, o_ref, l_ref)
+        print(f"{w.name} head {h} (KV {g}), all {w.L} rows: out max-abs {err_o:.3e} lse rel {err_l:.3e}")
+        assert err_o <= 2e-2
+        assert err_l <= 1e-3
