@@ -73,6 +73,16 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kCuCache = 4096;
 constexpr uint64_t kSuperGroupKV = 64ull << 20;  // K/V bytes per super-group of units (launch_attn_tc)
 constexpr float kLn2 = 0.69314718055994531f;
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 
 template <int HD> struct Cfg {
@@ -102,7 +112,13 @@ template <int HD> struct Cfg {
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     // at kTmemSlot: tensor memory address, skip flag; then (packed samples only) a copy of cu_seqlens
     static constexpr int kCu = kTmemSlot + 16;
-    static constexpr int kSmemBytes = kCu + 1024;  // + slack for 1024-byte alignment
+    // epilogue staging of the packed-sample kernel, after the cu_seqlens copy: one slot per softmax
+    // warp (32 rows x 64 bytes)
+    static constexpr int kStgSlot = 32 * 64;
+    static constexpr int kStgBytes = kSoftmaxWarps * kStgSlot;
+    __host__ __device__ static constexpr int stg_offset(bool pk) {
+        return (kCu + (pk ? kCuCache * 4 : 0) + 127) / 128 * 128;
+    }
     __device__ static constexpr uint32_t colS(int i) { return 128u * (uint32_t)i; }
     __device__ static constexpr uint32_t colO(int i) { return 256u + (uint32_t)(HD * i); }
 };
@@ -282,8 +298,16 @@ __device__ __forceinline__ void iter_setup(const TcParams &p, const Work &w, Til
 
 template <bool PK>
 __device__ __forceinline__ void iter_init(const TcParams &p, const Work &w, TileIter &it) {
-    it.t = w.t_begin;
-    iter_setup<PK>(p, w, it);
+    if constexpr (PK) {
+        // the first iter_next call sets up ring step t_begin: one inlined copy of iter_setup, which
+        // pays for packed samples (units of a few tiles) and not for long units
+        it.t = w.t_begin - 1;
+        it.kt = 0;
+        it.nkt = 0;
+    } else {
+        it.t = w.t_begin;
+        iter_setup<PK>(p, w, it);
+    }
 }
 
 // the next KV tile that at least one Q tile of the unit needs (packed samples can leave gaps between
@@ -551,6 +575,110 @@ __device__ void mma_role(const TcParams &p, uint32_t cu_s, uint32_t sbase, uint3
     wait(C::DONE + i, 0);
 }
 
+// The issuer of the packed-sample kernel: the same products, commits and turn order as mma_role,
+// written so that the unit decode (cursor_next) and the S burst are each inlined once, and with the
+// stream's first S products outside the turn order like every later unit's. Packed samples cross a
+// unit boundary every few tiles, so the boundary code runs often and its size and latency count:
+// measured on GB300 this version is 9-12% faster for packed samples of 1024 to 4096 tokens, while
+// for long units (one sample) it is 1.5-2% slower than mma_role, which stays there.
+template <int HD, bool PK>
+__device__ void mma_role_pk(const TcParams &p, uint32_t cu_s, uint32_t sbase, uint32_t bar0, uint32_t tmem, int i) {
+    using C = Cfg<HD>;
+    auto BAR = [&](int k) { return bar0 + 8u * k; };
+    auto wait = [&](int bar, uint32_t parity) {
+        return tc::mbar_wait(BAR(bar), parity, p.status, USP_ERR_TIMEOUT, kWaitLimitNs);
+    };
+    const uint32_t sQ = sbase + C::kQ, sK = sbase + C::kK, sV = sbase + C::kV;
+    // base descriptors: this Q tile and stage 0 of K / V (K-major: LBO unused, SBO = 8 rows x 128 B;
+    // V as MN-major: LBO = next 64-column block, SBO = next 8-key group)
+    const uint64_t qdesc = tc::sw128_desc(sQ + (uint32_t)i * C::kTileBytes, 16, 1024);
+    const uint64_t kdesc0 = tc::sw128_desc(sK, 16, 1024);
+    const uint64_t vdesc0 = tc::sw128_desc(sV, C::kBoxBytes, 1024);
+    auto stage_off = [](uint32_t st) { return (uint64_t)((st * C::kTileBytes) >> 4); };
+    const uint32_t tS = tmem + C::colS(i), tO = tmem + C::colO(i);
+    const int barS = C::S_FULL + i, barP = C::P_FULL + i;
+    const int my_turn = C::TURN + i, other_turn = C::TURN + (1 - i);
+    // turn phases: issuer 0's burst j (j >= 0) waits for issuer 1's burst j-1; issuer 1's burst j
+    // (j >= -1) waits for issuer 0's burst j
+    uint32_t turns = 0;
+    auto take_turn = [&]() { return wait(my_turn, (turns++) & 1u); };
+    // S_i of tile t from K stage st, and this issuer's release of the stage
+    auto s_burst = [&](const Tile &t, uint32_t st) {
+        if (i ? t.act[1] : t.act[0]) {
+            issue_s<HD>(tS, qdesc, kdesc0 + stage_off(st));
+            tc::mma_commit(BAR(barS));
+        }
+        tc::mma_commit(BAR(C::K_EMPTY + st));
+    };
+    Cursor cs;
+    cs.k = 0;
+    cs.live = false;
+    Tile cur, nxt;
+    bool have = false;             // cur holds tile j of the stream
+    bool ok = true;
+    uint32_t pc = 0, started = 0;  // P waits; a PV of the current unit has been issued
+    uint32_t nq = 0, no = 0;       // Q loads consumed; O_i read-outs handed to the softmax
+    uint32_t j = 0;                // tiles of the stream (stage ring position)
+    // The stream's first S products are outside the turn order like every unit's first ones; issuer
+    // 1's empty "burst -1" lets issuer 0's burst 0 go first.
+    if (i == 1) tc::mbar_arrive(BAR(other_turn));
+    // One loop pass per tile j: PV_i(j) in the turn order, then S_i(j+1); cursor_next and the S
+    // burst are inlined once each.
+    while (ok) {
+        const bool have_n = cursor_next<PK>(p, cu_s, cs, nxt);
+        const bool boundary = have_n && nxt.first;  // tile j+1 opens a unit (the stream's first tile too)
+        const uint32_t jn = have ? j + 1 : 0;       // stream index of nxt
+        const uint32_t stn = jn % C::kStages, phn = (jn / C::kStages) & 1u;
+        bool turn_after_s = false;                   // S_i(j+1) is part of this burst
+        if (have) {
+            const bool last = !have_n || nxt.first;  // tile j is the last of its unit
+            const uint32_t st = j % C::kStages, ph = (j / C::kStages) & 1u;
+            const bool act = i ? cur.act[1] : cur.act[0];
+            if (last) tc::mma_commit(BAR(C::Q_EMPTY));  // this issuer's S products of the unit are issued
+            // operands first: every issuer waits for a stage's fill before releasing it, even when its
+            // Q tile skips the tile, so neither issuer can release fill f + kStages before the producer
+            // has refilled the stage (which needs both releases of fill f): the shared release barrier
+            // never runs ahead
+            if (!(ok = wait(C::V_FULL + st, ph))) break;
+            if (act && !(ok = wait(barP, pc & 1u))) break;
+            if (act && !started && no > 0 && !(ok = wait(C::O_EMPTY + i, (no - 1) & 1u))) break;
+            if (have_n && !boundary && !(ok = wait(C::K_FULL + stn, phn))) break;
+            if (!(ok = take_turn())) break;
+            if (act) {
+                ++pc;
+                tc::fence_after_sync();
+                issue_pv<HD>(tO, tS, vdesc0 + stage_off(st), started);
+                started = 1;
+            }
+            tc::mma_commit(BAR(C::V_EMPTY + st));  // this issuer no longer reads V(j)
+            if (last) {
+                if (started) {
+                    tc::mma_commit(BAR(C::O_FULL + i));
+                    ++no;
+                }
+                started = 0;
+            }
+            turn_after_s = have_n && !boundary;
+            if (!turn_after_s) tc::mbar_arrive(BAR(other_turn));
+        }
+        if (!have_n) break;
+        if (boundary) {
+            if (!(ok = wait(C::Q_FULL, nq & 1u))) break;
+            ++nq;
+            if (!(ok = wait(C::K_FULL + stn, phn))) break;
+        }
+        s_burst(nxt, stn);
+        if (turn_after_s) tc::mbar_arrive(BAR(other_turn));
+        cur = nxt;
+        have = true;
+        j = jn;
+    }
+    if (!ok) tc::mbar_arrive(BAR(other_turn));  // let the other issuer reach its own bounded exit
+    // every MMA of this issuer has finished before tensor memory is released
+    tc::mma_commit(BAR(C::DONE + i));
+    wait(C::DONE + i, 0);
+}
+
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
 // columns at or beyond the row's key limit (relative to the tile) get score -inf
@@ -602,7 +730,7 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&r)[32], uint64_t sl22
 // barrier phases do. Returns false after a failed wait.
 template <int HD, bool PK>
 __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, const Work &w, uint32_t bar0,
-                                             uint32_t tmem, int i, uint32_t &ns, uint32_t &no) {
+                                             uint32_t tmem, uint32_t stg, int i, uint32_t &ns, uint32_t &no) {
     using C = Cfg<HD>;
     constexpr int kCh = 4;  // 32-column chunks of an S row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -730,7 +858,39 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(barOE);
-        if (row_ok) {
+        if (PK && p.mode != USP_MODE_ACCUM) {
+            // Packed samples (short units, where the epilogue recurs every few tiles): each lane packs
+            // its row's 32-column chunk (64 bytes) into the warp's staging slot, 16-byte
+            // pieces swizzled by (row / 2) mod 4 so that neither the row-wise writes nor the
+            // column-wise reads conflict on banks; then every store instruction of the warp writes 8
+            // whole 64-byte row segments (4 lanes per row), 8 lines instead of one per lane. Measured
+            // on GB300: packed samples of 1024 tokens 15% faster; one long sample 1.5% slower (there
+            // the epilogue is a few per cent of the time and the kernel's code layout moves), so the
+            // one-sample kernel keeps the per-row stores below.
+            const uint32_t wrow0 = q0 + (uint32_t)wq * 32u;  // local row of the warp's first row
+            const size_t gbase = (size_t)w.q_row_base + wrow0;
+            const uint32_t rd_r = (uint32_t)lane >> 2, rd_c = (uint32_t)lane & 3u;
+#pragma unroll
+            for (int oc = 0; oc < kOc; ++oc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = float2_to_bf16x2(u2f(o[oc][2 * e]) * inv_l, u2f(o[oc][2 * e + 1]) * inv_l);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+                    st_shared_v4(stg + (uint32_t)lane * 64u + (((uint32_t)c4 ^ (((uint32_t)lane >> 1) & 3u)) << 4),
+                                 pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int it8 = 0; it8 < 4; ++it8) {
+                    const uint32_t r = (uint32_t)it8 * 8u + rd_r;
+                    const uint4 x = ld_shared_v4(stg + r * 64u + ((rd_c ^ ((r >> 1) & 3u)) << 4));
+                    if (valid && wrow0 + r < p.Lr)
+                        *reinterpret_cast<uint4 *>(p.out + (gbase + r) * HD + oc * 32 + rd_c * 8) = x;
+                }
+                __syncwarp();
+            }
+        } else if (row_ok) {
 #pragma unroll
             for (int oc = 0; oc < kOc; ++oc) {
                 float v[32];
@@ -771,13 +931,13 @@ __device__ __forceinline__ bool softmax_unit(const TcParams &p, uint32_t cu_s, c
 }
 
 template <int HD, bool PK>
-__device__ void softmax_role(const TcParams &p, uint32_t cu_s, uint32_t bar0, uint32_t tmem, int i) {
+__device__ void softmax_role(const TcParams &p, uint32_t cu_s, uint32_t bar0, uint32_t tmem, uint32_t stg, int i) {
     uint32_t ns = 0, no = 0;
     for (uint32_t k = 0;; ++k) {
         uint32_t x;
         if (!unit_index(p, k, x)) break;
         const Work w = decode_work<PK>(p, cu_s, x);
-        if (!softmax_unit<HD, PK>(p, cu_s, w, bar0, tmem, i, ns, no)) return;
+        if (!softmax_unit<HD, PK>(p, cu_s, w, bar0, tmem, stg, i, ns, no)) return;
     }
 }
 
@@ -847,16 +1007,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (!skip) {
             if (warp == kProducerWarp && lane == 0)
                 producer_role<HD, PK>(p, cu_s, sbase, bar0);
-            else if (warp == kMmaWarp && lane == 0)
-                mma_role<HD, PK>(p, cu_s, sbase, bar0, tmem, 0);
-            else if (warp == kMmaWarp1 && lane == 0)
-                mma_role<HD, PK>(p, cu_s, sbase, bar0, tmem, 1);
+            else if (warp == kMmaWarp && lane == 0) {
+                if constexpr (PK) mma_role_pk<HD, PK>(p, cu_s, sbase, bar0, tmem, 0);
+                else mma_role<HD, PK>(p, cu_s, sbase, bar0, tmem, 0);
+            } else if (warp == kMmaWarp1 && lane == 0) {
+                if constexpr (PK) mma_role_pk<HD, PK>(p, cu_s, sbase, bar0, tmem, 1);
+                else mma_role<HD, PK>(p, cu_s, sbase, bar0, tmem, 1);
+            }
             __syncwarp();
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         // warpgroup i: Q tile i
-        if (!skip) softmax_role<HD, PK>(p, cu_s, bar0, tmem, warp >> 2);
+        if (!skip)
+            softmax_role<HD, PK>(p, cu_s, bar0, tmem, sbase + (uint32_t)(C::stg_offset(PK) + warp * C::kStgSlot),
+                                 warp >> 2);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -872,7 +1037,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 template <int HD, bool PK>
 int launch_typed(const TcParams &prm, uint32_t grid, cudaStream_t s) {
     using C = Cfg<HD>;
-    constexpr int kSmem = C::kSmemBytes + (PK ? kCuCache * 4 : 0);
+    // + 1024 bytes of slack for the 1024-byte alignment of the base
+    constexpr int kSmem = (PK ? C::stg_offset(PK) + C::kStgBytes : C::kCu) + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static bool attr_set[64] = {};
     int dev = 0;
@@ -936,9 +1102,11 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     // fits in the 126 MiB L2 (with a little spill), not when one group's K/V alone is larger than the
     // budget, and not for packed samples (a unit then reads only its own sample's K/V). Working on
     // fewer heads at a time costs time of its own (measured: 7% at L = 8192 with two super-groups,
-    // 50% for packed samples of 1024 with one head per super-group, 1.6% at L = 262144 with one of
-    // two 128 MiB groups per super-group), while at L = 131072 (32 groups of 64 MiB) one group per
-    // super-group cuts DRAM reads from 151 to 60 GB per launch.
+    // 50% for packed samples of 1024 with one head per super-group), while at L = 131072 (32 groups
+    // of 64 MiB) one group per super-group cuts DRAM reads from 151 to 60 GB per launch. At
+    // L = 262144 (a head group of 8 query heads: two groups of 128 MiB) one group per super-group cuts
+    // them from 58-88 GB to 14-26 GB per launch, but runs 2.8% fewer FLOP per clock (the clock under
+    // the power cap rose only 1.2%), so the budget stays below one such group.
     p.Gl = p.Hl / p.Hkl;
     p.ngroups = p.ud * p.Hkl * p.bs;
     p.nouter = (uint32_t)ranks * p.npairs;

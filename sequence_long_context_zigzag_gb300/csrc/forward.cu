@@ -5,7 +5,8 @@
 // Per head group (UPipe-style head chunking): the composed zigzag split + AllToAll4D of Q, K, V, the
 // fused ring attention, and the composed inverse of out and lse. The host-buffer variant overlaps,
 // on three internal streams, the host-to-device copy of group g+1 and the device-to-host copy of
-// group g-1 with the kernels of group g (two staging slots per direction).
+// group g-1 with the kernels of group g (two staging slots per direction) -- or, when the host
+// buffers are mapped page-locked memory, lets the kernels read and write them directly.
 #include <mutex>
 
 #include "usp_internal.cuh"
@@ -110,6 +111,43 @@ bool pipe_init(HostPipe &hp) {
     return true;
 }
 
+// The forward of every head group, on buffers the kernels can address: the composed split +
+// all-to-all of q, k, v, the ring attention, and the composed inverse of out and lse. q, k, v, out and
+// lse may be device memory or mapped page-locked host memory (usp_forward_host's direct path).
+int forward_groups(const FwdShape &s, const usp_attn_desc &d, const void *q, const void *k, const void *v, void *out,
+                   float *lse, void *qh, void *kh, void *vh, void *oh, float *lh, usp_stream_t stream) {
+    int rc;
+    for (int g0 = 0; g0 < s.hq; g0 += s.hc) {
+        const int gk = g0 / s.G;
+        const void *srcs[3] = {q, k, v};
+        void *dsts[3] = {qh, kh, vh};
+        usp_dims dd[3] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype), dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype),
+                          dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype)};
+        if ((rc = usp_extract_a2a(3, srcs, dsts, dd, 0, stream))) return rc;
+        usp_attn_desc ad = d;
+        ad.hq = s.hc;
+        ad.hkv = s.hkc;
+        if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, stream))) return rc;
+        // out and lse back to natural order in one launch
+        const void *os[2] = {oh, lh};
+        void *od[2] = {out, lse};
+        usp_dims odims[2] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype), dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
+        if ((rc = usp_extract_a2a(2, os, od, odims, 1, stream))) return rc;
+    }
+    return USP_OK;
+}
+
+// Device address of a host buffer that is page-locked and mapped into the current device's address
+// space (cudaHostAlloc, cudaHostRegister, or a pinned torch tensor), else nullptr.
+void *mapped_host(const void *p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer is not an error of the call; clear it
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 // 2-D copy of a head window: `rows` rows of `width` bytes, source / destination pitches in bytes
 inline bool copy2d(void *dst, size_t dpitch, const void *src, size_t spitch, size_t width, size_t rows,
                    cudaMemcpyKind kind, cudaStream_t s) {
@@ -141,24 +179,7 @@ int usp_forward(const void *q, const void *k, const void *v, void *out, float *l
     Carve cv{static_cast<char *>(workspace), workspace_bytes};
     void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *oh = cv.take(s.q_grp);
     float *lh = static_cast<float *>(cv.take(s.lse_grp));
-    for (int g0 = 0; g0 < s.hq; g0 += s.hc) {
-        const int gk = g0 / s.G;
-        const void *srcs[3] = {q, k, v};
-        void *dsts[3] = {qh, kh, vh};
-        usp_dims dd[3] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype), dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype),
-                          dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype)};
-        if ((rc = usp_extract_a2a(3, srcs, dsts, dd, 0, stream))) return rc;
-        usp_attn_desc ad = d;
-        ad.hq = s.hc;
-        ad.hkv = s.hkc;
-        if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, stream))) return rc;
-        // out and lse back to natural order in one launch
-        const void *os[2] = {oh, lh};
-        void *od[2] = {out, lse};
-        usp_dims odims[2] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype), dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
-        if ((rc = usp_extract_a2a(2, os, od, odims, 1, stream))) return rc;
-    }
-    return USP_OK;
+    return forward_groups(s, d, q, k, v, out, lse, qh, kh, vh, oh, lh, stream);
 }
 
 int usp_forward_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, float *lse_host,
@@ -170,6 +191,21 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
     if (!q_host || !k_host || !v_host || !out_host || !lse_host || !workspace) return USP_ERR_INVALID_ARG;
     if (workspace_bytes < ws_host(s)) return USP_ERR_INVALID_ARG;
     if (!aligned(workspace, kAlign)) return USP_ERR_ALIGN;
+    // Direct path: when every host buffer is mapped page-locked memory, the kernels read q, k, v and
+    // write out and lse in host memory themselves, over the CPU-GPU link (NVLink-C2C on GB300), in
+    // the order usp_forward reads and writes device memory; nothing is staged or copied by DMA.
+    {
+        void *qd = mapped_host(q_host), *kd = mapped_host(k_host), *vd = mapped_host(v_host);
+        void *od = mapped_host(out_host), *ld = mapped_host(lse_host);
+        if (qd && kd && vd && od && ld) {
+            Carve cv{static_cast<char *>(workspace), workspace_bytes};
+            void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *oh = cv.take(s.q_grp);
+            float *lh = static_cast<float *>(cv.take(s.lse_grp));
+            return forward_groups(s, d, qd, kd, vd, od, static_cast<float *>(ld), qh, kh, vh, oh, lh, stream);
+        }
+    }
+    // Copy path (pageable or unmapped host buffers): staged DMA copies of each head group's window,
+    // pipelined with the kernels on the library's streams.
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return USP_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_pipe_mu[dev]);

@@ -30,15 +30,21 @@ def test_forward_device_matches_oracle_and_is_chunk_invariant(L, hq, hkv, hd, ud
     assert (np.abs(lse.cpu().numpy() - l_ref) / np.maximum(np.abs(l_ref), 1)).max() <= 1e-3
 
 
+@pytest.mark.parametrize("mem", ["pinned", "pageable", "mixed"])
 @pytest.mark.parametrize("L,hq,hkv,hd,ud,rd,chunk", [(1024, 32, 8, 128, 2, 2, 8), (512, 8, 8, 64, 1, 4, 2),
                                                      (256, 4, 4, 128, 2, 1, None)])
-def test_forward_host_equals_device(L, hq, hkv, hd, ud, rd, chunk):
-    """Pipelined host-buffer forward (4 groups exercise both staging slots and their reuse) gives
-    exactly the device-buffer result; two calls in a row on one workspace stay correct."""
+def test_forward_host_equals_device(L, hq, hkv, hd, ud, rd, chunk, mem):
+    """Host-buffer forward gives exactly the device-buffer result on both of its paths: pinned
+    buffers (the kernels read and write host memory directly), pageable or partly pageable buffers
+    (the pipelined copies; 4 groups exercise both staging slots and their reuse). Two calls in a row
+    on one workspace stay correct."""
     q, k, v = make_qkv(1, L, hq, hkv, hd, "bf16", seed=7 * L + hq)
-    qp, kp, vp = (x.pin_memory() for x in (q, k, v))
-    out = torch.empty_like(q).pin_memory()
-    lse = torch.empty(1, L, hq).pin_memory()
+    pin_in, pin_out = {"pinned": (True, True), "pageable": (False, False), "mixed": (True, False)}[mem]
+    qp, kp, vp = ((x.pin_memory() if pin_in else x.clone()) for x in (q, k, v))
+    out = torch.empty_like(q)
+    lse = torch.empty(1, L, hq)
+    if pin_out:
+        out, lse = out.pin_memory(), lse.pin_memory()
     ws = torch.empty(usp.usp_forward_workspace_size(q, k, ud, rd, chunk, host=True), dtype=torch.uint8,
                      device="cuda")
     od = torch.empty(q.shape, dtype=q.dtype, device="cuda")

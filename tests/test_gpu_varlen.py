@@ -152,3 +152,51 @@ def test_packed_autograd():
     rq, rk, rv = oracle.attn_direct_bwd(q, k, v, g, cu_seqlens=cu)
     for got, ref in ((qd.grad, rq), (kd.grad, rk), (vd.grad, rv)):
         assert np.abs(got.float().cpu().numpy() - ref).max() / max(np.abs(ref).max(), 1.0) <= 2e-2
+
+
+@pytest.mark.parametrize("L,hq,hkv,hd,ud,rd,cu", [(2048, 4, 2, 128, 2, 4, [0, 100, 700, 701, 1500, 2048]),
+                                                  (1024, 4, 4, 64, 1, 2, list(range(0, 1025, 128)))])
+def test_packed_ring_steps_match_oracle_blocks(L, hq, hkv, hd, ud, rd, cu):
+    """Packed samples in the single-step modes: USP_MODE_STEP's partial of ring step t matches the
+    oracle's block attention of rank r's queries against rank (r - t) mod rd's keys restricted to each
+    query's sample (rows with no key in that block: (0, -inf)); folding the steps with
+    USP_MODE_ACCUM reproduces USP_MODE_FUSED."""
+    import math
+    q, k, v = make_qkv(1, L, hq, hkv, hd, "bf16", seed=L + 3 * len(cu))
+    cud = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    Lu, Lr, c = L // (rd * ud), L // rd, L // (2 * rd)
+    hs = []
+    for x, H in zip((q, k, v), (hq, hkv, hkv)):
+        h = torch.empty(rd, ud, H // ud, 1, Lr, hd, dtype=x.dtype, device="cuda")
+        usp.usp_extract_a2a([x.cuda()], [h], rd, ud)
+        hs.append(h)
+    qh, kh, vh = hs
+    Q = oracle.a2a_fwd(oracle.extract_local(q.double().numpy(), rd, ud), ud)
+    K = oracle.a2a_fwd(oracle.extract_local(k.double().numpy(), rd, ud), ud)
+    V = oracle.a2a_fwd(oracle.extract_local(v.double().numpy(), rd, ud), ud)
+    _, _, seg = oracle.seg_bounds(cu, L)
+    scale = 1.0 / math.sqrt(hd)
+    acc_o, acc_l = torch.empty_like(qh), torch.empty(qh.shape[:5], device="cuda", dtype=torch.float32)
+    for t in range(rd):
+        o_t, l_t = torch.empty_like(qh), torch.empty_like(acc_l)
+        usp.usp_attn_fwd(qh, kh, vh, o_t, l_t, mode=usp.USP_MODE_STEP, step=t, cu_seqlens=cud)
+        usp.usp_attn_fwd(qh, kh, vh, acc_o, acc_l, mode=usp.USP_MODE_STEP if t == 0 else usp.USP_MODE_ACCUM,
+                         step=t, cu_seqlens=cud)
+        usp.usp_check()
+        o_np, l_np = o_t.float().cpu().numpy(), l_t.cpu().numpy()
+        for r in range(rd):
+            s = oracle.ring_source(r, t, rd)
+            qpos, kpos = oracle.zig(r, np.arange(Lr), c, rd), oracle.zig(s, np.arange(Lr), c, rd)
+            for u in range(ud):
+                o_ref, l_ref = oracle.attn_block(Q[r, u, :, 0], qpos, K[s, u, :, 0], V[s, u, :, 0], kpos, scale,
+                                                 qseg=seg[qpos], kseg=seg[kpos])
+                assert np.abs(o_np[r, u, :, 0] - o_ref).max() <= 2e-2
+                both = np.isneginf(l_np[r, u, :, 0]) & np.isneginf(l_ref)
+                assert np.array_equal(np.isneginf(l_np[r, u, :, 0]), np.isneginf(l_ref))
+                d = np.abs(np.where(both, 0, l_np[r, u, :, 0]) - np.where(both, 0, l_ref))
+                assert (d / np.maximum(np.abs(np.where(both, 0, l_ref)), 1)).max() <= 1e-3
+    fo, fl = torch.empty_like(qh), torch.empty_like(acc_l)
+    usp.usp_attn_fwd(qh, kh, vh, fo, fl, cu_seqlens=cud)
+    usp.usp_check()
+    assert (acc_o.float() - fo.float()).abs().max().item() <= 2e-2
+    assert ((acc_l - fl).abs() / fl.abs().clamp_min(1.0)).max().item() <= 1e-3
