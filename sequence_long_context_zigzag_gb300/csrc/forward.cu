@@ -191,27 +191,61 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
     if (!q_host || !k_host || !v_host || !out_host || !lse_host || !workspace) return USP_ERR_INVALID_ARG;
     if (workspace_bytes < ws_host(s)) return USP_ERR_INVALID_ARG;
     if (!aligned(workspace, kAlign)) return USP_ERR_ALIGN;
-    // Direct path: when every host buffer is mapped page-locked memory, the kernels read q, k, v and
-    // write out and lse in host memory themselves, over the CPU-GPU link (NVLink-C2C on GB300), in
-    // the order usp_forward reads and writes device memory; nothing is staged or copied by DMA.
-    {
-        void *qd = mapped_host(q_host), *kd = mapped_host(k_host), *vd = mapped_host(v_host);
-        void *od = mapped_host(out_host), *ld = mapped_host(lse_host);
-        if (qd && kd && vd && od && ld) {
-            Carve cv{static_cast<char *>(workspace), workspace_bytes};
-            void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *oh = cv.take(s.q_grp);
-            float *lh = static_cast<float *>(cv.take(s.lse_grp));
-            return forward_groups(s, d, qd, kd, vd, od, static_cast<float *>(ld), qh, kh, vh, oh, lh, stream);
-        }
-    }
-    // Copy path (pageable or unmapped host buffers): staged DMA copies of each head group's window,
-    // pipelined with the kernels on the library's streams.
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return USP_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_pipe_mu[dev]);
     HostPipe &hp = g_pipe[dev];
     if (!pipe_init(hp)) return USP_ERR_CUDA;
     cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
+    bool okc = true;
+    auto chk = [&](bool c) { okc = okc && c; };
+    // Direct path: when every host buffer is mapped page-locked memory, the kernels read q, k, v and
+    // write out and lse in host memory themselves, over the CPU-GPU link (NVLink-C2C on GB300);
+    // nothing is staged or copied by DMA. Per head group: the split + all-to-all gathers the group
+    // from host memory, the attention runs, and the inverse scatters out and lse to host memory on a
+    // second stream, where it overlaps the next group's gather (the link carries both directions at
+    // once; the two touch different buffers). The next attention waits for the scatter, which reads
+    // the head-sharded out and lse it overwrites.
+    {
+        void *qd = mapped_host(q_host), *kd = mapped_host(k_host), *vd = mapped_host(v_host);
+        void *odh = mapped_host(out_host), *ldh = mapped_host(lse_host);
+        if (qd && kd && vd && odh && ldh) {
+            Carve cv{static_cast<char *>(workspace), workspace_bytes};
+            void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *oh = cv.take(s.q_grp);
+            float *lh = static_cast<float *>(cv.take(s.lse_grp));
+            usp_stream_t side = reinterpret_cast<usp_stream_t>(hp.d2h);
+            chk(cudaEventRecord(hp.start, user) == cudaSuccess);
+            chk(cudaStreamWaitEvent(hp.d2h, hp.start, 0) == cudaSuccess);
+            const int ngroups = s.hq / s.hc;
+            for (int g = 0; g < ngroups && okc; ++g) {
+                const int g0 = g * s.hc, gk = g0 / s.G, sl = g & 1;
+                const void *srcs[3] = {qd, kd, vd};
+                void *dsts[3] = {qh, kh, vh};
+                usp_dims dd[3] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype),
+                                  dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype),
+                                  dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype)};
+                if ((rc = usp_extract_a2a(3, srcs, dsts, dd, 0, stream))) return rc;
+                if (g > 0) chk(cudaStreamWaitEvent(user, hp.out_free[sl ^ 1], 0) == cudaSuccess);
+                usp_attn_desc ad = d;
+                ad.hq = s.hc;
+                ad.hkv = s.hkc;
+                if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, stream))) return rc;
+                chk(cudaEventRecord(hp.out_ready[sl], user) == cudaSuccess);
+                chk(cudaStreamWaitEvent(hp.d2h, hp.out_ready[sl], 0) == cudaSuccess);
+                const void *os[2] = {oh, lh};
+                void *od[2] = {odh, ldh};
+                usp_dims odims[2] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype),
+                                     dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
+                if ((rc = usp_extract_a2a(2, os, od, odims, 1, side))) return rc;
+                chk(cudaEventRecord(hp.out_free[sl], hp.d2h) == cudaSuccess);
+            }
+            chk(cudaEventRecord(hp.d2h_done, hp.d2h) == cudaSuccess);
+            chk(cudaStreamWaitEvent(user, hp.d2h_done, 0) == cudaSuccess);
+            return okc ? USP_OK : USP_ERR_CUDA;
+        }
+    }
+    // Copy path (pageable or unmapped host buffers): staged DMA copies of each head group's window,
+    // pipelined with the kernels on the library's streams.
 
     Carve cv{static_cast<char *>(workspace), workspace_bytes};
     void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *oh = cv.take(s.q_grp);
@@ -228,8 +262,6 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
 
     const size_t rows = (size_t)s.bs * s.L;
     const size_t row_q = (size_t)s.hd * s.es;  // bytes of one (token, head) row
-    bool okc = true;
-    auto chk = [&](bool c) { okc = okc && c; };
     chk(cudaEventRecord(hp.start, user) == cudaSuccess);
     chk(cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess);
     chk(cudaStreamWaitEvent(hp.comp, hp.start, 0) == cudaSuccess);
