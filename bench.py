@@ -576,9 +576,9 @@ def main():
     perm_gbs = step.permute_bytes / (sum(perm_t) / args.steps) / 1e9
 
     # ---- end to end through the public API, host buffers ------------------------------------
-    # usp_forward_host: pinned host Q/K/V in, pinned host out/lse back; with mapped pinned buffers the
-    # split + all-to-all kernel reads each head group from host memory and the inverse writes out and
-    # lse there, every step; the caller-owned workspace is allocated once, outside the timed loop
+    # usp_forward_host: pinned host Q/K/V in, pinned host out/lse back, every step (the library moves
+    # the bytes over the CPU-GPU link with its permute kernels and the copy engines); the
+    # caller-owned workspace is allocated once, outside the timed loop
     qp, kp, vp = (x.pin_memory() for x in (q_h, k_h, v_h))
     out_h = torch.empty(w.bs, w.L, w.hq, w.hd, dtype=q_h.dtype).pin_memory()
     lse_h = torch.empty(w.bs, w.L, w.hq, dtype=torch.float32).pin_memory()
@@ -650,8 +650,10 @@ def main():
                          "algorithmic_flops_per_launch": per_group_flops},
             "e2e": {"value": dist.world * flops / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
-                    "api": f"usp_forward_host (pinned host buffers, read and written by the kernels over the "
-                           f"CPU-GPU link; head_chunk={chunk}; wall clock)"},
+                    "api": f"usp_forward_host (pinned host buffers; head_chunk={chunk}: the first group gathered "
+                           f"from host memory by the permute kernel while the copy engine brings the rest, the "
+                           f"last scattered straight back, the others returned by the copy engine during the "
+                           f"next group; wall clock)"},
             "gpu_launches": step.launches_per_step * args.steps,
             "rank_balance": balance,
             "backward": backward,
