@@ -342,6 +342,42 @@ def rank_balance(usp, w, q, k, v, reps=5):
     return res
 
 
+def secondary_workloads(usp, main_wi, steps=5, warmup=2):
+    """The other bf16 workloads, each timed briefly after the main timed region (not clock-sampled):
+    the same step (split + AllToAll4D, ring attention, inverse, per head group) on seeded N(0,1)
+    inputs drawn on the device. Reported as extra keys beside the main workload's line."""
+    res = []
+    for wi, w in enumerate(WORKLOADS):
+        if wi == main_wi or w.dtype != "bf16":
+            continue
+        g = torch.Generator(device="cuda").manual_seed(default_seed(wi))
+        q = torch.randn(w.bs, w.L, w.hq, w.hd, device="cuda", generator=g).to(torch.bfloat16)
+        k = torch.randn(w.bs, w.L, w.hkv, w.hd, device="cuda", generator=g).to(torch.bfloat16)
+        v = torch.randn(w.bs, w.L, w.hkv, w.hd, device="cuda", generator=g).to(torch.bfloat16)
+        step = Step(usp, w, q, k, v)
+        for _ in range(warmup):
+            step.run()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(steps):
+            step.run(record=True)
+        e1.record(st)
+        torch.cuda.synchronize()
+        usp.usp_check()
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        attn = sum(a.elapsed_time(b) for a, b in step.attn_events) / 1e3 / len(step.attn_events)
+        perm = sum(a.elapsed_time(b) + c.elapsed_time(d) for a, b, c, d in step.perm_events) / 1e3 / steps
+        res.append({"workload": w.name, "ms_per_step": round(t * 1e3, 3),
+                    "step_tflops": round(w.causal_flops / t / 1e12, 1),
+                    "attn_kernel_tflops": round(w.causal_flops / len(step.groups) / attn / 1e12, 1),
+                    "permute_gbs": round(step.permute_bytes / perm / 1e9, 1), "steps": steps})
+        del q, k, v, step
+        torch.cuda.empty_cache()
+    return res
+
+
 def attn_src_hash():
     """First 16 hex digits of the SHA-256 of the forward kernel's sources, concatenated in order."""
     hs = hashlib.sha256()
@@ -611,6 +647,9 @@ def main():
     backward = time_backward(usp, w, step, reps=min(20, max(3, args.steps // 2)))
     packed = packing(usp, w, step)
 
+    # ---- the other bf16 workloads, briefly (outside the timed region) ------------------------
+    others = secondary_workloads(usp, wi) if dist.world == 1 else None
+
     # ---- CPU baseline (the oracle on the host cores), rank 0 at N = 1 -----------------------
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -650,14 +689,15 @@ def main():
                          "algorithmic_flops_per_launch": per_group_flops},
             "e2e": {"value": dist.world * flops / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
-                    "api": f"usp_forward_host (pinned host buffers; head_chunk={chunk}: the first group gathered "
-                           f"from host memory by the permute kernel while the copy engine brings the rest, the "
-                           f"last scattered straight back, the others returned by the copy engine during the "
-                           f"next group; wall clock)"},
+                    "api": f"usp_forward_host (pinned host buffers, read and written by the permute kernels "
+                           f"over the CPU-GPU link; head_chunk={chunk}; wall clock)"},
             "gpu_launches": step.launches_per_step * args.steps,
             "rank_balance": balance,
             "backward": backward,
             "packing": packed,
+            "other_workloads": others,
+            "other_workloads_note": "each timed for 5 steps after the main timed region, inputs drawn on the "
+                                    "device, not clock-sampled",
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

@@ -253,13 +253,11 @@ USP_API int usp_forward(const void *q, const void *k, const void *v, void *out, 
  * Two paths, chosen per call:
  *   direct -- when all five host buffers are page-locked and mapped into the current device's address
  *     space (cudaHostAlloc, cudaHostRegister, a pinned torch tensor: cudaPointerGetAttributes reports
- *     cudaMemoryTypeHost with a device pointer), the kernels read and write them over the CPU-GPU
- *     link: the first head group's split + all-to-all gathers from host memory, and while its
- *     attention runs the copy engine brings the whole q, k, v into the workspace, from which later
- *     groups are gathered; each group but the last scatters out into the workspace (its head window
- *     then goes back by the copy engine during the next group's attention) and lse straight to host
- *     memory; the last group scatters straight to host memory. Each buffer must lie within one
- *     page-locked allocation.
+ *     cudaMemoryTypeHost with a device pointer), the kernels read q, k, v and write out and lse in host
+ *     memory themselves over the CPU-GPU link: per head group the split + all-to-all gathers from
+ *     host memory and the attention runs on `stream`, and the inverse scatters to host memory on a
+ *     library stream, overlapping the next group's gather. Each buffer must lie within one
+ *     page-locked allocation. Only the device part of the workspace is used.
  *   copy -- otherwise, pipelined per head group: the host-to-device copy of group g+1 and the
  *     device-to-host copy of group g-1 overlap the kernels of group g, on three streams the library
  *     keeps per device; pageable buffers work but their copies do not overlap.
@@ -267,8 +265,7 @@ USP_API int usp_forward(const void *q, const void *k, const void *v, void *out, 
  * waits for it (the host outputs are complete once `stream` is synchronised); calls on one device
  * are serialised by the library (its streams are per device).
  *   workspace : DEVICE buffer of at least usp_forward_workspace_size(d, head_chunk, 1) bytes
- *               (copy path: two staging slots per direction plus the full lse; direct path with
- *               several head groups: device copies of the whole q, k, v and out), 256-byte aligned.
+ *               (two staging slots per direction plus the full lse), 256-byte aligned.
  * Calls on one device are serialised on the library's streams; calls that share a workspace must be
  * ordered on one stream.
  */

@@ -58,21 +58,11 @@ size_t ws_backward(const FwdShape &s) {
     return align_up(d_all) + align_up(s.q_grp) * 3 + align_up(s.kv_hs) * 4 + align_up(s.lse_grp) * 2;
 }
 
-// the host-buffer forward adds, on its copy path, two slots of compact natural-order staging for q,
-// k, v and out and the full natural lse (copied back once at the end); on its direct path (several
-// head groups), device copies of the whole natural q, k, v and out
-size_t ws_host_copy(const FwdShape &s) {
-    const size_t lse_all = (size_t)s.bs * s.L * s.hq * 4;
-    return 2 * (align_up(s.q_grp) * 2 + align_up(s.kv_grp) * 2) + align_up(lse_all);
-}
-size_t ws_host_direct(const FwdShape &s) {
-    if (s.hc == s.hq) return 0;
-    const size_t tok = (size_t)s.bs * s.L;
-    return align_up(tok * s.hq * s.hd * s.es) * 2 + align_up(tok * s.hkv * s.hd * s.es) * 2;
-}
+// the host-buffer forward adds two slots of compact natural-order staging for q, k, v and out, and
+// the full natural lse (copied back once at the end)
 size_t ws_host(const FwdShape &s) {
-    const size_t a = ws_host_copy(s), b = ws_host_direct(s);
-    return ws_device(s) + (a > b ? a : b);
+    const size_t lse_all = (size_t)s.bs * s.L * s.hq * 4;
+    return ws_device(s) + 2 * (align_up(s.q_grp) * 2 + align_up(s.kv_grp) * 2) + align_up(lse_all);
 }
 
 struct Carve {
@@ -209,14 +199,13 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
     cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
     bool okc = true;
     auto chk = [&](bool c) { okc = okc && c; };
-    // Direct path: when every host buffer is mapped page-locked memory, the kernels read and write it
-    // themselves over the CPU-GPU link (NVLink-C2C on GB300). The link is exposed only at the two ends:
-    //   * group 0's split + all-to-all gathers from host memory; then, while group 0's attention
-    //     runs, the copy engine brings the whole natural q, k, v into device memory (contiguous
-    //     copies), from which the later groups are gathered;
-    //   * each group but the last scatters out into a device copy of the natural out (and lse
-    //     straight to host memory), and the copy engine sends that head window to the host while the
-    //     next group's attention runs; the last group scatters straight to host memory.
+    // Direct path: when every host buffer is mapped page-locked memory, the kernels read q, k, v and
+    // write out and lse in host memory themselves, over the CPU-GPU link (NVLink-C2C on GB300);
+    // nothing is staged or copied by DMA. Per head group: the split + all-to-all gathers the group
+    // from host memory, the attention runs, and the inverse scatters out and lse to host memory on a
+    // second stream, where it overlaps the next group's gather (the link carries both directions at
+    // once; the two touch different buffers). The next attention waits for the scatter, which reads
+    // the head-sharded out and lse it overwrites.
     {
         void *qd = mapped_host(q_host), *kd = mapped_host(k_host), *vd = mapped_host(v_host);
         void *odh = mapped_host(out_host), *ldh = mapped_host(lse_host);
@@ -224,64 +213,34 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
             Carve cv{static_cast<char *>(workspace), workspace_bytes};
             void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *oh = cv.take(s.q_grp);
             float *lh = static_cast<float *>(cv.take(s.lse_grp));
-            const int ngroups = s.hq / s.hc;
-            const size_t tok = (size_t)s.bs * s.L;
-            const size_t row_q = (size_t)s.hd * s.es;  // bytes of one (token, head) row
-            void *q_nat = nullptr, *k_nat = nullptr, *v_nat = nullptr, *o_nat = nullptr;
-            if (ngroups > 1) {
-                q_nat = cv.take(tok * s.hq * row_q);
-                k_nat = cv.take(tok * s.hkv * row_q);
-                v_nat = cv.take(tok * s.hkv * row_q);
-                o_nat = cv.take(tok * s.hq * row_q);
-                if (!o_nat) return USP_ERR_INVALID_ARG;
-            }
+            usp_stream_t side = reinterpret_cast<usp_stream_t>(hp.d2h);
             chk(cudaEventRecord(hp.start, user) == cudaSuccess);
-            chk(cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess);
             chk(cudaStreamWaitEvent(hp.d2h, hp.start, 0) == cudaSuccess);
+            const int ngroups = s.hq / s.hc;
             for (int g = 0; g < ngroups && okc; ++g) {
                 const int g0 = g * s.hc, gk = g0 / s.G, sl = g & 1;
-                const bool last = g == ngroups - 1;
-                if (g == 1) chk(cudaStreamWaitEvent(user, hp.in_ready[1], 0) == cudaSuccess);
-                const void *srcs[3] = {g == 0 ? qd : q_nat, g == 0 ? kd : k_nat, g == 0 ? vd : v_nat};
+                const void *srcs[3] = {qd, kd, vd};
                 void *dsts[3] = {qh, kh, vh};
                 usp_dims dd[3] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype),
                                   dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype),
                                   dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype)};
                 if ((rc = usp_extract_a2a(3, srcs, dsts, dd, 0, stream))) return rc;
-                if (g == 0 && ngroups > 1) {
-                    // the whole natural q, k, v by the copy engine, after group 0's gather
-                    chk(cudaEventRecord(hp.in_ready[0], user) == cudaSuccess);
-                    chk(cudaStreamWaitEvent(hp.h2d, hp.in_ready[0], 0) == cudaSuccess);
-                    chk(cudaMemcpyAsync(q_nat, q_host, tok * s.hq * row_q, cudaMemcpyHostToDevice, hp.h2d) ==
-                        cudaSuccess);
-                    chk(cudaMemcpyAsync(k_nat, k_host, tok * s.hkv * row_q, cudaMemcpyHostToDevice, hp.h2d) ==
-                        cudaSuccess);
-                    chk(cudaMemcpyAsync(v_nat, v_host, tok * s.hkv * row_q, cudaMemcpyHostToDevice, hp.h2d) ==
-                        cudaSuccess);
-                    chk(cudaEventRecord(hp.in_ready[1], hp.h2d) == cudaSuccess);
-                }
+                if (g > 0) chk(cudaStreamWaitEvent(user, hp.out_free[sl ^ 1], 0) == cudaSuccess);
                 usp_attn_desc ad = d;
                 ad.hq = s.hc;
                 ad.hkv = s.hkc;
                 if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, stream))) return rc;
+                chk(cudaEventRecord(hp.out_ready[sl], user) == cudaSuccess);
+                chk(cudaStreamWaitEvent(hp.d2h, hp.out_ready[sl], 0) == cudaSuccess);
                 const void *os[2] = {oh, lh};
-                void *od[2] = {last ? odh : o_nat, ldh};
+                void *od[2] = {odh, ldh};
                 usp_dims odims[2] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype),
                                      dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
-                if ((rc = usp_extract_a2a(2, os, od, odims, 1, stream))) return rc;
-                if (!last) {
-                    // this group's head window of out back to the host while the next group runs
-                    chk(cudaEventRecord(hp.out_ready[sl], user) == cudaSuccess);
-                    chk(cudaStreamWaitEvent(hp.d2h, hp.out_ready[sl], 0) == cudaSuccess);
-                    chk(copy2d(static_cast<char *>(out_host) + g0 * row_q, s.hq * row_q,
-                               static_cast<char *>(o_nat) + g0 * row_q, s.hq * row_q, s.hc * row_q, tok,
-                               cudaMemcpyDeviceToHost, hp.d2h));
-                }
+                if ((rc = usp_extract_a2a(2, os, od, odims, 1, side))) return rc;
+                chk(cudaEventRecord(hp.out_free[sl], hp.d2h) == cudaSuccess);
             }
             chk(cudaEventRecord(hp.d2h_done, hp.d2h) == cudaSuccess);
             chk(cudaStreamWaitEvent(user, hp.d2h_done, 0) == cudaSuccess);
-            chk(cudaEventRecord(hp.comp_done, hp.h2d) == cudaSuccess);
-            chk(cudaStreamWaitEvent(user, hp.comp_done, 0) == cudaSuccess);
             return okc ? USP_OK : USP_ERR_CUDA;
         }
     }
