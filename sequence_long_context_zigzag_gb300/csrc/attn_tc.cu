@@ -72,6 +72,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // global memory
 constexpr int kCuCache = 4096;
 constexpr uint64_t kSuperGroupKV = 64ull << 20;  // K/V bytes per super-group of units (launch_attn_tc)
+constexpr uint64_t kSingleGroupKV = 128ull << 20;  // largest group K/V numbered as its own super-group
 constexpr float kLn2 = 0.69314718055994531f;
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -129,7 +130,7 @@ struct TcParams {
     float *lse;
     int *status;
     uint32_t bs, Lr, c, rd, ud, Hl, Hkl, npairs, units;
-    uint32_t Gl, ngroups, nouter, sg;  // unit numbering: see decode_work
+    uint32_t Gl, ngroups, nouter, sg, sg_flip;  // unit numbering: see decode_work
     int causal, mode, step, lpt, split, ring_rank_only;
     float scale_log2;
     const int32_t *cu;  // packed samples' cumulative lengths, or nullptr
@@ -208,16 +209,23 @@ __device__ __forceinline__ Work decode_work(const TcParams &p, uint32_t cu_s, ui
     Work w;
     // Units that read the same K/V (one local KV head of one Ulysses rank and batch element: a
     // group of Gl query heads x nouter 256-row blocks) are numbered in super-groups of sg groups.
-    // Inside a super-group the blocks go heaviest first (outer), each block across the super-group's
-    // heads. sg is all groups unless a smaller super-group saves DRAM traffic (launch_attn_tc): then
+    // Inside a super-group the blocks go by cost (outer), each block across the super-group's heads.
+    // sg is all groups unless a smaller super-group saves DRAM traffic (launch_attn_tc): then
     // the SMs work on one or two heads at a time and read their K/V from L2 after the first touch,
     // even though the static schedule lets units that share K/V drift apart in time.
     const uint32_t per_group = p.nouter * p.Gl;
-    const uint32_t g0 = x / (p.sg * per_group) * p.sg;
+    const uint32_t sgi = x / (p.sg * per_group);  // super-group
+    const uint32_t g0 = sgi * p.sg;
     const uint32_t n = min(p.sg, p.ngroups - g0);
     const uint32_t xl = x - g0 * per_group;
-    const uint32_t outer = xl / (n * p.Gl);
+    uint32_t outer = xl / (n * p.Gl);
     const uint32_t rem = xl % (n * p.Gl);
+    // super-groups alternate in direction, the last one heaviest first (sg_flip = parity of the
+    // super-group count minus one): where one super-group ends and the next begins, the costs meet
+    // at the same level (both light or both heavy), which keeps the snake's pairs of rounds balanced
+    // across the boundary; a heavy-to-light order throughout put two of the heaviest units on the
+    // CTAs at the end of the boundary's round
+    if ((sgi ^ p.sg_flip) & 1u) outer = p.nouter - 1 - outer;
     const uint32_t grp = g0 + rem / p.Gl;
     w.b = grp % p.bs;
     const uint32_t uk = grp / p.bs;  // u Hkl + kh
@@ -1098,21 +1106,29 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     if (units >= (1ull << 31)) return USP_ERR_UNSUPPORTED;
     p.units = (uint32_t)units;
     // unit numbering: groups of units sharing K/V (4 L hd bytes of K and V per group), in
-    // super-groups of kSuperGroupKV of K/V where that saves DRAM traffic: not when all groups' K/V
-    // fits in the 126 MiB L2 (with a little spill), not when one group's K/V alone is larger than the
-    // budget, and not for packed samples (a unit then reads only its own sample's K/V). Working on
-    // fewer heads at a time costs time of its own (measured: 7% at L = 8192 with two super-groups,
-    // 50% for packed samples of 1024 with one head per super-group), while at L = 131072 (32 groups
-    // of 64 MiB) one group per super-group cuts DRAM reads from 151 to 60 GB per launch. At
-    // L = 262144 (a head group of 8 query heads: two groups of 128 MiB) one group per super-group cuts
-    // them from 58-88 GB to 14-26 GB per launch, but runs 2.8% fewer FLOP per clock (the clock under
-    // the power cap rose only 1.2%), so the budget stays below one such group.
+    // super-groups of kSuperGroupKV of K/V (or one group alone of up to kSingleGroupKV) where that
+    // saves DRAM traffic: not when all groups' K/V fits in the 126 MiB L2 (with a little spill), not
+    // when one group's K/V alone is larger than kSingleGroupKV (not measured), and not for packed
+    // samples (a unit then reads only its own sample's K/V). Working on fewer heads at a time costs
+    // time of its own where the heads' K/V fits L2 anyway (measured: 7% at L = 8192 with two
+    // super-groups, 50% for packed samples of 1024 with one head per super-group). Measured gains:
+    // L = 131072 (32 groups of 64 MiB): DRAM reads 151 -> 60 GB per launch; with the super-groups in
+    // alternating directions (decode_work) 3.6% more FLOP/s than all heads at once. L = 262144 (a head
+    // group of 8 query heads: two groups of 128 MiB): 3.2% more FLOP/s, most of it from the higher
+    // clock under the power cap that the smaller DRAM traffic leaves (1930 against 1810-1910 MHz).
+    // One ring rank's rows alone are not grouped: under zigzag they come from two chunks whose costs
+    // jump from the heaviest rows to the lightest, and a super-group numbered lightest first puts a
+    // second such jump into the walk (measured at L = 262144: rank 0's rows alone 8% slower than the
+    // other ranks', against 1% with all heads at once).
     p.Gl = p.Hl / p.Hkl;
     p.ngroups = p.ud * p.Hkl * p.bs;
     p.nouter = (uint32_t)ranks * p.npairs;
     const uint64_t kv_group = 4ull * (uint64_t)a.L * (uint64_t)a.hd;
-    const bool grouped = !p.cu && (uint64_t)p.ngroups * kv_group > (160ull << 20) && kv_group <= kSuperGroupKV;
-    p.sg = grouped ? (uint32_t)std::min<uint64_t>(p.ngroups, kSuperGroupKV / kv_group) : p.ngroups;
+    const bool grouped = !p.cu && a.ring_rank_only == 0 && (uint64_t)p.ngroups * kv_group > (160ull << 20) &&
+                         kv_group <= kSingleGroupKV;
+    p.sg = grouped ? (uint32_t)std::min<uint64_t>(p.ngroups, std::max<uint64_t>(1, kSuperGroupKV / kv_group))
+                   : p.ngroups;
+    p.sg_flip = ((p.ngroups + p.sg - 1) / p.sg - 1) & 1u;
     // persistent: one CTA per SM (the shared-memory footprint allows one), each walking its units
     const uint32_t grid = (uint32_t)std::min<uint64_t>(units, (uint64_t)std::max(di->sm_count, 1));
     // packed samples run a separate instantiation, so the one-sample kernel carries none of their code

@@ -3,7 +3,8 @@
 A unit of work is 256 query rows of one (ring rank, Ulysses rank, head, batch element); one CTA per SM
 walks a fixed list of units, carrying its barrier phases, stage ring and tensor-memory hand-offs from
 one unit into the next. Checked here at shapes with several units per CTA (more units than the GPU
-has SMs), including shapes whose K/V is larger than L2 (units numbered in super-groups of heads):
+has SMs), including shapes whose K/V is larger than L2 (units numbered in super-groups of heads, the
+super-groups in alternating directions, odd and even counts of them):
 the result matches the oracle on sampled rows; repeated launches give the same bits; the single-step
 modes (whose units can have no visible key at all) fold back into the whole-ring result; one ring
 rank's rows alone and packed samples give the bits of the full run.
@@ -25,7 +26,8 @@ SHAPES = [  # bs, L, hq, hkv, hd, ud, rd; units = rd * hq * bs * ceil(L / rd / 2
     (1, 4096, 16, 4, 128, 2, 4),     # 256 units, GQA
     (2, 3072, 8, 8, 64, 1, 3),       # 192 units, hd 64, odd ring degree
     (1, 6000, 8, 2, 128, 2, 2),      # 192 units, Lr = 3000: ragged last unit of every head
-    (1, 65536, 8, 8, 128, 1, 2),     # 2048 units; K/V 256 MiB: super-groups of 2 heads
+    (1, 65536, 8, 8, 128, 1, 2),     # 2048 units; K/V 256 MiB: four super-groups of 2 heads
+    (1, 65536, 6, 6, 128, 1, 2),     # 1536 units; K/V 192 MiB: three super-groups (alternating order)
     (4, 32768, 8, 4, 128, 2, 2),     # 4096 units; K/V 256 MiB over 16 (u, kv head, b) groups
 ]
 
