@@ -5,7 +5,8 @@ walks a fixed list of units, carrying its barrier phases, stage ring and tensor-
 one unit into the next. Checked here at shapes with several units per CTA (more units than the GPU
 has SMs), including shapes whose K/V is larger than L2 (units numbered in super-groups of heads, the
 super-groups in alternating directions, odd and even counts of them):
-the result matches the oracle on sampled rows; repeated launches give the same bits; the single-step
+every output row is written and matches the oracle on sampled rows; repeated launches give the same
+bits; the single-step
 modes (whose units can have no visible key at all) fold back into the whole-ring result; one ring
 rank's rows alone and packed samples give the bits of the full run.
 
@@ -29,6 +30,7 @@ SHAPES = [  # bs, L, hq, hkv, hd, ud, rd; units = rd * hq * bs * ceil(L / rd / 2
     (1, 65536, 8, 8, 128, 1, 2),     # 2048 units; K/V 256 MiB: four super-groups of 2 heads
     (1, 65536, 6, 6, 128, 1, 2),     # 1536 units; K/V 192 MiB: three super-groups (alternating order)
     (4, 32768, 8, 4, 128, 2, 2),     # 4096 units; K/V 256 MiB over 16 (u, kv head, b) groups
+    (1, 262144, 2, 2, 128, 1, 2),    # 2048 units; two 128 MiB groups, one per super-group
 ]
 
 
@@ -52,8 +54,9 @@ def natural(oh, lh, bs, L, hq, hd, ud, rd):
 
 
 def run(qh, kh, vh, hkv, **kw):
-    oh = torch.empty_like(qh)
-    lh = torch.empty(qh.shape[:5], device="cuda", dtype=torch.float32)
+    # NaN-filled, so that a unit the walk missed shows up
+    oh = torch.full_like(qh, float("nan"))
+    lh = torch.full(qh.shape[:5], float("nan"), device="cuda", dtype=torch.float32)
     usp.usp_attn_fwd(qh, kh, vh, oh, lh, hkv=hkv, **kw)
     usp.usp_check()  # a hand-off stall shows as a bounded wait running out, not as wrong bits
     return oh, lh
@@ -65,6 +68,8 @@ def test_many_units_per_cta_match_oracle(bs, L, hq, hkv, hd, ud, rd):
     qh, kh, vh = sharded(q, k, v, ud, rd)
     o1, l1 = run(qh, kh, vh, hkv)
     o2, l2 = run(qh, kh, vh, hkv)
+    # every row of every unit written (causal: each row sees at least its own key), the same bits twice
+    assert bool(torch.isfinite(o1).all()) and bool(torch.isfinite(l1).all())
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     out, lse = natural(o1, l1, bs, L, hq, hd, ud, rd)
     rows = make_rows(L, L // (2 * rd), 40, seed=L)
