@@ -11,9 +11,9 @@
 // Kernel design. A unit of work is 256 query rows = two 128-row Q tiles of one (r, u, h, b). The
 // kernel is persistent: one CTA per SM walks a static list of units, and its roles run through the
 // units without a CTA-wide barrier, so one unit's epilogue overlaps the next unit's Q / K loads and
-// first S products. Units are numbered heaviest first (see decode_work for the order of heads), and
-// round k of gridDim.x units goes to the CTAs in order for even k and in reverse for odd k, which
-// balances the rounds' decreasing costs.
+// first S products. Units are numbered by cost, heaviest first, or in super-groups of heads whose
+// directions alternate (see decode_work), and round k of gridDim.x units goes to the CTAs in order for
+// even k and in reverse for odd k, which balances rounds whose costs fall or rise steadily.
 //   warp 8      TMA producer: Q0, Q1 once per unit (after both issuers' last S product of the previous
 //               unit has completed); K and V tiles (128 keys x hd) through a ring of stages that runs on
 //               across units.
@@ -169,8 +169,8 @@ struct TileIter {
     uint32_t lomin[2], lomax[2];
 };
 
-// The k-th unit of this CTA: round k covers units [k G, (k + 1) G) of the heaviest-first numbering,
-// in CTA order for even k and in reverse order for odd k. False when the CTA has no k-th unit.
+// The k-th unit of this CTA: round k covers units [k G, (k + 1) G) of the numbering (decode_work), in
+// CTA order for even k and in reverse order for odd k. False when the CTA has no k-th unit.
 __device__ __forceinline__ bool unit_index(const TcParams &p, uint32_t k, uint32_t &x) {
     const uint32_t G = gridDim.x, b = blockIdx.x;
     x = k * G + ((k & 1u) ? G - 1 - b : b);
