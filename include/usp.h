@@ -254,10 +254,11 @@ USP_API int usp_forward(const void *q, const void *k, const void *v, void *out, 
  *   direct -- when all five host buffers are page-locked and mapped into the current device's address
  *     space (cudaHostAlloc, cudaHostRegister, a pinned torch tensor: cudaPointerGetAttributes reports
  *     cudaMemoryTypeHost with a device pointer), the kernels read q, k, v and write out and lse in host
- *     memory themselves over the CPU-GPU link: per head group the split + all-to-all gathers from
- *     host memory and the attention runs on `stream`, and the inverse scatters to host memory on a
- *     library stream, overlapping the next group's gather. Each buffer must lie within one
- *     page-locked allocation. Only the device part of the workspace is used.
+ *     memory themselves over the CPU-GPU link. The head groups alternate between two slots of device
+ *     buffers in the workspace: group g's attention runs on `stream` on all but 4 SMs, while group
+ *     g+1's split + all-to-all gathers from host memory and group g-1's inverse scatters to host
+ *     memory on two library streams, 2 thread blocks each (the first gather and the last scatter run
+ *     on the whole GPU). Each buffer must lie within one page-locked allocation.
  *   copy -- otherwise, pipelined per head group: the host-to-device copy of group g+1 and the
  *     device-to-host copy of group g-1 overlap the kernels of group g, on three streams the library
  *     keeps per device; pageable buffers work but their copies do not overlap.
@@ -265,7 +266,8 @@ USP_API int usp_forward(const void *q, const void *k, const void *v, void *out, 
  * waits for it (the host outputs are complete once `stream` is synchronised); calls on one device
  * are serialised by the library (its streams are per device).
  *   workspace : DEVICE buffer of at least usp_forward_workspace_size(d, head_chunk, 1) bytes
- *               (two staging slots per direction plus the full lse), 256-byte aligned.
+ *               (copy path: two staging slots per direction plus the full lse; direct path: two
+ *               slots of the head-sharded buffers), 256-byte aligned.
  * Calls on one device are serialised on the library's streams; calls that share a workspace must be
  * ordered on one stream.
  */

@@ -1130,7 +1130,8 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
                    : p.ngroups;
     p.sg_flip = ((p.ngroups + p.sg - 1) / p.sg - 1) & 1u;
     // persistent: one CTA per SM (the shared-memory footprint allows one), each walking its units
-    const uint32_t grid = (uint32_t)std::min<uint64_t>(units, (uint64_t)std::max(di->sm_count, 1));
+    const int ctas = a.max_ctas > 0 ? std::min(a.max_ctas, di->sm_count) : di->sm_count;
+    const uint32_t grid = (uint32_t)std::min<uint64_t>(units, (uint64_t)std::max(ctas, 1));
     // packed samples run a separate instantiation, so the one-sample kernel carries none of their code
     if (p.cu)
         return a.hd == 128 ? launch_typed<128, true>(p, grid, s) : launch_typed<64, true>(p, grid, s);

@@ -18,6 +18,11 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// usp_forward_host's direct path: SMs the attention leaves to the host transfers that run beside it,
+// and thread blocks per such transfer (each block holds at most one SM)
+constexpr int kXferReserveSms = 4;
+constexpr int kXferBlocks = 2;
+
 struct FwdShape {
     int64_t bs, L;
     int hq, hkv, hd, rd, ud, hc, hkc, G, es, split;
@@ -58,11 +63,13 @@ size_t ws_backward(const FwdShape &s) {
     return align_up(d_all) + align_up(s.q_grp) * 3 + align_up(s.kv_hs) * 4 + align_up(s.lse_grp) * 2;
 }
 
-// the host-buffer forward adds two slots of compact natural-order staging for q, k, v and out, and
-// the full natural lse (copied back once at the end)
+// the host-buffer forward: the copy path adds two slots of compact natural-order staging for q, k, v
+// and out, and the full natural lse (copied back once at the end); the direct path takes two slots of
+// the device buffers
 size_t ws_host(const FwdShape &s) {
     const size_t lse_all = (size_t)s.bs * s.L * s.hq * 4;
-    return ws_device(s) + 2 * (align_up(s.q_grp) * 2 + align_up(s.kv_grp) * 2) + align_up(lse_all);
+    const size_t copy_path = ws_device(s) + 2 * (align_up(s.q_grp) * 2 + align_up(s.kv_grp) * 2) + align_up(lse_all);
+    return std::max(copy_path, 2 * ws_device(s));  // the direct path: two slots of device buffers
 }
 
 struct Carve {
@@ -111,9 +118,8 @@ bool pipe_init(HostPipe &hp) {
     return true;
 }
 
-// The forward of every head group, on buffers the kernels can address: the composed split +
-// all-to-all of q, k, v, the ring attention, and the composed inverse of out and lse. q, k, v, out and
-// lse may be device memory or mapped page-locked host memory (usp_forward_host's direct path).
+// The forward of every head group on device buffers (usp_forward): the composed split + all-to-all
+// of q, k, v, the ring attention, and the composed inverse of out and lse.
 int forward_groups(const FwdShape &s, const usp_attn_desc &d, const void *q, const void *k, const void *v, void *out,
                    float *lse, void *qh, void *kh, void *vh, void *oh, float *lh, usp_stream_t stream) {
     int rc;
@@ -201,43 +207,72 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
     auto chk = [&](bool c) { okc = okc && c; };
     // Direct path: when every host buffer is mapped page-locked memory, the kernels read q, k, v and
     // write out and lse in host memory themselves, over the CPU-GPU link (NVLink-C2C on GB300);
-    // nothing is staged or copied by DMA. Per head group: the split + all-to-all gathers the group
-    // from host memory, the attention runs, and the inverse scatters out and lse to host memory on a
-    // second stream, where it overlaps the next group's gather (the link carries both directions at
-    // once; the two touch different buffers). The next attention waits for the scatter, which reads
-    // the head-sharded out and lse it overwrites.
+    // nothing is staged or copied by DMA. The head groups are pipelined over two slots of device
+    // buffers: while group g's attention runs, group g + 1's split + all-to-all gathers its input from
+    // host memory (one stream) and group g - 1's inverse scatters out and lse to host memory (another
+    // stream). The persistent attention then leaves kXferReserveSms SMs to those two transfers, each
+    // capped at kXferBlocks thread blocks; the first gather and the last scatter have the GPU to
+    // themselves and run uncapped.
     {
         void *qd = mapped_host(q_host), *kd = mapped_host(k_host), *vd = mapped_host(v_host);
         void *odh = mapped_host(out_host), *ldh = mapped_host(lse_host);
         if (qd && kd && vd && odh && ldh) {
             Carve cv{static_cast<char *>(workspace), workspace_bytes};
-            void *qh = cv.take(s.q_grp), *kh = cv.take(s.kv_hs), *vh = cv.take(s.kv_hs), *oh = cv.take(s.q_grp);
-            float *lh = static_cast<float *>(cv.take(s.lse_grp));
-            usp_stream_t side = reinterpret_cast<usp_stream_t>(hp.d2h);
-            chk(cudaEventRecord(hp.start, user) == cudaSuccess);
-            chk(cudaStreamWaitEvent(hp.d2h, hp.start, 0) == cudaSuccess);
+            void *qh[2], *kh[2], *vh[2], *oh[2];
+            float *lh[2];
+            for (int b = 0; b < 2; ++b) {
+                qh[b] = cv.take(s.q_grp);
+                kh[b] = cv.take(s.kv_hs);
+                vh[b] = cv.take(s.kv_hs);
+                oh[b] = cv.take(s.q_grp);
+                lh[b] = static_cast<float *>(cv.take(s.lse_grp));
+            }
+            if (!lh[1]) return USP_ERR_INVALID_ARG;
             const int ngroups = s.hq / s.hc;
-            for (int g = 0; g < ngroups && okc; ++g) {
-                const int g0 = g * s.hc, gk = g0 / s.G, sl = g & 1;
+            const bool piped = ngroups > 1;
+            const int attn_ctas = piped ? std::max(1, device_info()->sm_count - kXferReserveSms) : 0;
+            usp_stream_t gat = reinterpret_cast<usp_stream_t>(hp.h2d), sca = reinterpret_cast<usp_stream_t>(hp.d2h);
+            auto gather = [&](int g, usp_stream_t st, int max_blocks) {
+                const int g0 = g * s.hc, gk = g0 / s.G, b = g & 1;
                 const void *srcs[3] = {qd, kd, vd};
-                void *dsts[3] = {qh, kh, vh};
+                void *dsts[3] = {qh[b], kh[b], vh[b]};
                 usp_dims dd[3] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype),
                                   dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype),
                                   dims_of(s, s.hkc, s.hkv, gk, s.hd, d.dtype)};
-                if ((rc = usp_extract_a2a(3, srcs, dsts, dd, 0, stream))) return rc;
-                if (g > 0) chk(cudaStreamWaitEvent(user, hp.out_free[sl ^ 1], 0) == cudaSuccess);
-                usp_attn_desc ad = d;
-                ad.hq = s.hc;
-                ad.hkv = s.hkc;
-                if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, stream))) return rc;
-                chk(cudaEventRecord(hp.out_ready[sl], user) == cudaSuccess);
-                chk(cudaStreamWaitEvent(hp.d2h, hp.out_ready[sl], 0) == cudaSuccess);
-                const void *os[2] = {oh, lh};
+                return extract_a2a_capped(3, srcs, dsts, dd, 0, max_blocks, st);
+            };
+            auto scatter = [&](int g, usp_stream_t st, int max_blocks) {
+                const int g0 = g * s.hc, b = g & 1;
+                const void *os[2] = {oh[b], lh[b]};
                 void *od[2] = {odh, ldh};
                 usp_dims odims[2] = {dims_of(s, s.hc, s.hq, g0, s.hd, d.dtype),
                                      dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
-                if ((rc = usp_extract_a2a(2, os, od, odims, 1, side))) return rc;
-                chk(cudaEventRecord(hp.out_free[sl], hp.d2h) == cudaSuccess);
+                return extract_a2a_capped(2, os, od, odims, 1, max_blocks, st);
+            };
+            chk(cudaEventRecord(hp.start, user) == cudaSuccess);
+            chk(cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess);
+            chk(cudaStreamWaitEvent(hp.d2h, hp.start, 0) == cudaSuccess);
+            if ((rc = gather(0, stream, 0))) return rc;
+            for (int g = 0; g < ngroups && okc; ++g) {
+                const int b = g & 1;
+                // inputs of slot b gathered (group 0: earlier on this stream); outputs of slot b
+                // scattered (group g - 2)
+                if (g > 0) chk(cudaStreamWaitEvent(user, hp.in_ready[b], 0) == cudaSuccess);
+                if (g > 1) chk(cudaStreamWaitEvent(user, hp.out_free[b], 0) == cudaSuccess);
+                usp_attn_desc ad = d;
+                ad.hq = s.hc;
+                ad.hkv = s.hkc;
+                if ((rc = attn_fwd_capped(qh[b], kh[b], vh[b], oh[b], lh[b], ad, attn_ctas, stream))) return rc;
+                chk(cudaEventRecord(hp.in_free[b], user) == cudaSuccess);  // slot b's inputs read, outputs written
+                if (g + 1 < ngroups) {
+                    // group g + 1 into the other slot, once group g - 1's attention has read it
+                    if (g > 0) chk(cudaStreamWaitEvent(hp.h2d, hp.in_free[b ^ 1], 0) == cudaSuccess);
+                    if ((rc = gather(g + 1, gat, kXferBlocks))) return rc;
+                    chk(cudaEventRecord(hp.in_ready[b ^ 1], hp.h2d) == cudaSuccess);
+                }
+                chk(cudaStreamWaitEvent(hp.d2h, hp.in_free[b], 0) == cudaSuccess);
+                if ((rc = scatter(g, sca, g + 1 < ngroups ? kXferBlocks : 0))) return rc;
+                chk(cudaEventRecord(hp.out_free[b], hp.d2h) == cudaSuccess);
             }
             chk(cudaEventRecord(hp.d2h_done, hp.d2h) == cudaSuccess);
             chk(cudaStreamWaitEvent(user, hp.d2h_done, 0) == cudaSuccess);

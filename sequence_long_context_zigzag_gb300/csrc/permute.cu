@@ -323,7 +323,7 @@ int launch_permute(const PermArgs &a, cudaStream_t s) {
     p.f_ud = FastDiv(p.ud);
     p.f_Lr = FastDiv(p.Lr);
     int64_t blocks = (nbatch + kWarps - 1) / kWarps;
-    const int64_t cap = (int64_t)di->sm_count * 8;
+    const int64_t cap = a.max_blocks > 0 ? (int64_t)a.max_blocks : (int64_t)di->sm_count * 8;
     if (blocks > cap) blocks = cap;
     permute_rows_kernel<<<(unsigned)blocks, kWarps * 32, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA;

@@ -139,7 +139,7 @@ int usp_a2a4d(const void *src, void *dst, usp_dims d, int dir, usp_stream_t stre
 
 // the multi-tensor permutes: usp_extract_a2a (split + all-to-all composed) and usp_a2a4d_multi
 static int permute_multi(int n, const void *const *src, void *const *dst, const usp_dims *d, int mode,
-                         usp_stream_t stream) {
+                         usp_stream_t stream, int max_blocks = 0) {
     if (n < 1 || n > kMaxPermJobs || !src || !dst || !d) return USP_ERR_INVALID_ARG;
     PermArgs a{};
     a.njobs = n;
@@ -170,6 +170,7 @@ static int permute_multi(int n, const void *const *src, void *const *dst, const 
     a.split = d[0].split;
     a.bs = d[0].bs; a.L = d[0].L;
     a.rd = d[0].rd; a.ud = d[0].ud;
+    a.max_blocks = max_blocks;
     return launch_permute(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -251,23 +252,7 @@ int usp_attn_bwd(const void *q, const void *k, const void *v, const void *dout, 
 
 int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, usp_attn_desc d,
                  usp_stream_t stream) {
-    int rc = check_attn_desc(d);
-    if (rc) return rc;
-    if (d.bs == 0 || d.L == 0) return USP_OK;
-    if (!q || !k || !v || !out || !lse) return USP_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 16))
-        return USP_ERR_ALIGN;
-    AttnArgs a = attn_args(d);
-    a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (d.dtype == USP_BF16) {
-        // the tensor-core launcher sets each kernel's shared-memory attribute on its first launch on
-        // a device and remembers it; host threads launching at the same time take turns here
-        static std::mutex tc_mu;
-        std::lock_guard<std::mutex> lk(tc_mu);
-        return launch_attn_tc(a, s);
-    }
-    return launch_attn_simt(a, s);
+    return attn_fwd_capped(q, k, v, out, lse, d, 0, stream);
 }
 
 int usp_lse_merge(void *o_acc, float *lse_acc, const void *o_new, const float *lse_new, int64_t rows,
@@ -311,3 +296,34 @@ int usp_check(usp_stream_t stream) {
 }
 
 }  // extern "C"
+
+namespace usp {
+
+int extract_a2a_capped(int n, const void *const *src, void *const *dst, const usp_dims *d, int inverse,
+                       int max_blocks, usp_stream_t stream) {
+    return permute_multi(n, src, dst, d, inverse ? PERM_FUSED_INV : PERM_FUSED_FWD, stream, max_blocks);
+}
+
+int attn_fwd_capped(const void *q, const void *k, const void *v, void *out, float *lse, const usp_attn_desc &d,
+                    int max_ctas, usp_stream_t stream) {
+    int rc = check_attn_desc(d);
+    if (rc) return rc;
+    if (d.bs == 0 || d.L == 0) return USP_OK;
+    if (!q || !k || !v || !out || !lse) return USP_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 16))
+        return USP_ERR_ALIGN;
+    AttnArgs a = attn_args(d);
+    a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
+    a.max_ctas = max_ctas;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d.dtype == USP_BF16) {
+        // the tensor-core launcher sets each kernel's shared-memory attribute on its first launch on
+        // a device and remembers it; host threads launching at the same time take turns here
+        static std::mutex tc_mu;
+        std::lock_guard<std::mutex> lk(tc_mu);
+        return launch_attn_tc(a, s);
+    }
+    return launch_attn_simt(a, s);
+}
+
+}  // namespace usp

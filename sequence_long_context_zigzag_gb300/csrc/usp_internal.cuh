@@ -135,6 +135,7 @@ struct PermArgs {
     int64_t bs, L;
     int32_t rd, ud;
     int32_t r_fixed, u_fixed;  // >= 0 when only one virtual rank takes part (extract only)
+    int32_t max_blocks;        // > 0: at most this many thread blocks (grid-stride), else the default
 };
 int launch_permute(const PermArgs &a, cudaStream_t s);
 
@@ -150,9 +151,17 @@ struct AttnArgs {
     float scale;
     const int32_t *cu;  // packed samples' cumulative lengths (nseq + 1 entries), or nullptr
     int32_t nseq;       // > 1 when packed
+    int32_t max_ctas;   // > 0: the persistent tensor-core kernel runs at most this many CTAs
 };
 int launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 int launch_attn_tc(const AttnArgs &a, cudaStream_t s);
+
+// usp_extract_a2a and usp_attn_fwd with a cap on the SMs they take (0: no cap), for pipelines that
+// keep a few SMs free for another stream's kernels
+int extract_a2a_capped(int n, const void *const *src, void *const *dst, const usp_dims *d, int inverse,
+                       int max_blocks, usp_stream_t stream);
+int attn_fwd_capped(const void *q, const void *k, const void *v, void *out, float *lse, const usp_attn_desc &d,
+                    int max_ctas, usp_stream_t stream);
 
 // backward: the forward's arguments plus dout, delta and the three gradients
 struct BwdArgs {
