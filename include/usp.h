@@ -255,10 +255,12 @@ USP_API int usp_forward(const void *q, const void *k, const void *v, void *out, 
  *     space (cudaHostAlloc, cudaHostRegister, a pinned torch tensor: cudaPointerGetAttributes reports
  *     cudaMemoryTypeHost with a device pointer), the kernels read q, k, v and write out and lse in host
  *     memory themselves over the CPU-GPU link. The head groups alternate between two slots of device
- *     buffers in the workspace: group g's attention runs on `stream` on all but 4 SMs, while group
- *     g+1's split + all-to-all gathers from host memory and group g-1's inverse scatters to host
- *     memory on two library streams, 2 thread blocks each (the first gather and the last scatter run
- *     on the whole GPU). Each buffer must lie within one page-locked allocation.
+ *     buffers in the workspace: group g's attention runs on `stream` while group g+1's split +
+ *     all-to-all gathers from host memory and group g-1's inverse scatters to host memory on two
+ *     library streams. For bf16 without packed samples, each transfer gets a few thread blocks,
+ *     enough to finish within about half of an attention, and the attention leaves that many SMs
+ *     free; the first gather and the last scatter run on the whole GPU. Each buffer must lie within
+ *     one page-locked allocation.
  *   copy -- otherwise, pipelined per head group: the host-to-device copy of group g+1 and the
  *     device-to-host copy of group g-1 overlap the kernels of group g, on three streams the library
  *     keeps per device; pageable buffers work but their copies do not overlap.

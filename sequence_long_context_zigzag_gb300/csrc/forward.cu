@@ -7,6 +7,8 @@
 // on three internal streams, the host-to-device copy of group g+1 and the device-to-host copy of
 // group g-1 with the kernels of group g (two staging slots per direction) -- or, when the host
 // buffers are mapped page-locked memory, lets the kernels read and write them directly.
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "usp_internal.cuh"
@@ -18,10 +20,14 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-// usp_forward_host's direct path: SMs the attention leaves to the host transfers that run beside it,
-// and thread blocks per such transfer (each block holds at most one SM)
-constexpr int kXferReserveSms = 4;
-constexpr int kXferBlocks = 2;
+// usp_forward_host's direct path runs a head group's host transfers beside the previous or next
+// group's attention, on a few thread blocks each (a block holds at most one SM, which the persistent
+// attention then leaves free). Blocks per transfer are chosen so that it moves its bytes in about
+// half of the attention's time, from per-block rates over NVLink-C2C measured on GB300 (about 18 GB/s
+// reading pinned host memory and 16 GB/s writing it; 210 and 159 GB/s uncapped) and the attention
+// estimated at 1.5 PFLOP/s. More than kXferMaxBlocks per transfer: no overlap.
+constexpr double kXferReadGBs = 18.0, kXferWriteGBs = 16.0, kXferAttnTflops = 1500.0;
+constexpr int kXferMaxBlocks = 8;
 
 struct FwdShape {
     int64_t bs, L;
@@ -118,6 +124,26 @@ bool pipe_init(HostPipe &hp) {
     return true;
 }
 
+struct XferPlan {
+    int in_blocks = 0, out_blocks = 0;  // 0: the transfers do not run beside the attention
+};
+
+XferPlan xfer_plan(const FwdShape &s, const usp_attn_desc &d) {
+    XferPlan x;
+    // one group; packed samples (their cost is unknown here); fp32 (the attention is not persistent)
+    if (s.hq / s.hc < 2 || d.nseq > 1 || d.dtype != USP_BF16) return x;
+    const double flop = 4.0 * s.bs * s.hc * s.hd * (double)s.L * s.L * (d.causal ? 0.5 : 1.0);
+    const double t_attn = flop / (kXferAttnTflops * 1e12);
+    const double in_b = (double)s.bs * s.L * (s.hc + 2 * s.hkc) * s.hd * s.es;
+    const double out_b = (double)s.bs * s.L * s.hc * ((double)s.hd * s.es + 4);
+    const int bi = (int)std::ceil(2.0 * in_b / (kXferReadGBs * 1e9 * t_attn));
+    const int bo = (int)std::ceil(2.0 * out_b / (kXferWriteGBs * 1e9 * t_attn));
+    if (bi > kXferMaxBlocks || bo > kXferMaxBlocks) return x;
+    x.in_blocks = std::max(bi, 1);
+    x.out_blocks = std::max(bo, 1);
+    return x;
+}
+
 // The forward of every head group on device buffers (usp_forward): the composed split + all-to-all
 // of q, k, v, the ring attention, and the composed inverse of out and lse.
 int forward_groups(const FwdShape &s, const usp_attn_desc &d, const void *q, const void *k, const void *v, void *out,
@@ -210,9 +236,10 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
     // nothing is staged or copied by DMA. The head groups are pipelined over two slots of device
     // buffers: while group g's attention runs, group g + 1's split + all-to-all gathers its input from
     // host memory (one stream) and group g - 1's inverse scatters out and lse to host memory (another
-    // stream). The persistent attention then leaves kXferReserveSms SMs to those two transfers, each
-    // capped at kXferBlocks thread blocks; the first gather and the last scatter have the GPU to
-    // themselves and run uncapped.
+    // stream). The persistent attention then leaves as many SMs as those two transfers have thread
+    // blocks (xfer_plan); the first gather and the last scatter have the GPU to themselves and run
+    // uncapped. Without a plan (xfer_plan: 0) every launch is uncapped and the transfers wait for
+    // the SMs the attention holds.
     {
         void *qd = mapped_host(q_host), *kd = mapped_host(k_host), *vd = mapped_host(v_host);
         void *odh = mapped_host(out_host), *ldh = mapped_host(lse_host);
@@ -229,8 +256,10 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
             }
             if (!lh[1]) return USP_ERR_INVALID_ARG;
             const int ngroups = s.hq / s.hc;
-            const bool piped = ngroups > 1;
-            const int attn_ctas = piped ? std::max(1, device_info()->sm_count - kXferReserveSms) : 0;
+            const XferPlan xp = xfer_plan(s, d);
+            const DeviceInfo *di = device_info();
+            if (!di) return USP_ERR_CUDA;
+            const int attn_ctas = xp.in_blocks ? std::max(1, di->sm_count - xp.in_blocks - xp.out_blocks) : 0;
             usp_stream_t gat = reinterpret_cast<usp_stream_t>(hp.h2d), sca = reinterpret_cast<usp_stream_t>(hp.d2h);
             auto gather = [&](int g, usp_stream_t st, int max_blocks) {
                 const int g0 = g * s.hc, gk = g0 / s.G, b = g & 1;
@@ -267,11 +296,11 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
                 if (g + 1 < ngroups) {
                     // group g + 1 into the other slot, once group g - 1's attention has read it
                     if (g > 0) chk(cudaStreamWaitEvent(hp.h2d, hp.in_free[b ^ 1], 0) == cudaSuccess);
-                    if ((rc = gather(g + 1, gat, kXferBlocks))) return rc;
+                    if ((rc = gather(g + 1, gat, xp.in_blocks))) return rc;
                     chk(cudaEventRecord(hp.in_ready[b ^ 1], hp.h2d) == cudaSuccess);
                 }
                 chk(cudaStreamWaitEvent(hp.d2h, hp.in_free[b], 0) == cudaSuccess);
-                if ((rc = scatter(g, sca, g + 1 < ngroups ? kXferBlocks : 0))) return rc;
+                if ((rc = scatter(g, sca, g + 1 < ngroups ? xp.out_blocks : 0))) return rc;
                 chk(cudaEventRecord(hp.out_free[b], hp.d2h) == cudaSuccess);
             }
             chk(cudaEventRecord(hp.d2h_done, hp.d2h) == cudaSuccess);
