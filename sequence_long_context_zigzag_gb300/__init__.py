@@ -377,9 +377,11 @@ def usp_forward_noalloc(q, k, v, out, lse, ud: int, rd: int, causal: bool = True
 def usp_forward_host(q, k, v, out, lse, ud: int, rd: int, causal: bool = True, scale: Optional[float] = None,
                      head_chunk: Optional[int] = None, workspace: Optional[torch.Tensor] = None, device=None,
                      stream=None):
-    """The whole forward from host tensors to host tensors (pin them for overlapped copies), pipelined
-    per head group inside the library. Work is queued on ``stream`` (the current stream of ``device``);
-    synchronise it before reading ``out`` / ``lse``."""
+    """The whole forward from host tensors to host tensors, pipelined per head group inside the
+    library. With all five tensors pinned, the library's kernels read and write them directly over the
+    CPU-GPU link, beside the attention of the neighbouring head group; otherwise each group's window is
+    copied in and out (pageable tensors: without overlap). Work is queued on ``stream`` (the current
+    stream of ``device``); synchronise it before reading ``out`` / ``lse``."""
     for t in (q, k, v, out, lse):
         _need(isinstance(t, torch.Tensor) and not t.is_cuda and t.is_contiguous(), "expected contiguous host tensors")
     _check_natural(q, k, v, out, lse)
