@@ -65,3 +65,28 @@ def test_attention_host_helper():
     o_ref, l_ref = oracle.attn_direct(q, k, v)
     assert np.abs(out.float().numpy() - o_ref).max() <= 2e-2
     assert (np.abs(lse.numpy() - l_ref) / np.maximum(np.abs(l_ref), 1)).max() <= 1e-3
+
+
+@pytest.mark.parametrize("L,hq,hkv,ud,rd", [(32768, 32, 8, 1, 8), (16384, 24, 6, 2, 4)])
+def test_forward_host_overlapped_transfers(L, hq, hkv, ud, rd):
+    """Pinned buffers at lengths where each head group's attention is long enough for the library to
+    run the neighbouring groups' host transfers beside it, on a few thread blocks, with the attention
+    on the remaining SMs (4 and 3 head groups of 8 query heads: both buffer slots, an odd count).
+    Bit-identical to the device-buffer forward (the same units, on fewer CTAs), three calls in a row
+    on one workspace."""
+    q, k, v = make_qkv(1, L, hq, hkv, 128, "bf16", seed=L + hq)
+    qp, kp, vp = (x.pin_memory() for x in (q, k, v))
+    out = torch.empty_like(q).pin_memory()
+    lse = torch.empty(1, L, hq).pin_memory()
+    ws = torch.empty(usp.usp_forward_workspace_size(q, k, ud, rd, 8, host=True), dtype=torch.uint8, device="cuda")
+    od = torch.empty(q.shape, dtype=q.dtype, device="cuda")
+    ld = torch.empty(1, L, hq, device="cuda")
+    usp.usp_forward(q.cuda(), k.cuda(), v.cuda(), od, ld, ud, rd, head_chunk=8)
+    od, ld = od.cpu(), ld.cpu()
+    for _ in range(3):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        usp.usp_forward_host(qp, kp, vp, out, lse, ud, rd, head_chunk=8, workspace=ws)
+        torch.cuda.current_stream().synchronize()
+        usp.usp_check()
+        assert torch.equal(out, od) and torch.equal(lse, ld)
