@@ -278,10 +278,19 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
                                      dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
                 return extract_a2a_capped(2, os, od, odims, 1, max_blocks, st);
             };
+            // an error after work was queued still orders the caller's stream after everything this
+            // call put on the library's streams
+            auto fail = [&](int code) {
+                cudaEventRecord(hp.comp_done, hp.h2d);
+                cudaStreamWaitEvent(user, hp.comp_done, 0);
+                cudaEventRecord(hp.d2h_done, hp.d2h);
+                cudaStreamWaitEvent(user, hp.d2h_done, 0);
+                return code;
+            };
             chk(cudaEventRecord(hp.start, user) == cudaSuccess);
             chk(cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess);
             chk(cudaStreamWaitEvent(hp.d2h, hp.start, 0) == cudaSuccess);
-            if ((rc = gather(0, stream, 0))) return rc;
+            if ((rc = gather(0, stream, 0))) return fail(rc);
             for (int g = 0; g < ngroups && okc; ++g) {
                 const int b = g & 1;
                 // inputs of slot b gathered (group 0: earlier on this stream); outputs of slot b
@@ -291,16 +300,16 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
                 usp_attn_desc ad = d;
                 ad.hq = s.hc;
                 ad.hkv = s.hkc;
-                if ((rc = attn_fwd_capped(qh[b], kh[b], vh[b], oh[b], lh[b], ad, attn_ctas, stream))) return rc;
+                if ((rc = attn_fwd_capped(qh[b], kh[b], vh[b], oh[b], lh[b], ad, attn_ctas, stream))) return fail(rc);
                 chk(cudaEventRecord(hp.in_free[b], user) == cudaSuccess);  // slot b's inputs read, outputs written
                 if (g + 1 < ngroups) {
                     // group g + 1 into the other slot, once group g - 1's attention has read it
                     if (g > 0) chk(cudaStreamWaitEvent(hp.h2d, hp.in_free[b ^ 1], 0) == cudaSuccess);
-                    if ((rc = gather(g + 1, gat, xp.in_blocks))) return rc;
+                    if ((rc = gather(g + 1, gat, xp.in_blocks))) return fail(rc);
                     chk(cudaEventRecord(hp.in_ready[b ^ 1], hp.h2d) == cudaSuccess);
                 }
                 chk(cudaStreamWaitEvent(hp.d2h, hp.in_free[b], 0) == cudaSuccess);
-                if ((rc = scatter(g, sca, g + 1 < ngroups ? xp.out_blocks : 0))) return rc;
+                if ((rc = scatter(g, sca, g + 1 < ngroups ? xp.out_blocks : 0))) return fail(rc);
                 chk(cudaEventRecord(hp.out_free[b], hp.d2h) == cudaSuccess);
             }
             chk(cudaEventRecord(hp.d2h_done, hp.d2h) == cudaSuccess);
@@ -326,6 +335,15 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
 
     const size_t rows = (size_t)s.bs * s.L;
     const size_t row_q = (size_t)s.hd * s.es;  // bytes of one (token, head) row
+    auto fail = [&](int code) {  // as in the direct path: the caller's stream after all queued work
+        cudaEventRecord(hp.in_ready[0], hp.h2d);
+        cudaStreamWaitEvent(user, hp.in_ready[0], 0);
+        cudaEventRecord(hp.comp_done, hp.comp);
+        cudaStreamWaitEvent(user, hp.comp_done, 0);
+        cudaEventRecord(hp.d2h_done, hp.d2h);
+        cudaStreamWaitEvent(user, hp.d2h_done, 0);
+        return code;
+    };
     chk(cudaEventRecord(hp.start, user) == cudaSuccess);
     chk(cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess);
     chk(cudaStreamWaitEvent(hp.comp, hp.start, 0) == cudaSuccess);
@@ -350,17 +368,17 @@ int usp_forward_host(const void *q_host, const void *k_host, const void *v_host,
         void *dsts[3] = {qh, kh, vh};
         usp_dims dd[3] = {dims_of(s, s.hc, s.hc, 0, s.hd, d.dtype), dims_of(s, s.hkc, s.hkc, 0, s.hd, d.dtype),
                           dims_of(s, s.hkc, s.hkc, 0, s.hd, d.dtype)};
-        if ((rc = usp_extract_a2a(3, srcs, dsts, dd, 0, cs))) return rc;
+        if ((rc = usp_extract_a2a(3, srcs, dsts, dd, 0, cs))) return fail(rc);
         chk(cudaEventRecord(hp.in_free[sl], hp.comp) == cudaSuccess);
         usp_attn_desc ad = d;
         ad.hq = s.hc;
         ad.hkv = s.hkc;
-        if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, cs))) return rc;
+        if ((rc = usp_attn_fwd(qh, kh, vh, oh, lh, ad, cs))) return fail(rc);
         if (g >= 2) chk(cudaStreamWaitEvent(hp.comp, hp.out_free[sl], 0) == cudaSuccess);
         const void *os[2] = {oh, lh};
         void *od[2] = {out_o[sl], lse_all};
         usp_dims odims[2] = {dims_of(s, s.hc, s.hc, 0, s.hd, d.dtype), dims_of(s, s.hc, s.hq, g0, 1, USP_F32)};
-        if ((rc = usp_extract_a2a(2, os, od, odims, 1, cs))) return rc;
+        if ((rc = usp_extract_a2a(2, os, od, odims, 1, cs))) return fail(rc);
         chk(cudaEventRecord(hp.out_ready[sl], hp.comp) == cudaSuccess);
         // device -> host: this group's output window
         chk(cudaStreamWaitEvent(hp.d2h, hp.out_ready[sl], 0) == cudaSuccess);
