@@ -9,7 +9,8 @@
 // single ring step and write its partial, or merge it into (out, lse) in the epilogue.
 //
 // Kernel design. A unit of work is 256 query rows = two 128-row Q tiles of one (r, u, h, b). The
-// kernel is persistent: one CTA per SM walks a static list of units, and its roles run through the
+// kernel is persistent: one CTA per SM (or on fewer SMs, when a caller keeps some free for another
+// stream's kernels) walks a static list of units, and its roles run through the
 // units without a CTA-wide barrier, so one unit's epilogue overlaps the next unit's Q / K loads and
 // first S products. Units are numbered by cost, heaviest first, or in super-groups of heads whose
 // directions alternate (see decode_work), and round k of gridDim.x units goes to the CTAs in order for
@@ -1129,7 +1130,8 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     p.sg = grouped ? (uint32_t)std::min<uint64_t>(p.ngroups, std::max<uint64_t>(1, kSuperGroupKV / kv_group))
                    : p.ngroups;
     p.sg_flip = ((p.ngroups + p.sg - 1) / p.sg - 1) & 1u;
-    // persistent: one CTA per SM (the shared-memory footprint allows one), each walking its units
+    // persistent: one CTA per SM (the shared-memory footprint allows one), each walking its units;
+    // max_ctas leaves the remaining SMs to other kernels (usp_forward_host's concurrent transfers)
     const int ctas = a.max_ctas > 0 ? std::min(a.max_ctas, di->sm_count) : di->sm_count;
     const uint32_t grid = (uint32_t)std::min<uint64_t>(units, (uint64_t)std::max(ctas, 1));
     // packed samples run a separate instantiation, so the one-sample kernel carries none of their code
